@@ -1,0 +1,293 @@
+"""Pins of the float64 oracle against what the pages and the mathematics fix.
+
+Each ``pin_*`` function takes a loaded oracle library and raises ``AssertionError`` when the
+oracle disagrees. None of them re-calls the oracle to produce its own expected values: the
+expectations come from closed forms, hand-worked examples, a separately written brute-force
+sum or real-arithmetic loop, or invariants that hold exactly. ``test_oracle_pins.py`` runs
+them on the real oracle; ``test_oracle_mutants.py`` runs them on copies of the oracle with a
+planted mistake and checks that every planted mistake is caught.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def rel_err(a, b) -> float:
+    a = np.asarray(a)
+    b = np.asarray(b)
+    scale = max(float(np.max(np.abs(b))), 1e-300)
+    return float(np.max(np.abs(a - b))) / scale
+
+
+def random_case(rng, B, L, D, N, mode, dt_range=(1e-2, 0.5), theta_max=1.0):
+    """Small random inputs in float64 (the oracle takes any float64 values)."""
+    return dict(
+        x=rng.standard_normal((B, L, D)),
+        delta=np.exp(rng.uniform(math.log(dt_range[0]), math.log(dt_range[1]), (B, L, D))),
+        A=-np.exp(rng.uniform(0.0, math.log(8.0), (D, N))),
+        Bc=rng.standard_normal((B, L, N)) * 0.5 + 1j * rng.standard_normal((B, L, N)) * 0.5,
+        Cc=rng.standard_normal((B, L, N)) * 0.5 + 1j * rng.standard_normal((B, L, N)) * 0.5,
+        theta=rng.uniform(-theta_max, theta_max, (B, L, N)),
+        lam=1.0 / (1.0 + np.exp(-rng.standard_normal((B, L)))) if mode == 1 else None,
+        Dskip=rng.standard_normal(D),
+    )
+
+
+def run(lib, c, mode, **kw):
+    return oracle.forward(c["x"], c["delta"], c["A"], c["Bc"], c["Cc"], c["theta"], c["lam"], c["Dskip"],
+                          mode, lib=lib, **kw)
+
+
+# ----------------------------------------------------------------------------------------
+def pin_combine_associative(lib):
+    """(O3 (x) O2) (x) O1 == O3 (x) (O2 (x) O1) on random complex triples ("Complex parallel
+    scan", section 并行扫描的数学本质: the combine is associative, also for complex values)."""
+    rng = np.random.default_rng(11)
+    worst = 0.0
+    for _ in range(2000):
+        ops = [(complex(*rng.standard_normal(2)), complex(*rng.standard_normal(2))) for _ in range(3)]
+        o3, o2, o1 = ops
+        left = oracle.combine(oracle.combine(o3, o2, lib), o1, lib)
+        right = oracle.combine(o3, oracle.combine(o2, o1, lib), lib)
+        scale = max(1.0, abs(left[0]), abs(left[1]))
+        worst = max(worst, abs(left[0] - right[0]) / scale, abs(left[1] - right[1]) / scale)
+    assert worst <= 1e-14, worst
+
+
+def pin_combine_is_composition(lib):
+    """Folding the combine over O_0..O_{L-1} and applying the result once equals applying the
+    operators one after another; and the combined operator's multiplier is the product of the
+    a_t. Checked against plain complex arithmetic of the step h -> a h + u."""
+    rng = np.random.default_rng(12)
+    for _ in range(20):
+        L = 40
+        a = (rng.uniform(0.5, 1.0, L) * np.exp(1j * rng.uniform(-3, 3, L)))
+        u = rng.standard_normal(L) + 1j * rng.standard_normal(L)
+        h0 = complex(*rng.standard_normal(2))
+        h = h0
+        for t in range(L):
+            h = a[t] * h + u[t]
+        acc = (complex(a[0]), complex(u[0]))
+        for t in range(1, L):
+            acc = oracle.combine((complex(a[t]), complex(u[t])), acc, lib)
+        assert abs(acc[0] - np.prod(a)) <= 1e-13 * max(1.0, abs(np.prod(a)))
+        got = oracle.apply(acc, h0, lib)
+        assert abs(got - h) <= 1e-12 * max(1.0, abs(h)), (got, h)
+
+
+def _bruteforce_y(c, mode):
+    """y_t = sum_{s<=t} Re(C_t prod_{k=s+1..t} a_k u_s) + D x_t by explicit products."""
+    x, dt, A, Bc, Cc, th, lam, Ds = (c[k] for k in ("x", "delta", "A", "Bc", "Cc", "theta", "lam", "Dskip"))
+    B, L, D = x.shape
+    N = A.shape[1]
+    y = np.zeros((B, L, D))
+    for b in range(B):
+        for d in range(D):
+            for n in range(N):
+                a = np.exp(dt[b, :, d] * A[d, n] + 1j * th[b, :, n])
+                if mode == 0:
+                    u = dt[b, :, d] * x[b, :, d] * Bc[b, :, n]
+                else:
+                    u = lam[b] * dt[b, :, d] * x[b, :, d] * Bc[b, :, n]
+                    u[1:] += (1 - lam[b, 1:]) * dt[b, 1:, d] * a[1:] * x[b, :-1, d] * Bc[b, :-1, n]
+                for t in range(L):
+                    for s in range(t + 1):
+                        prod = 1.0 + 0j
+                        for k in range(s + 1, t + 1):
+                            prod *= a[k]
+                        y[b, t, d] += (Cc[b, t, n] * prod * u[s]).real
+            y[b, :, d] += Ds[d] * x[b, :, d]
+    return y
+
+
+def pin_bruteforce(lib):
+    """The recurrence against the unrolled double sum on tiny inputs, both modes."""
+    rng = np.random.default_rng(13)
+    for mode in (0, 1):
+        c = random_case(rng, 2, 10, 3, 4, mode)
+        y = run(lib, c, mode)
+        assert rel_err(y, _bruteforce_y(c, mode)) <= 1e-12
+
+
+def pin_closed_form(lib):
+    """Constant dt, theta, Bc, x (and lam): h_t is a geometric series.
+    mode 0: h_t = w (1 - a^{t+1}) / (1 - a);
+    mode 1: h_t = w [lam (1 - a^{t+1}) + (1 - lam) a (1 - a^t)] / (1 - a), with w = dt Bc x."""
+    rng = np.random.default_rng(14)
+    B, L, D, N = 1, 200, 2, 3
+    for mode in (0, 1):
+        dt = np.array([0.05, 0.3])
+        xv = np.array([0.7, -1.3])
+        A = -np.array([[0.5, 1.0, 2.0], [0.2, 3.0, 0.9]])
+        th = np.array([0.3, -1.1, 2.0])
+        Bv = np.array([0.4 - 0.2j, -0.6 + 0.1j, 0.3 + 0.8j])
+        Cv = np.array([1.0 + 0.5j, -0.2 + 0.3j, 0.6 - 0.9j])
+        lam = 0.37
+        c = dict(x=np.broadcast_to(xv, (B, L, D)).copy(), delta=np.broadcast_to(dt, (B, L, D)).copy(), A=A,
+                 Bc=np.broadcast_to(Bv, (B, L, N)).copy(), Cc=np.broadcast_to(Cv, (B, L, N)).copy(),
+                 theta=np.broadcast_to(th, (B, L, N)).copy(),
+                 lam=np.full((B, L), lam) if mode == 1 else None, Dskip=np.array([0.25, -1.5]))
+        y, traj = run(lib, c, mode, want_traj=True)
+        t = np.arange(L)[:, None, None]
+        a = np.exp(dt[None, :, None] * A[None] + 1j * th[None, None, :])   # (1, D, N)
+        w = (dt * xv)[None, :, None] * Bv[None, None, :]
+        if mode == 0:
+            h = w * (1 - a ** (t + 1)) / (1 - a)
+        else:
+            h = w * (lam * (1 - a ** (t + 1)) + (1 - lam) * a * (1 - a ** t)) / (1 - a)
+        assert rel_err(traj[0], h) <= 1e-12
+        y_ref = (Cv[None, None, :] * h).real.sum(-1) + np.array([0.25, -1.5]) * xv
+        assert rel_err(y[0], y_ref) <= 1e-12
+
+
+def pin_real_reduction(lib):
+    """theta = 0 and real Bc, Cc give the real selective scan h = e^{dt A} h + dt B x,
+    y = sum_n C h + D x (and its trapezoidal form), computed here with a real loop."""
+    rng = np.random.default_rng(15)
+    for mode in (0, 1):
+        c = random_case(rng, 2, 30, 3, 5, mode)
+        c["theta"][:] = 0.0
+        c["Bc"] = c["Bc"].real.astype(np.complex128)
+        c["Cc"] = c["Cc"].real.astype(np.complex128)
+        y = run(lib, c, mode)
+        x, dt, A = c["x"], c["delta"], c["A"]
+        Br, Cr = c["Bc"].real, c["Cc"].real
+        B, L, D = x.shape
+        yr = np.zeros_like(x)
+        h = np.zeros((B, D, A.shape[1]))
+        for t in range(L):
+            abar = np.exp(dt[:, t, :, None] * A[None])
+            inj = dt[:, t, :, None] * x[:, t, :, None] * Br[:, t, None, :]
+            if mode == 1:
+                lam = c["lam"][:, t, None, None]
+                inj = lam * inj
+                if t > 0:
+                    inj = inj + (1 - lam) * dt[:, t, :, None] * abar * x[:, t - 1, :, None] * Br[:, t - 1, None, :]
+            h = abar * h + inj
+            yr[:, t, :] = (Cr[:, t, None, :] * h).sum(-1) + c["Dskip"][None, :] * x[:, t, :]
+        assert rel_err(y, yr) <= 1e-13
+
+
+def pin_rotation(lib):
+    """A = 0 and x_t = 0 after the first input: the state only rotates, |h_t| stays fixed and
+    h_t = e^{i sum theta} h_first, over 10^4 steps."""
+    rng = np.random.default_rng(16)
+    L = 10000
+    for mode in (0, 1):
+        c = random_case(rng, 1, L, 1, 2, mode)
+        c["A"][:] = 0.0
+        c["x"][:, 1:, :] = 0.0
+        y, traj = run(lib, c, mode, want_traj=True)
+        h = traj[0, :, 0, :]            # (L, N)
+        first = 0 if mode == 0 else 1   # mode 1 injects x_0 again at t = 1
+        dt0, x0, B0 = c["delta"][0, 0, 0], c["x"][0, 0, 0], c["Bc"][0, 0]
+        if mode == 0:
+            h_first = dt0 * x0 * B0
+        else:
+            lam = c["lam"][0]
+            a1 = np.exp(1j * c["theta"][0, 1])
+            h_first = a1 * (lam[0] * dt0 * x0 * B0) + (1 - lam[1]) * c["delta"][0, 1, 0] * a1 * x0 * B0
+        phase = np.cumsum(c["theta"][0, first + 1:], axis=0)
+        expect = h_first[None, :] * np.exp(1j * phase)
+        assert rel_err(np.abs(h[first:]), np.broadcast_to(np.abs(h_first), h[first:].shape)) <= 1e-12
+        assert rel_err(h[first], h_first) <= 1e-13
+        assert rel_err(h[first + 1:], expect) <= 1e-11
+
+
+def pin_lambda_one(lib):
+    """Trapezoid with lam = 1 is exp-Euler (beta = 0, gamma = dt)."""
+    rng = np.random.default_rng(17)
+    c = random_case(rng, 2, 50, 3, 4, 1)
+    c["lam"][:] = 1.0
+    y1 = run(lib, c, 1)
+    y0 = run(lib, c, 0)
+    assert np.array_equal(y1, y0)
+
+
+def pin_linearity_and_causality(lib):
+    """y is linear in x for fixed dt, Bc, Cc, theta, lam; y_t does not depend on inputs after t."""
+    rng = np.random.default_rng(18)
+    for mode in (0, 1):
+        c1 = random_case(rng, 1, 40, 2, 3, mode)
+        c2 = dict(c1)
+        c2["x"] = rng.standard_normal(c1["x"].shape)
+        c3 = dict(c1)
+        c3["x"] = c1["x"] + 2.5 * c2["x"]
+        y1, y2, y3 = run(lib, c1, mode), run(lib, c2, mode), run(lib, c3, mode)
+        assert rel_err(y3, y1 + 2.5 * y2) <= 1e-12
+        s = 23
+        for key in ("x", "delta", "Bc", "theta"):
+            cp = dict(c1)
+            cp[key] = c1[key].copy()
+            cp[key][:, s] += 0.75
+            yp = run(lib, cp, mode)
+            assert np.array_equal(yp[:, :s], y1[:, :s]), key
+            assert np.max(np.abs(yp[:, s] - y1[:, s])) > 1e-6, key
+        cp = dict(c1)
+        cp["Cc"] = c1["Cc"].copy()
+        cp["Cc"][:, s] += 0.75
+        yp = run(lib, cp, mode)
+        assert np.array_equal(yp[:, :s], y1[:, :s]) and np.array_equal(yp[:, s + 1:], y1[:, s + 1:])
+
+
+def pin_split_invariance(lib):
+    """Running [0, t0) and then [t0, L) from the carried state (and, in the trapezoid mode,
+    step t0-1's x and Bc as the halo) equals one run over [0, L)."""
+    rng = np.random.default_rng(19)
+    for mode in (0, 1):
+        c = random_case(rng, 2, 64, 3, 4, mode)
+        y_full, h_full = run(lib, c, mode, want_h_last=True)
+        for t0 in (1, 17, 63):
+            head = {k: (v[:, :t0] if k in ("x", "delta", "Bc", "Cc", "theta", "lam") and v is not None else v)
+                    for k, v in c.items()}
+            tail = {k: (v[:, t0:] if k in ("x", "delta", "Bc", "Cc", "theta", "lam") and v is not None else v)
+                    for k, v in c.items()}
+            y_head, h_mid = run(lib, head, mode, want_h_last=True)
+            y_tail, h_end = run(lib, tail, mode, want_h_last=True, h0=h_mid,
+                                x_prev=c["x"][:, t0 - 1], Bc_prev=c["Bc"][:, t0 - 1])
+            assert rel_err(np.concatenate([y_head, y_tail], axis=1), y_full) <= 1e-13
+            assert rel_err(h_end, h_full) <= 1e-13
+
+
+def load_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN_DIR, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.split()
+    mode = int(vals["mode"][0])
+    B, L, D, N = (int(s) for s in vals["shape"])
+    num = lambda key: np.array([float(s) for s in vals[key]])
+    cpx = lambda key: np.array([complex(float(s.split(",")[0]), float(s.split(",")[1])) for s in vals[key]])
+    c = dict(
+        x=num("x").reshape(B, L, D), delta=num("dt").reshape(B, L, D), A=num("A").reshape(D, N),
+        theta=np.stack([num(f"theta_n{n}") for n in range(N)], -1).reshape(B, L, N),
+        Bc=np.stack([cpx(f"Bc_n{n}") for n in range(N)], -1).reshape(B, L, N),
+        Cc=np.stack([cpx(f"Cc_n{n}") for n in range(N)], -1).reshape(B, L, N),
+        Dskip=num("Dskip"),
+        lam=None if vals["lam"][0] == "none" else num("lam").reshape(B, L),
+    )
+    return mode, c, num("y").reshape(B, L, D)
+
+
+def pin_golden(lib):
+    """The hand-worked examples under tests/golden/."""
+    for name in ("worked_example_exp_euler.txt", "worked_example_exp_trapezoid.txt"):
+        mode, c, y_expect = load_golden(name)
+        y = run(lib, c, mode)
+        assert np.max(np.abs(y - y_expect)) <= 1e-12, (name, y, y_expect)
+
+
+ALL_PINS = [pin_combine_associative, pin_combine_is_composition, pin_bruteforce, pin_closed_form,
+            pin_real_reduction, pin_rotation, pin_lambda_one, pin_linearity_and_causality,
+            pin_split_invariance, pin_golden]

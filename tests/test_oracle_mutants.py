@@ -1,0 +1,86 @@
+"""Plants plausible mistakes in copies of the oracle and checks the pins catch every one.
+
+A pin set that passes on the oracle says little unless it would fail on a wrong oracle.
+Each case below rewrites one snippet of ``oracle/oracle.c`` in a temporary copy (a dropped
+term, a wrong sign, index or conjugation, a transposed operand), compiles it, and runs all
+pins from ``pins.py`` against it: at least one must fail. CPU only; the real oracle file is
+never modified.
+"""
+import os
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import pins
+
+MUTANTS = [
+    ("rotation conjugated", "cexp(dt * A + I * theta)", "cexp(dt * A - I * theta)"),
+    ("dt dropped from the decay", "cexp(dt * A + I * theta)", "cexp(A + I * theta)"),
+    ("theta scaled by dt", "cexp(dt * A + I * theta)", "cexp(dt * A + I * dt * theta)"),
+    ("rotation as a cosine factor", "cexp(dt * A + I * theta)", "exp(dt * A) * cos(theta)"),
+    ("exp-Euler gamma dropped", "double gamma = dt;", "double gamma = 1.0;"),
+    ("beta without a_t", "cplx beta = (1.0 - lam) * dt * a;", "cplx beta = (1.0 - lam) * dt;"),
+    ("beta weighted by lam", "cplx beta = (1.0 - lam) * dt * a;", "cplx beta = lam * dt * a;"),
+    ("beta with conj(a_t)", "cplx beta = (1.0 - lam) * dt * a;", "cplx beta = (1.0 - lam) * dt * conj(a);"),
+    ("gamma without lam", "double gamma = lam * dt;", "double gamma = dt;"),
+    ("trapezoid halo term dropped", "u = beta * v_prev + gamma * v;", "u = gamma * v;"),
+    ("y conjugates C", "acc += creal(load_c(j->Cc, tn) * h[n]);",
+     "acc += creal(conj(load_c(j->Cc, tn)) * h[n]);"),
+    ("y reads the imaginary part", "acc += creal(load_c(j->Cc, tn) * h[n]);",
+     "acc += cimag(load_c(j->Cc, tn) * h[n]);"),
+    ("y from the pre-update state",
+     "h[n] = (op[0] + I * op[1]) * h[n] + (op[2] + I * op[3]);\n      acc += creal(load_c(j->Cc, tn) * h[n]);",
+     "acc += creal(load_c(j->Cc, tn) * h[n]);\n      h[n] = (op[0] + I * op[1]) * h[n] + (op[2] + I * op[3]);"),
+    ("D-skip dropped", "j->y[td] = acc + j->Dskip[d] * xt;", "j->y[td] = acc;"),
+    ("D-skip on the previous x", "j->y[td] = acc + j->Dskip[d] * xt;", "j->y[td] = acc + j->Dskip[d] * x_prev;"),
+    ("x_{t-1} read at t", "if (t > 0) x_prev = j->x[td - D];", "if (t > 0) x_prev = j->x[td];"),
+    ("Bc_{t-1} read at t",
+     "B_prev[0] = j->Bc[2 * (tn - N)]; B_prev[1] = j->Bc[2 * (tn - N) + 1];",
+     "B_prev[0] = j->Bc[2 * tn]; B_prev[1] = j->Bc[2 * tn + 1];"),
+    ("injection subtracted", "h[n] = (op[0] + I * op[1]) * h[n] + (op[2] + I * op[3]);",
+     "h[n] = (op[0] + I * op[1]) * h[n] - (op[2] + I * op[3]);"),
+    ("decay dropped from the update", "h[n] = (op[0] + I * op[1]) * h[n] + (op[2] + I * op[3]);",
+     "h[n] = h[n] + (op[2] + I * op[3]);"),
+    ("A transposed", "j->A[d * N + n]", "j->A[n * D + d]"),
+    ("combine operands swapped", "cplx a = a2 * a1, u = a2 * u1 + u2;", "cplx a = a2 * a1, u = a1 * u2 + u1;"),
+    ("combine drops the multiplier", "cplx a = a2 * a1, u = a2 * u1 + u2;", "cplx a = a2 * a1, u = u1 + u2;"),
+    ("initial state ignored", "h[n] = j->h0 ? load_c(j->h0, (b * D + d) * N + n) : 0.0;", "h[n] = 0.0;"),
+    ("halo x ignored", "else if (j->x_prev) x_prev = j->x_prev[b * D + d];", "else if (j->x_prev) x_prev = 0.0;"),
+    ("apply drops the multiplier", "cplx r = a * hh + u;", "cplx r = hh + u;"),
+]
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    d = tempfile.mkdtemp(prefix="oracle_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+def test_mutant_snippets_present():
+    src = open(oracle.SOURCE).read()
+    for name, old, _ in MUTANTS:
+        assert src.count(old) >= 1, f"snippet for mutant '{name}' no longer in oracle.c"
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(workdir, name, old, new):
+    src = open(oracle.SOURCE).read()
+    assert old in src
+    tag = "".join(ch if ch.isalnum() else "_" for ch in name)
+    c_path = os.path.join(workdir, f"{tag}.c")
+    so_path = os.path.join(workdir, f"lib{tag}.so")
+    with open(c_path, "w") as f:
+        f.write(src.replace(old, new))
+    oracle.build(c_path, so_path)
+    lib = oracle.load(so_path)
+    caught = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, RuntimeError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin catches the planted mistake '{name}'"
