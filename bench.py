@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark: forward selective scan of the diagonal complex recurrence on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one full forward pass (rotation tables + scan, every output written) over one
+batch of synthetic inputs already resident in device memory. Prints ONE JSON line (rank 0).
+
+Default workload: the large-batch exp-trapezoidal scan, B=16 L=8192 D=2560 N=16, bf16
+inputs, float32 arithmetic (2.71 GB of minimum traffic, far larger than the 126 MB L2, so no
+flush is needed between steps; smaller workloads are flushed and timed step by step).
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent
+problems, no data-path collective): weak scaling, value = all ranks' elements / max time.
+
+--impl reference times the float64 CPU oracle (the correctness reference) on a bounded
+sample of the same workload on the host cores, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_diagonal_b300 import workloads as wl  # noqa: E402
+
+METRIC = "selective-scan Gelem/s (B·L·D·N) and HBM GB/s as % of B300 peak, 1 GPU"
+UNIT = "Gelem/s"
+DEFAULT_WORKLOAD = "trap_bf16_batch"
+L2_BYTES = 126 * 1024 * 1024
+# FP32 pipe lane-operations per scanned element in this implementation's formulation: one
+# multiply for the decay exponent, four for the complex decay-and-inject update, two for the
+# real part of C h (plus one MUFU ex2 on its own pipe).
+ALU_OPS_PER_ELEM = 7
+FP32_LANES_PER_SM = 128
+N_SM = 148
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS))
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the CPU-baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("sm_max_mhz", 2032.0)), "measured"
+    except Exception:
+        return 6400.0, 2032.0, "fallback"
+
+
+# ------------------------------------------------------------------------------ ranks
+def rank_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(value: float, group=None) -> float:
+    """Max of a scalar over all ranks (a timing reduction, not part of the data path)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def aggregate_value(elements_per_rank_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Whole-job Gelem/s: every rank's elements over the slowest rank's time."""
+    return elements_per_rank_step * steps * world / max_seconds / 1e9
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML (read-only) while running."""
+
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples = []
+        self.period = period_s
+        self._stop = threading.Event()
+        self._t = None
+        self.max_mhz = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nvml = pynvml
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            idx = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() else device_index
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(idx)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self.nvml = None
+
+    def _run(self):
+        nv = self.nvml
+        while not self._stop.is_set():
+            try:
+                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+                self.samples.append((mhz, reasons, pw))
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.nvml:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._t:
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
+        reasons = set()
+        for _, r, _ in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples),
+                "power_w_max": max(s[2] for s in self.samples)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(inp: wl.Inputs, target_s: float, nthreads: int = 0):
+    """Times the float64 oracle on a prefix of batch 0's channels (all L steps, all N states),
+    sized to about target_s seconds. Returns (Gelem/s, threads, description, seconds)."""
+    import oracle
+    w = inp.workload
+    lib = oracle.load()
+    threads = oracle.last_thread_count(nthreads)
+
+    def run(nd):
+        f = wl.widen(inp, b=slice(0, 1), d=np.arange(nd))
+        t0 = time.perf_counter()
+        oracle.forward(f["x"], f["delta"], f["A"], f["Bc"], f["Cc"], f["theta"], f["lam"], f["Dskip"], w.mode,
+                       nthreads=nthreads, lib=lib)
+        return time.perf_counter() - t0
+
+    nd = min(w.D, threads)
+    dt = run(nd)
+    while dt < 0.5 and nd < w.D:
+        nd = min(w.D, nd * 4)
+        dt = run(nd)
+    nd_final = max(1, min(w.D, int(nd * target_s / max(dt, 1e-6))))
+    if nd_final != nd:
+        dt = run(nd_final)
+        nd = nd_final
+    elems = w.L * nd * w.N
+    desc = f"batch 0, channels 0..{nd - 1} of {w.D}, all {w.L} steps and {w.N} states ({elems:.3e} elements)"
+    return elems / dt / 1e9, oracle.last_thread_count(nthreads, rows=nd), desc, dt
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return 0
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.generate(w)
+    per_step = max(1.0, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
+    value, cores, desc, _ = cpu_oracle_sample(inp, per_step)
+    import oracle
+    lib = oracle.load()
+    nd = int(desc.split("channels 0..")[1].split(" ")[0]) + 1
+    f = wl.widen(inp, b=slice(0, 1), d=np.arange(nd))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(f["x"], f["delta"], f["A"], f["Bc"], f["Cc"], f["theta"], f["lam"], f["Dskip"], w.mode,
+                       lib=lib)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    elems = w.L * nd * w.N
+    total = sum(times)
+    v = elems * len(times) / total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w: wl.Workload, l2_note: str = ""):
+    cfg = {"workload": w.name, "B": w.B, "L": w.L, "D": w.D, "N": w.N,
+           "mode": "exp-trapezoidal" if w.mode == 1 else "exp-Euler", "input_dtype": w.dtype,
+           "elements": w.elements, "min_bytes": w.min_bytes()}
+    if l2_note:
+        cfg["l2"] = l2_note
+    return cfg
+
+
+# ------------------------------------------------------------------------------ our arm
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from selective_state_space_diagonal_b300 import csscan
+
+    rank, world, local = rank_info()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    csscan.load_library()
+    w = wl.WORKLOADS[args.workload]
+    inp = wl.generate(w)
+
+    def pinned(a):
+        if a is None:
+            return None
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        t = t.pin_memory()
+        return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
+
+    keys = ("x", "delta", "A", "Bc", "Cc", "theta", "lam", "Dskip")
+    host = {k: pinned(getattr(inp, k)) for k in keys}
+    dev = {k: (None if v is None else v.to("cuda", non_blocking=True)) for k, v in host.items()}
+    y = torch.empty((w.B, w.L, w.D), dtype=torch.float32, device="cuda")
+    y_host = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(sb=None, se=None):
+        rc = csscan.csscan_forward_ex(dev["x"], dev["delta"], dev["A"], dev["Bc"], dev["Cc"], dev["theta"],
+                                      dev["lam"], dev["Dskip"], y, w.mode, stream=stream, scan_begin=sb, scan_end=se)
+        if rc != csscan.CSSCAN_OK:
+            raise RuntimeError(csscan.csscan_status_string(rc))
+
+    footprint = w.min_bytes()
+    flush = footprint < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
+    l2_note = ("L2 flushed (a 252 MB write) before every step; steps timed individually"
+               if flush else f"inputs larger than L2 ({footprint / 1e9:.2f} GB minimum traffic per step), no flush")
+
+    for _ in range(args.warmup):
+        if flush:
+            scratch.zero_()
+        step()
+    torch.cuda.synchronize()
+    st = csscan.csscan_get_device_status(stream)
+    if st != csscan.CSSCAN_OK:
+        raise RuntimeError("device status after warm-up: " + csscan.csscan_status_string(st))
+
+    K = args.steps
+    sb = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    se = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)] if flush else None
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        ev0.record(stream)
+        for i in range(K):
+            if flush:
+                scratch.zero_()
+                step_ev[i][0].record(stream)
+            step(sb[i], se[i])
+            if flush:
+                step_ev[i][1].record(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    if flush:
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
+    else:
+        elapsed_ms = ev0.elapsed_time(ev1)
+    scan_ms = [a.elapsed_time(b) for a, b in zip(sb, se)]
+    st = csscan.csscan_get_device_status(stream)
+    if st != csscan.CSSCAN_OK:
+        raise RuntimeError("device status after timed steps: " + csscan.csscan_status_string(st))
+    max_s = reduce_max(elapsed_ms / 1e3)
+    value = aggregate_value(w.elements, K, world, max_s)
+
+    # end to end through the public API: pinned host inputs -> device, scan, y -> host
+    e2e_steps = max(1, args.e2e_steps)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = y.numel() * 4
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for k in keys:
+            if host[k] is not None:
+                dev[k].copy_(host[k], non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    e2e_s = reduce_max(time.perf_counter() - t0)
+    e2e_value = aggregate_value(w.elements, e2e_steps, world, e2e_s)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    hbm_peak, sm_max_mhz, peak_kind = measured_peaks()
+    scan_mean_s = statistics.mean(scan_ms) / 1e3
+    clk = clocks.summary()
+    alu_peak = FP32_LANES_PER_SM * N_SM * sm_max_mhz * 1e6 / 1e12           # T lane-ops/s
+    alu_achieved = ALU_OPS_PER_ELEM * w.elements / scan_mean_s / 1e12
+    hbm_achieved = w.min_bytes() / scan_mean_s / 1e9
+    traffic = traffic_from_profiles(w.name)
+    roofline = {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak, "unit": "Tops/s",
+                "frac": alu_achieved / alu_peak, "traffic": traffic,
+                "kernel": "scan_kernel", "ms_per_launch": 1e3 * scan_mean_s,
+                "peak_note": f"FP32 pipe: {FP32_LANES_PER_SM} lanes/SM x {N_SM} SMs x {sm_max_mhz:.0f} MHz; "
+                             f"{ALU_OPS_PER_ELEM} lane-ops per element"}
+    hbm = {"achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s", "frac": hbm_achieved / hbm_peak,
+           "peak_kind": peak_kind, "whole_step_gbs": w.min_bytes() * K / (elapsed_ms / 1e3) / 1e9}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, cores, desc, secs = cpu_oracle_sample(inp, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "seconds": secs}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": workload_config(w, l2_note),
+            "roofline": roofline, "hbm": hbm, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": 2 * K, "clocks": clk}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def traffic_from_profiles(workload: str):
+    """DRAM bytes per scan-kernel launch from the committed ncu summary of this workload, if
+    one exists for the current kernel (profiles/<kernel>_<workload>.json)."""
+    path = os.path.join(ROOT, "profiles", f"scan_kernel_{workload}.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,145 @@
+/*
+ * csscan.h -- C ABI of the forward selective scan of a diagonal, complex-valued,
+ * input-dependent linear recurrence, on one NVIDIA B300 (sm_103a).
+ *
+ * What it computes. Per batch b, channel d and state n, starting from a zero state:
+ *
+ *   a_t      = exp(dt[b,t,d] * A[d,n] + i * theta[b,t,n])
+ *   exp-Euler         h_t = a_t h_{t-1} + dt_t Bc[b,t,n] x[b,t,d]
+ *   exp-trapezoidal   h_t = a_t h_{t-1} + (1 - lam_t) dt_t a_t Bc[b,t-1,n] x[b,t-1,d]
+ *                                       + lam_t dt_t Bc[b,t,n] x[b,t,d],  with Bc_{-1} x_{-1} = 0
+ *   y[b,t,d] = Re(sum_n Cc[b,t,n] h_t[n]) + Dskip[d] x[b,t,d]
+ *
+ * Sources (pages of the reference material, by title and section):
+ *   - "Complex parallel scan" (fengwang.github.io), section 并行扫描的数学本质: the step
+ *     h_t = A_t h_{t-1} + B_t x_t as an operator, its associative combine, and its validity
+ *     for complex coefficients (the basis of the chunked carry used inside);
+ *   - "Mamba-3 paper story" (ai.tomabc.com): the discretisation table (Exp-Euler row:
+ *     alpha = exp(dt A), gamma = dt; Exp-Trapezoidal row: beta = (1 - lam) dt exp(dt A),
+ *     gamma = lam dt) and the complex-state section (real decay A, input-dependent phase
+ *     e^{i theta});
+ *   - "状态空间模型的对偶谱理论 2026" (blog.lonae.com), section 3.1: the sequential loop, y read
+ *     from the updated state and summed over the state index;
+ *   - "Mamba-3: 选择性状态空间模型的下一代架构" (metaphor-xennon), section 2.2: y = C h + D x.
+ *   The exponential in beta is read as the full complex a_t of the current step, and theta
+ *   is not scaled by dt.
+ *
+ * Layout (every tensor contiguous, row-major, last index fastest; complex values stored
+ * interleaved (re, im) in a trailing dimension of 2):
+ *   x, delta        (B, L, D)      input dtype
+ *   Bc, Cc          (B, L, N, 2)   input dtype
+ *   theta           (B, L, N)      input dtype
+ *   lambda          (B, L)         input dtype (trapezoid mode only)
+ *   A               (D, N)         float32, real (one decay per channel and state)
+ *   Dskip           (D)            float32
+ *   y               (B, L, D)      float32 output
+ * The input dtype is float32 or bf16 (CSSCAN_F32 / CSSCAN_BF16). Arithmetic is float32 with
+ * the complex state held in registers; the (B, L, D, N) state never reaches device memory.
+ *
+ * Ownership. Every pointer is caller-owned DEVICE memory of the current CUDA device; the
+ * library never frees it. The library owns one internal workspace per (device, stream)
+ * that it grows with cudaMalloc on first use and when a larger problem arrives (the first
+ * call on a stream must therefore not be inside a stream capture); csscan_release_workspace
+ * frees all of them.
+ *
+ * Asynchrony. Calls enqueue work on `stream` (0 = the legacy default stream) and return; y
+ * is valid once the stream reaches that point. Calls on one stream are ordered; calls on
+ * different streams use different workspaces and may overlap.
+ *
+ * Errors. Every function returns an int status (CSSCAN_OK = 0) and throws nothing. Argument
+ * checks run on the host before any launch, so a rejected call touches no device memory.
+ */
+#ifndef CSSCAN_H
+#define CSSCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  CSSCAN_OK = 0,
+  CSSCAN_ERR_INVALID_ARG = 1,      /* null pointer, negative size, N == 0, bad mode/dtype,
+                                      lambda == NULL in trapezoid mode, bad option */
+  CSSCAN_ERR_MISALIGNED = 2,       /* x or delta not 16-byte aligned, or D * sizeof(dtype) not a
+                                      multiple of 16 bytes (the tile copies need both) */
+  CSSCAN_ERR_UNSUPPORTED = 3,      /* N not in {2, 4, 8, 16, 32, 64}, or sizes beyond 2^31 */
+  CSSCAN_ERR_CUDA = 4,             /* a CUDA runtime/driver call or a launch failed */
+  CSSCAN_ERR_LOOKBACK_TIMEOUT = 5, /* device: a chunk waited past its limit for its
+                                      predecessor's carry (reported by csscan_get_device_status;
+                                      the outputs of that call are not valid) */
+  CSSCAN_ERR_PIPELINE_TIMEOUT = 6  /* device: a tile copy did not arrive within its limit */
+};
+
+typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1 } csscan_mode_t;
+typedef enum { CSSCAN_F32 = 0, CSSCAN_BF16 = 1 } csscan_dtype_t;
+
+/*
+ * Forward scan. Computes y from x, delta, A, Bc, Cc, theta, lambda and Dskip as above.
+ *   x, delta, Bc, Cc, theta, lambda : device pointers in `dtype`; lambda may be NULL in
+ *                                     exp-Euler mode and is required in trapezoid mode
+ *   A, Dskip                        : device float32
+ *   y                               : device float32, written in full (B*L*D values)
+ *   B, L, D, N                      : sizes; B, L or D == 0 is a no-op returning CSSCAN_OK
+ *   mode                            : csscan_mode_t
+ *   dtype                           : csscan_dtype_t
+ *   stream                          : CUDA stream to enqueue on
+ * Alignment: x and delta 16-byte aligned and D * sizeof(dtype) a multiple of 16 (D % 4 == 0
+ * for float32, D % 8 == 0 for bf16); other pointers need only their natural alignment.
+ */
+int csscan_forward(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                   const void* theta, const void* lambda, const float* Dskip, float* y,
+                   int64_t B, int64_t L, int64_t D, int64_t N, int mode, int dtype, cudaStream_t stream);
+
+/*
+ * Launch options for csscan_forward_ex. Zero-initialise and set only what you need.
+ *   rows_per_cta  : reserved, must be 0 (the row tile follows from N)
+ *   chunk_len     : sequence chunk per thread block (multiple of 32); 0 = automatic
+ *   carry         : 0 automatic, 1 serial (each chunk waits for its predecessor's final state),
+ *                   2 decoupled (each chunk first computes its own aggregate, then looks back)
+ *   silent_chunk  : test hook; -1 normally. Chunks with this index never publish their carry,
+ *                   so their successors run into the bounded wait and report
+ *                   CSSCAN_ERR_LOOKBACK_TIMEOUT through csscan_get_device_status
+ *   poll_limit    : maximum polls of one carry wait (about 0.5 us each); 0 = default (about 2 s)
+ *   scan_begin,
+ *   scan_end      : optional CUDA events (NULL = none), recorded on `stream` right before and
+ *                   right after the scan kernel, to time it apart from the small table kernel
+ */
+typedef struct {
+  int32_t rows_per_cta;
+  int32_t chunk_len;
+  int32_t carry;
+  int32_t silent_chunk;
+  int64_t poll_limit;
+  cudaEvent_t scan_begin;
+  cudaEvent_t scan_end;
+} csscan_options_t;
+
+/* csscan_forward with explicit launch options (opts may be NULL = automatic). */
+int csscan_forward_ex(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                      const void* theta, const void* lambda, const float* Dskip, float* y,
+                      int64_t B, int64_t L, int64_t D, int64_t N, int mode, int dtype,
+                      const csscan_options_t* opts, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the device-side status of the calls made on it since
+ * the last query (CSSCAN_OK, CSSCAN_ERR_LOOKBACK_TIMEOUT or CSSCAN_ERR_PIPELINE_TIMEOUT), or
+ * CSSCAN_ERR_CUDA if the stream reports an error. Clears the device status.
+ */
+int csscan_get_device_status(cudaStream_t stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* csscan_status_string(int status);
+
+/* Frees every internal workspace after synchronising its device. Returns CSSCAN_OK or
+ * CSSCAN_ERR_CUDA. Safe to call at any time outside stream capture. */
+int csscan_release_workspace(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSSCAN_H */

@@ -1,0 +1,132 @@
+"""Thin Python binding of the C ABI in ``include/csscan.h`` (``libcsscan.so``).
+
+Argument marshalling only: every step of the scan runs in the library's CUDA kernels. The
+functions take torch CUDA tensors (torch allocates device memory and supplies the stream)
+and pass their device pointers and sizes to the C entry points of the same names. There is
+no CPU fallback: if the library is missing or the GPU call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(_HERE, "libcsscan.so")
+
+CSSCAN_OK = 0
+CSSCAN_ERR_INVALID_ARG = 1
+CSSCAN_ERR_MISALIGNED = 2
+CSSCAN_ERR_UNSUPPORTED = 3
+CSSCAN_ERR_CUDA = 4
+CSSCAN_ERR_LOOKBACK_TIMEOUT = 5
+CSSCAN_ERR_PIPELINE_TIMEOUT = 6
+
+CSSCAN_MODE_EXP_EULER = 0
+CSSCAN_MODE_EXP_TRAPEZOID = 1
+CSSCAN_F32 = 0
+CSSCAN_BF16 = 1
+
+
+class CsscanError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where} failed: status {status} ({csscan_status_string(status)})")
+        self.status = status
+
+
+class csscan_options_t(ctypes.Structure):
+    _fields_ = [("rows_per_cta", ctypes.c_int32), ("chunk_len", ctypes.c_int32), ("carry", ctypes.c_int32),
+                ("silent_chunk", ctypes.c_int32), ("poll_limit", ctypes.c_int64),
+                ("scan_begin", ctypes.c_void_p), ("scan_end", ctypes.c_void_p)]
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIBRARY) -> ctypes.CDLL:
+    """Load ``libcsscan.so`` (built in-tree by ``build.py``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is not built; run selective_state_space_diagonal_b300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    fwd = [vp] * 9 + [i64] * 4 + [i32, i32]
+    lib.csscan_forward.argtypes = fwd + [vp]
+    lib.csscan_forward.restype = i32
+    lib.csscan_forward_ex.argtypes = fwd + [ctypes.POINTER(csscan_options_t), vp]
+    lib.csscan_forward_ex.restype = i32
+    lib.csscan_get_device_status.argtypes = [vp]
+    lib.csscan_get_device_status.restype = i32
+    lib.csscan_status_string.argtypes = [i32]
+    lib.csscan_status_string.restype = ctypes.c_char_p
+    lib.csscan_release_workspace.argtypes = []
+    lib.csscan_release_workspace.restype = i32
+    _lib = lib
+    return lib
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors must be contiguous CUDA tensors")
+    return t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return CSSCAN_F32
+    if t.dtype == torch.bfloat16:
+        return CSSCAN_BF16
+    raise ValueError(f"unsupported input dtype {t.dtype}")
+
+
+def _args(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode):
+    B, L, D = x.shape
+    N = A.shape[1]
+    return [_ptr(x), _ptr(delta), _ptr(A), _ptr(Bc), _ptr(Cc), _ptr(theta), _ptr(lam), _ptr(Dskip), _ptr(y),
+            B, L, D, N, int(mode), _dtype_code(x)]
+
+
+def csscan_forward(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode: int, stream=None) -> None:
+    """y <- scan(x, delta, A, Bc, Cc, theta, lam, Dskip); shapes and layouts as in csscan.h:
+    x, delta, y (B,L,D); Bc, Cc (B,L,N,2); theta (B,L,N); lam (B,L) or None; A (D,N) float32;
+    Dskip (D,) float32; y float32. Enqueued on ``stream`` (default: torch's current stream)."""
+    rc = load_library().csscan_forward(*_args(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode), _stream_handle(stream))
+    if rc != CSSCAN_OK:
+        raise CsscanError(rc, "csscan_forward")
+
+
+def csscan_forward_ex(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode: int, stream=None, *, chunk_len: int = 0,
+                      carry: int = 0, silent_chunk: int = -1, poll_limit: int = 0, scan_begin=None,
+                      scan_end=None) -> int:
+    """csscan_forward with launch options; returns the status instead of raising. scan_begin /
+    scan_end are optional torch.cuda.Event objects recorded around the scan kernel."""
+    ev = lambda e: None if e is None else e.cuda_event
+    o = csscan_options_t(0, chunk_len, carry, silent_chunk, poll_limit, ev(scan_begin), ev(scan_end))
+    return load_library().csscan_forward_ex(*_args(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode),
+                                            ctypes.byref(o), _stream_handle(stream))
+
+
+def csscan_get_device_status(stream=None) -> int:
+    return load_library().csscan_get_device_status(_stream_handle(stream))
+
+
+def csscan_status_string(status: int) -> str:
+    return load_library().csscan_status_string(int(status)).decode()
+
+
+def csscan_release_workspace() -> int:
+    return load_library().csscan_release_workspace()

@@ -1,0 +1,77 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry point, and rejects
+bad arguments on the host (before any CUDA call) with the documented status codes."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from selective_state_space_diagonal_b300 import build as libbuild
+from selective_state_space_diagonal_b300 import csscan
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return csscan.load_library()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(csscan_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert "csscan_forward" in names and len(names) >= 5
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(0, 8):
+        s = csscan.csscan_status_string(code)
+        assert isinstance(s, str) and s
+
+
+A16 = 1 << 20  # fake, 16-byte-aligned addresses: rejected calls never dereference them
+
+
+def call(lib, B=1, L=64, D=16, N=8, mode=0, dtype=0, x=A16, lam=A16, y=A16, opts=None):
+    args = [x, A16, A16, A16, A16, A16, lam, A16, y, B, L, D, N, mode, dtype]
+    if opts is None:
+        return lib.csscan_forward(*args, None)
+    return lib.csscan_forward_ex(*args, ctypes.byref(opts), None)
+
+
+def test_rejects_bad_arguments_on_host(lib):
+    assert call(lib, mode=2) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert call(lib, dtype=7) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert call(lib, B=-1) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert call(lib, N=0) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert call(lib, x=None) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert call(lib, y=None) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert call(lib, mode=1, lam=None) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert call(lib, N=3) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert call(lib, N=128) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert call(lib, x=A16 + 4) == csscan.CSSCAN_ERR_MISALIGNED
+    assert call(lib, D=6, dtype=0) == csscan.CSSCAN_ERR_MISALIGNED      # 24-byte rows
+    assert call(lib, D=12, dtype=1) == csscan.CSSCAN_ERR_MISALIGNED     # 24-byte rows
+    bad = csscan.csscan_options_t(0, 48, 0, -1, 0, None, None)                      # chunk not a multiple of 32
+    assert call(lib, opts=bad) == csscan.CSSCAN_ERR_INVALID_ARG
+    bad = csscan.csscan_options_t(0, 0, 3, -1, 0, None, None)
+    assert call(lib, opts=bad) == csscan.CSSCAN_ERR_INVALID_ARG
+
+
+def test_empty_problem_is_a_noop(lib):
+    # valid arguments with nothing to compute return before touching the device
+    assert call(lib, B=0) == csscan.CSSCAN_OK
+    assert call(lib, L=0) == csscan.CSSCAN_OK
+    assert call(lib, D=0) == csscan.CSSCAN_OK
+    assert call(lib, mode=1, B=0) == csscan.CSSCAN_OK
