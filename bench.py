@@ -283,6 +283,8 @@ def run_ours(args):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)] if flush else None
+    for e in sb + se:
+        e.record(stream)   # torch creates events lazily: make the handles exist before the library records them
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
