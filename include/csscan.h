@@ -71,7 +71,9 @@ enum {
   CSSCAN_ERR_LOOKBACK_TIMEOUT = 5, /* device: a chunk waited past its limit for its
                                       predecessor's carry (reported by csscan_get_device_status;
                                       the outputs of that call are not valid) */
-  CSSCAN_ERR_PIPELINE_TIMEOUT = 6  /* device: a tile copy did not arrive within its limit */
+  CSSCAN_ERR_PIPELINE_TIMEOUT = 6, /* device: a tile copy did not arrive within its limit */
+  CSSCAN_ERR_SCRATCH_LIMIT = 7     /* csscan_forward_noalloc: the problem needs more scratch than
+                                      its fixed CSSCAN_NOALLOC_SCRATCH_BYTES array holds */
 };
 
 typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1 } csscan_mode_t;
@@ -133,6 +135,36 @@ int csscan_get_device_status(cudaStream_t stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* csscan_status_string(int status);
+
+/*
+ * Forward scan that allocates no device memory. The reference pages have no counterpart:
+ * this entry point exists for callers that cannot call cudaMalloc -- for example a serving
+ * loop that must not allocate after start-up (cudaMalloc can synchronise the device and has
+ * no latency bound), or a host program whose device memory is entirely owned by another
+ * allocator or a fixed budget. It computes exactly what csscan_forward computes, with the
+ * same arguments, layouts and alignment rules, but its scratch space (the per-chunk carry
+ * records and the rotation tables) lives in one fixed array of CSSCAN_NOALLOC_SCRATCH_BYTES
+ * compiled into the library, which every GPU that loads the library holds until the
+ * process exits.
+ *
+ *   device_status : optional (NULL = none) caller-owned DEVICE pointer to one uint32_t; when
+ *                   the stream reaches the end of the call it holds this call's device-side
+ *                   status bits (0 = ok, 1 = a carry wait timed out, 2 = a tile copy timed out)
+ *
+ * Returns CSSCAN_ERR_SCRATCH_LIMIT, before any launch, when the problem needs more scratch
+ * than the fixed array holds (roughly B*L*N*16 bytes of tables plus 8 to 16 bytes per state
+ * of every chunk); csscan_forward has no such limit. The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress, which may load the library's GPU code on
+ * that device), so make that first call before any stream capture. All calls share the one
+ * array, whose contents persist from call to call; the call resets the parts that must start
+ * at zero. Calls that can overlap on the GPU (other streams, other threads) race on the
+ * array: issue them one after another on a single stream.
+ */
+#define CSSCAN_NOALLOC_SCRATCH_BYTES (32u << 20)
+int csscan_forward_noalloc(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                           const void* theta, const void* lambda, const float* Dskip, float* y,
+                           int64_t B, int64_t L, int64_t D, int64_t N, int mode, int dtype,
+                           uint32_t* device_status, cudaStream_t stream);
 
 /* Frees every internal workspace after synchronising its device. Returns CSSCAN_OK or
  * CSSCAN_ERR_CUDA. Safe to call at any time outside stream capture. */

@@ -23,6 +23,7 @@ CSSCAN_ERR_UNSUPPORTED = 3
 CSSCAN_ERR_CUDA = 4
 CSSCAN_ERR_LOOKBACK_TIMEOUT = 5
 CSSCAN_ERR_PIPELINE_TIMEOUT = 6
+CSSCAN_ERR_SCRATCH_LIMIT = 7
 
 CSSCAN_MODE_EXP_EULER = 0
 CSSCAN_MODE_EXP_TRAPEZOID = 1
@@ -130,3 +131,20 @@ def csscan_status_string(status: int) -> str:
 
 def csscan_release_workspace() -> int:
     return load_library().csscan_release_workspace()
+
+
+def csscan_forward_noalloc(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode: int, device_status=None,
+                           stream=None) -> int:
+    """The scan without any device allocation by the library (see csscan.h): for callers that
+    cannot call cudaMalloc, such as a serving loop that must not allocate after start-up or a
+    program whose device memory belongs to another allocator. Scratch comes from one fixed
+    array inside the library; problems that need more return CSSCAN_ERR_SCRATCH_LIMIT.
+    ``device_status`` is an optional one-element uint32/int32 CUDA tensor that receives the
+    call's device-side status bits. Returns the status instead of raising."""
+    lib = load_library()
+    fn = lib.csscan_forward_noalloc
+    if fn.argtypes is None:
+        fn.argtypes = [ctypes.c_void_p] * 9 + [ctypes.c_int64] * 4 + [ctypes.c_int, ctypes.c_int,
+                                                                       ctypes.c_void_p, ctypes.c_void_p]
+        fn.restype = ctypes.c_int
+    return fn(*_args(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode), _ptr(device_status), _stream_handle(stream))
