@@ -49,7 +49,7 @@ N_SM = 148
 def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--steps", type=int, default=400)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS))
@@ -99,61 +99,86 @@ def barrier():
 
 # ------------------------------------------------------------------------------ clocks
 class ClockSampler:
-    """Samples SM clock, power and clock-event reasons through NVML (read-only) while running."""
+    """Samples SM clock, power and clock-event reasons with nvidia-smi (read-only queries)
+    while the timed region runs; only samples taken between enter() and exit() count."""
 
-    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+    FIELDS = ("clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
+    def __init__(self, device_index: int, period_ms: int = 50):
         self.samples = []
-        self.period = period_s
-        self._stop = threading.Event()
-        self._t = None
-        self.max_mhz = None
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nvml = pynvml
-            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-            idx = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() else device_index
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(idx)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
-            self.nvml = None
+        self.error = None
+        self._proc = None
+        self._reader = None
+        self._t0 = self._t1 = None
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        ids = [v.strip() for v in vis.split(",")] if vis else []
+        self.gpu_id = ids[device_index] if device_index < len(ids) and ids[device_index] else str(device_index)
+        self.period_ms = period_ms
+        self._lines = []
 
-    def _run(self):
-        nv = self.nvml
-        while not self._stop.is_set():
-            try:
-                mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-                reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
-                self.samples.append((mhz, reasons, pw))
-            except Exception:
-                pass
-            time.sleep(self.period)
+    def start(self):
+        import subprocess
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # no nvidia-smi: report that instead of clocks
+            self.error = f"nvidia-smi unavailable: {e}"
+            return self
+
+        def read():
+            for line in self._proc.stdout:
+                self._lines.append((time.monotonic(), line.strip()))
+        self._reader = threading.Thread(target=read, daemon=True)
+        self._reader.start()
+        # wait for the first sample so that the sampler is running when the timed region starts
+        t_end = time.monotonic() + 5.0
+        while not self._lines and time.monotonic() < t_end and self._proc.poll() is None:
+            time.sleep(0.01)
+        return self
 
     def __enter__(self):
-        if self.nvml:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        self._t0 = time.monotonic()
         return self
 
     def __exit__(self, *exc):
-        self._stop.set()
-        if self._t:
-            self._t.join()
+        self._t1 = time.monotonic()
+
+    def stop(self):
+        if self._proc is not None:
+            time.sleep(0.12)
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
+        if self._reader is not None:
+            self._reader.join(timeout=5)
+        for ts, line in self._lines:
+            if self._t0 is None or not (self._t0 <= ts <= (self._t1 or ts)):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                mhz, max_mhz, pw = float(parts[0]), float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            active = [name for name, v in zip(self.REASONS, parts[3:]) if v.lower().startswith("active")]
+            self.samples.append((mhz, max_mhz, pw, active))
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
-        reasons = set()
-        for _, r, _ in self.samples:
-            for bit, name in self.REASONS.items():
-                if r & bit:
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(s[0] for s in self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(reasons), "samples": len(self.samples),
-                "power_w_max": max(s[2] for s in self.samples)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0,
+                    "error": self.error or "no sample fell inside the timed region"}
+        reasons = sorted({r for s in self.samples for r in s[3]})
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples), "sm_max_mhz": max(s[1] for s in self.samples),
+                "reasons": reasons, "samples": len(self.samples), "power_w_max": max(s[2] for s in self.samples),
+                "source": "nvidia-smi"}
 
 
 # ------------------------------------------------------------------------------ CPU oracle
@@ -287,7 +312,8 @@ def run_ours(args):
         e.record(stream)   # torch creates events lazily: make the handles exist before the library records them
     barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
+    clocks = ClockSampler(local).start()
+    with clocks:
         ev0.record(stream)
         for i in range(K):
             if flush:
@@ -298,6 +324,7 @@ def run_ours(args):
                 step_ev[i][1].record(stream)
         ev1.record(stream)
         torch.cuda.synchronize()
+    clocks.stop()
     barrier()
     if flush:
         elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
@@ -365,14 +392,34 @@ def run_ours(args):
     return 0
 
 
+KERNEL_SOURCES = ("selective_state_space_diagonal_b300/csrc/scan_kernels.cuh",
+                  "selective_state_space_diagonal_b300/csrc/device_util.cuh")
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profiles(workload: str):
-    """DRAM bytes per scan-kernel launch from the committed ncu summary of this workload, if
-    one exists for the current kernel (profiles/<kernel>_<workload>.json)."""
-    path = os.path.join(ROOT, "profiles", f"scan_kernel_{workload}.json")
+    """DRAM bytes per scan-kernel launch from the committed ncu summary of this workload
+    (profiles/scan_kernel_<workload>.md), or None when there is none or it was taken on
+    other kernel sources than the ones built now."""
+    path = os.path.join(ROOT, "profiles", f"scan_kernel_{workload}.md")
     try:
+        vals = {}
         with open(path) as f:
-            d = json.load(f)
-        return d.get("dram_bytes_per_launch")
+            for line in f:
+                if ":" in line and line.split(":", 1)[0].strip() in ("kernel_source_sha256_16", "dram_bytes_per_launch"):
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return int(vals["dram_bytes_per_launch"])
     except Exception:
         return None
 

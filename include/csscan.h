@@ -98,7 +98,8 @@ int csscan_forward(const void* x, const void* delta, const float* A, const void*
 
 /*
  * Launch options for csscan_forward_ex. Zero-initialise and set only what you need.
- *   rows_per_cta  : reserved, must be 0 (the row tile follows from N)
+ *   cta_warps     : reserved, must be 0 (a block is 4 warps covering 2 * 32 * 4 / NG channels,
+ *                   NG = N / 8 lanes sharing a channel pair for N >= 16, else 1)
  *   chunk_len     : sequence chunk per thread block (multiple of 32); 0 = automatic
  *   carry         : 0 automatic, 1 serial (each chunk waits for its predecessor's final state),
  *                   2 decoupled (each chunk first computes its own aggregate, then looks back)
@@ -111,7 +112,7 @@ int csscan_forward(const void* x, const void* delta, const float* A, const void*
  *                   right after the scan kernel, to time it apart from the small table kernel
  */
 typedef struct {
-  int32_t rows_per_cta;
+  int32_t cta_warps;
   int32_t chunk_len;
   int32_t carry;
   int32_t silent_chunk;

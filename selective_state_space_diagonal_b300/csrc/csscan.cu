@@ -1,6 +1,7 @@
 // csscan.cu -- host side of the C ABI declared in include/csscan.h: argument checks,
-// per-(device, stream) workspace, tile-copy descriptors, tiling choice and the launches of
-// the rotation-table kernel and the scan kernel (scan_kernels.cuh).
+// launch planning (block width, sequence chunks, shared-memory ring), the per-(device,
+// stream) workspace, tile-copy descriptors, and the launches of the rotation-table kernel
+// and the scan kernel (scan_kernels.cuh).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -8,6 +9,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "csscan.h"
@@ -57,6 +59,241 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+constexpr size_t HDR_BYTES = 256;
+
+// ----------------------------------------------------------------------------- arguments
+struct Args {
+  const void *x, *delta, *Bc, *Cc, *theta, *lam;
+  const float *A, *Dskip;
+  float* y;
+  const float* h0;
+  float* h_last;
+  const void *x_prev, *Bc_prev;
+  int64_t B, L, D, N;
+  int mode, dtype;
+};
+
+// ----------------------------------------------------------------------------- launch plan
+// Everything a launch needs that follows from the sizes, the options and the device: sequence
+// chunks and carry kind, and the workspace layout (byte offsets into the region after the
+// header and the flag words). The block shape and its shared-memory ring are compile-time
+// properties of the kernel (Tile, Stage in scan_kernels.cuh).
+struct Plan {
+  int DT = 0, n_dtiles = 0, n_tiles = 0, TC = 0, n_chunks = 0, n_units = 0, carry = 0, smem = 0;
+  int64_t S = 0;
+  size_t o_inc = 0, o_agg = 0, o_sdt = 0, o_crot = 0, o_tab = 0, o_aux = 0, o_rot = 0, rest_bytes = 0;
+};
+
+constexpr int MAX_DYN_SMEM = 160 * 1024;         // opt-in dynamic shared memory per block
+constexpr int RESIDENT_WARPS_PER_SM = 8;         // target of the automatic chunking
+
+// Blocks of `threads` threads and `smem` dynamic bytes resident per SM (cached per device).
+template <int N, typename Tin, int MODE, int CARRY>
+int occupancy(int dev, int threads, int smem, int* out) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, int> cache;
+  static std::map<int, bool> attr_set;
+  std::lock_guard<std::mutex> lk(mu);
+  auto kern = scan_kernel<N, Tin, MODE, CARRY>;
+  if (!attr_set[dev]) {
+    CSSCAN_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_DYN_SMEM));
+    attr_set[dev] = true;
+  }
+  auto key = std::make_tuple(dev, threads, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return CSSCAN_OK;
+  }
+  int occ = 0;
+  CSSCAN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem));
+  cache[key] = occ;
+  *out = occ;
+  return CSSCAN_OK;
+}
+
+template <int N, typename Tin, int MODE>
+int occupancy_for(int carry, int dev, int threads, int smem, int* out) {
+  if (carry == CARRY_SERIAL) return occupancy<N, Tin, MODE, CARRY_SERIAL>(dev, threads, smem, out);
+  if (carry == CARRY_DECOUPLED) return occupancy<N, Tin, MODE, CARRY_DECOUPLED>(dev, threads, smem, out);
+  return occupancy<N, Tin, MODE, CARRY_NONE>(dev, threads, smem, out);
+}
+
+// Launch plan. Blocks are 4 warps wide (one warp per SM sub-partition, so that the warps of a
+// block, which meet at a barrier once per sub-chunk, progress at the same rate). Rows with
+// enough parallelism are split into a few serial-carry chunks, chosen so that the chunk-units
+// fill the block slots in nearly whole waves; rows with too little parallelism are split into
+// as many decoupled chunks as fill the GPU.
+template <int N, typename Tin, int MODE>
+int make_plan(const Args& a, const csscan_options_t& o, int dev, Plan* pl) {
+  using TL = Tile<N>;
+  using SG = Stage<N, Tin, MODE>;
+  static_assert(SG::SMEM <= MAX_DYN_SMEM, "stage ring too large");
+  int nsm = 0;
+  CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+  const int64_t S = (a.L + T_SUB - 1) / T_SUB;
+  const int64_t target = int64_t(nsm) * RESIDENT_WARPS_PER_SM;
+  const int w = WARPS;
+  const int DT = TL::DT;
+  const int smem = SG::SMEM;
+  const int64_t n_dtiles = (a.D + DT - 1) / DT;
+  const int64_t tiles = a.B * n_dtiles;
+
+  int carry = o.carry;
+  int64_t TC = o.chunk_len;
+  if (TC == 0) {
+    int64_t chunks = 1;
+    // Measured on B300: the aggregate pass of decoupled chunks costs more than the extra
+    // parallelism returns unless the rows alone would leave most SMs idle.
+    const bool rich = 4 * tiles * w >= 3 * target;
+    const bool starved = 2 * tiles < nsm;
+    if (carry == CARRY_SERIAL || (carry == 0 && rich)) {
+      // serial chunks: each block runs at its own pace, so the time is about
+      // (waves of chunk-units) x (chunk length); pick the chunk count that minimises it, with
+      // ~1 % per extra chunk for the per-unit start-up
+      int occ = 0;
+      int rc = occupancy_for<N, Tin, MODE>(CARRY_SERIAL, dev, w * 32, smem, &occ);
+      if (rc != CSSCAN_OK) return rc;
+      const int64_t slots = int64_t(nsm) * std::max(occ, 1);
+      double best_t = 1e30;
+      for (int64_t C = 1; C <= std::min<int64_t>(S, 16); ++C) {
+        const int64_t waves = (tiles * C + slots - 1) / slots;
+        const double t = double(waves) / double(C) * (1.0 + 0.01 * double(C - 1));
+        if (t < best_t - 1e-12) { best_t = t; chunks = C; }
+      }
+      if (carry == 0) carry = CARRY_SERIAL;
+    } else if (carry == CARRY_DECOUPLED || (carry == 0 && starved)) {
+      // decoupled chunks: as many as fill every block slot once
+      int occ = 0;
+      int rc = occupancy_for<N, Tin, MODE>(CARRY_DECOUPLED, dev, w * 32, smem, &occ);
+      if (rc != CSSCAN_OK) return rc;
+      const int64_t slots = int64_t(nsm) * std::max(occ, 1);
+      chunks = std::max<int64_t>(1, std::min<int64_t>(S, slots / tiles));
+    }
+    TC = (S + chunks - 1) / chunks * T_SUB;
+  }
+  const int64_t n_chunks = (a.L + TC - 1) / TC;
+  if (n_chunks == 1) carry = CARRY_NONE;
+  else if (carry == 0) carry = CARRY_DECOUPLED;
+  const int64_t n_units = tiles * n_chunks;
+  if (n_units > (int64_t(1) << 30) || S > (int64_t(1) << 30)) return CSSCAN_ERR_UNSUPPORTED;
+  int occ = 0;
+  int rc = occupancy_for<N, Tin, MODE>(carry, dev, w * 32, smem, &occ);
+  if (rc != CSSCAN_OK) return rc;
+  if (occ < 1) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "scan block does not fit on this device");
+    return CSSCAN_ERR_CUDA;
+  }
+  pl->DT = DT;
+  pl->n_dtiles = int(n_dtiles);
+  pl->n_tiles = int(tiles);
+  pl->TC = int(TC);
+  pl->n_chunks = int(n_chunks);
+  pl->n_units = int(n_units);
+  pl->carry = carry;
+  pl->S = S;
+  pl->smem = smem;
+
+  // workspace layout after the header and the flags
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t r = off; off = align_up(off + bytes, 256); return r; };
+  pl->o_inc = carry != CARRY_NONE ? take(size_t(n_units) * DT * N * 8) : 0;
+  pl->o_agg = carry == CARRY_DECOUPLED ? take(size_t(n_units) * DT * N * 8) : 0;
+  pl->o_sdt = carry == CARRY_DECOUPLED ? take(size_t(n_units) * DT * 4) : 0;
+  pl->o_crot = carry == CARRY_DECOUPLED ? take(size_t(n_units) * N * 8) : 0;
+  pl->o_tab = take(size_t(a.B) * a.L * 4 * N * 4);
+  pl->o_aux = MODE == 1 ? take(size_t(a.B) * a.L * SG::AUX_W * 4) : 0;
+  pl->o_rot = take(size_t(a.B) * S * 2 * N * 4);
+  pl->rest_bytes = off;
+  return CSSCAN_OK;
+}
+
+// Fill the descriptors and pointers and enqueue both kernels. `hdr` is the workspace header
+// (epoch, ticket, done, status words), `flags` the per-unit flag words, `rest` the region laid
+// out by the plan.
+template <int N, typename Tin, int MODE>
+int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* hdr, uint32_t* flags, char* rest,
+            cudaStream_t st) {
+  TableParams tp;
+  tp.Bc = a.Bc;
+  tp.Cc = a.Cc;
+  tp.theta = a.theta;
+  tp.lam = a.lam;
+  tp.tab = reinterpret_cast<float*>(rest + pl.o_tab);
+  tp.aux = MODE == 1 ? reinterpret_cast<float*>(rest + pl.o_aux) : nullptr;
+  tp.rot = reinterpret_cast<float*>(rest + pl.o_rot);
+  tp.B = int(a.B);
+  tp.L = int(a.L);
+  tp.N = N;
+  tp.S = int(pl.S);
+
+  ScanParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  const CUtensorMapDataType tin = sizeof(Tin) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t s_in = sizeof(Tin);
+  const int64_t S = pl.S;
+  using SG = Stage<N, Tin, MODE>;
+  bool ok = make_map(&sp.tm_x, tin, a.x, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, pl.DT, SG::X_ROWS, 1) &&
+            make_map(&sp.tm_dt, tin, a.delta, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, pl.DT, SG::DT_ROWS, 1) &&
+            make_map(&sp.tm_tab, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.tab, 4 * N, a.L, a.B, 16 * N, a.L * 16 * N, 4 * N,
+                     SG::TAB_ROWS, 1) &&
+            make_map(&sp.tm_rot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.rot, 2 * N, S, a.B, 8 * N, S * 8 * N, 2 * N, 1, 1);
+  if (ok && MODE == 1)
+    ok = make_map(&sp.tm_aux, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.aux, SG::AUX_W, a.L, a.B, SG::AUX_W * 4,
+                  a.L * SG::AUX_W * 4, SG::AUX_W, SG::AUX_ROWS, 1);
+  if (!ok) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed or unavailable");
+    return CSSCAN_ERR_CUDA;
+  }
+  sp.A = a.A;
+  sp.Dskip = a.Dskip;
+  sp.y = a.y;
+  sp.x = a.x;
+  sp.dt = a.delta;
+  sp.Bc = a.Bc;
+  sp.lam = a.lam;
+  sp.h0 = a.h0;
+  sp.h_last = a.h_last;
+  sp.x_prev = a.x_prev;
+  sp.Bc_prev = a.Bc_prev;
+  sp.ws.hdr = hdr;
+  sp.ws.flags = flags;
+  sp.ws.inc = pl.carry != CARRY_NONE ? reinterpret_cast<float2*>(rest + pl.o_inc) : nullptr;
+  sp.ws.agg = pl.carry == CARRY_DECOUPLED ? reinterpret_cast<float2*>(rest + pl.o_agg) : nullptr;
+  sp.ws.sdt = pl.carry == CARRY_DECOUPLED ? reinterpret_cast<float*>(rest + pl.o_sdt) : nullptr;
+  sp.ws.crot = pl.carry == CARRY_DECOUPLED ? reinterpret_cast<float2*>(rest + pl.o_crot) : nullptr;
+  sp.B = int(a.B);
+  sp.L = int(a.L);
+  sp.D = int(a.D);
+  sp.N = N;
+  sp.S = int(S);
+  sp.n_dtiles = pl.n_dtiles;
+  sp.n_tiles = pl.n_tiles;
+  sp.TC = pl.TC;
+  sp.n_chunks = pl.n_chunks;
+  sp.n_units = pl.n_units;
+  sp.carry = pl.carry;
+  sp.y_vec2 = (reinterpret_cast<uintptr_t>(a.y) % 8) == 0;
+  sp.silent_chunk = o.silent_chunk;
+  sp.poll_limit = o.poll_limit > 0 ? o.poll_limit : (int64_t(1) << 22);
+
+  const int64_t table_threads = a.B * S * N;
+  table_kernel<Tin, MODE><<<unsigned((table_threads + 255) / 256), 256, 0, st>>>(tp);
+  CSSCAN_CUDA(cudaGetLastError());
+  if (o.scan_begin) CSSCAN_CUDA(cudaEventRecord(o.scan_begin, st));
+  const dim3 grid{unsigned(pl.n_units)}, block{unsigned(THREADS)};
+  if (pl.carry == CARRY_NONE)
+    scan_kernel<N, Tin, MODE, CARRY_NONE><<<grid, block, unsigned(pl.smem), st>>>(sp);
+  else if (pl.carry == CARRY_SERIAL)
+    scan_kernel<N, Tin, MODE, CARRY_SERIAL><<<grid, block, unsigned(pl.smem), st>>>(sp);
+  else
+    scan_kernel<N, Tin, MODE, CARRY_DECOUPLED><<<grid, block, unsigned(pl.smem), st>>>(sp);
+  CSSCAN_CUDA(cudaGetLastError());
+  if (o.scan_end) CSSCAN_CUDA(cudaEventRecord(o.scan_end, st));
+  return CSSCAN_OK;
+}
+
 // ----------------------------------------------------------------------------- workspace
 // Per (device, stream): [header 256 B][flags: flag_cap words][the rest, laid out per call].
 // The flags region only grows through a full reallocation, which zeroes it; records from
@@ -68,9 +305,6 @@ struct WsEntry {
 };
 std::mutex g_ws_mu;
 std::map<std::pair<int, uintptr_t>, WsEntry> g_ws;
-
-constexpr size_t HDR_BYTES = 256;
-size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 int get_workspace(int dev, cudaStream_t st, size_t units, size_t rest_bytes, WsEntry* out) {
   std::lock_guard<std::mutex> lk(g_ws_mu);
@@ -101,154 +335,30 @@ int get_workspace(int dev, cudaStream_t st, size_t units, size_t rest_bytes, WsE
   return CSSCAN_OK;
 }
 
-// ----------------------------------------------------------------------------- dispatch
-struct Args {
-  const void *x, *delta, *Bc, *Cc, *theta, *lam;
-  const float *A, *Dskip;
-  float* y;
-  const float* h0;
-  float* h_last;
-  const void *x_prev, *Bc_prev;
-  int64_t B, L, D, N;
-  int mode, dtype;
-};
-
-struct DeviceInfo {
-  int nsm = 0;
-};
-
-template <int N, int NG, typename Tin, int MODE>
+template <int N, typename Tin, int MODE>
 int launch(const Args& a, const csscan_options_t& o, cudaStream_t st) {
-  using SL = StageLayout<N, NG, Tin, MODE>;
-  constexpr int DT = SL::DT;
-  auto kern = scan_kernel<N, NG, Tin, MODE>;
   int dev = 0;
   CSSCAN_CUDA(cudaGetDevice(&dev));
-  static std::mutex mu;
-  static std::map<int, int> occ_cache;
-  int nsm = 0, occ = 0;
-  CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    auto it = occ_cache.find(dev);
-    if (it == occ_cache.end()) {
-      CSSCAN_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SL::SMEM));
-      CSSCAN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS, SL::SMEM));
-      occ_cache[dev] = occ;
-    } else {
-      occ = it->second;
-    }
-  }
-  const int64_t conc = int64_t(nsm) * std::max(occ, 1);
-  const int64_t n_dtiles = (a.D + DT - 1) / DT;
-  const int64_t n_tiles = a.B * n_dtiles;
-  const int64_t S = (a.L + T_SUB - 1) / T_SUB;
-
-  int carry = o.carry;
-  if (carry == 0) carry = (n_tiles >= conc) ? CARRY_SERIAL : CARRY_DECOUPLED;
-  int64_t TC = o.chunk_len;
-  if (TC == 0) {
-    const int64_t want = carry == CARRY_SERIAL ? (4 * conc + n_tiles - 1) / n_tiles : (2 * conc + n_tiles - 1) / n_tiles;
-    const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(S, want));
-    TC = (S + chunks - 1) / chunks * T_SUB;
-  }
-  const int64_t n_chunks = (a.L + TC - 1) / TC;
-  const int64_t n_units = n_tiles * n_chunks;
-  if (n_units > (int64_t(1) << 30) || S > (int64_t(1) << 30)) return CSSCAN_ERR_UNSUPPORTED;
-
-  // workspace layout after the header and flags
-  size_t off = 0;
-  auto take = [&](size_t bytes) { size_t r = off; off = align_up(off + bytes, 256); return r; };
-  const size_t o_inc = take(size_t(n_units) * DT * N * 8);
-  const size_t o_agg = carry == CARRY_DECOUPLED ? take(size_t(n_units) * DT * N * 8) : 0;
-  const size_t o_sdt = carry == CARRY_DECOUPLED ? take(size_t(n_units) * DT * 4) : 0;
-  const size_t o_crot = carry == CARRY_DECOUPLED ? take(size_t(n_units) * N * 8) : 0;
-  const size_t o_tab = take(size_t(a.B) * a.L * 4 * N * 4);
-  const size_t o_aux = MODE == 1 ? take(size_t(a.B) * a.L * 16) : 0;
-  const size_t o_rot = take(size_t(a.B) * S * 2 * N * 4);
-  WsEntry ws;
-  int rc = get_workspace(dev, st, size_t(n_units), off, &ws);
+  Plan pl;
+  int rc = make_plan<N, Tin, MODE>(a, o, dev, &pl);
   if (rc != CSSCAN_OK) return rc;
-  char* rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
-
-  TableParams tp;
-  tp.Bc = a.Bc;
-  tp.Cc = a.Cc;
-  tp.theta = a.theta;
-  tp.lam = a.lam;
-  tp.tab = reinterpret_cast<float*>(rest + o_tab);
-  tp.aux = MODE == 1 ? reinterpret_cast<float*>(rest + o_aux) : nullptr;
-  tp.rot = reinterpret_cast<float*>(rest + o_rot);
-  tp.B = int(a.B);
-  tp.L = int(a.L);
-  tp.N = N;
-  tp.S = int(S);
-
-  ScanParams sp;
-  std::memset(&sp, 0, sizeof(sp));
-  const CUtensorMapDataType tin = sizeof(Tin) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t s_in = sizeof(Tin);
-  bool ok = make_map(&sp.tm_x, tin, a.x, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, DT, T_SUB, 1) &&
-            make_map(&sp.tm_dt, tin, a.delta, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, DT, T_SUB + 1, 1) &&
-            make_map(&sp.tm_tab, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.tab, 4 * N, a.L, a.B, 16 * N, a.L * 16 * N, 4 * N,
-                     T_SUB, 1) &&
-            make_map(&sp.tm_rot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.rot, 2 * N, S, a.B, 8 * N, S * 8 * N, 2 * N, 1, 1);
-  if (ok && MODE == 1)
-    ok = make_map(&sp.tm_aux, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.aux, 4, a.L, a.B, 16, a.L * 16, 4, T_SUB, 1);
-  if (!ok) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed or unavailable");
-    return CSSCAN_ERR_CUDA;
-  }
-  sp.A = a.A;
-  sp.Dskip = a.Dskip;
-  sp.y = a.y;
-  sp.x = a.x;
-  sp.dt = a.delta;
-  sp.Bc = a.Bc;
-  sp.lam = a.lam;
-  sp.h0 = a.h0;
-  sp.h_last = a.h_last;
-  sp.x_prev = a.x_prev;
-  sp.Bc_prev = a.Bc_prev;
-  sp.ws.hdr = static_cast<uint32_t*>(ws.base);
-  sp.ws.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(ws.base) + HDR_BYTES);
-  sp.ws.inc = reinterpret_cast<float2*>(rest + o_inc);
-  sp.ws.agg = carry == CARRY_DECOUPLED ? reinterpret_cast<float2*>(rest + o_agg) : nullptr;
-  sp.ws.sdt = carry == CARRY_DECOUPLED ? reinterpret_cast<float*>(rest + o_sdt) : nullptr;
-  sp.ws.crot = carry == CARRY_DECOUPLED ? reinterpret_cast<float2*>(rest + o_crot) : nullptr;
-  sp.B = int(a.B);
-  sp.L = int(a.L);
-  sp.D = int(a.D);
-  sp.N = N;
-  sp.S = int(S);
-  sp.n_dtiles = int(n_dtiles);
-  sp.n_tiles = int(n_tiles);
-  sp.TC = int(TC);
-  sp.n_chunks = int(n_chunks);
-  sp.n_units = int(n_units);
-  sp.carry = carry;
-  sp.silent_chunk = o.silent_chunk;
-  sp.poll_limit = o.poll_limit > 0 ? o.poll_limit : (int64_t(1) << 22);
-
-  const int64_t table_threads = a.B * S * N;
-  table_kernel<Tin, MODE><<<unsigned((table_threads + 255) / 256), 256, 0, st>>>(tp);
-  CSSCAN_CUDA(cudaGetLastError());
-  if (o.scan_begin) CSSCAN_CUDA(cudaEventRecord(o.scan_begin, st));
-  kern<<<unsigned(n_units), THREADS, SL::SMEM, st>>>(sp);
-  CSSCAN_CUDA(cudaGetLastError());
-  if (o.scan_end) CSSCAN_CUDA(cudaEventRecord(o.scan_end, st));
-  return CSSCAN_OK;
+  WsEntry ws;
+  rc = get_workspace(dev, st, size_t(pl.n_units), pl.rest_bytes, &ws);
+  if (rc != CSSCAN_OK) return rc;
+  char* base = static_cast<char*>(ws.base);
+  return enqueue<N, Tin, MODE>(a, o, pl, reinterpret_cast<uint32_t*>(base), reinterpret_cast<uint32_t*>(base + HDR_BYTES),
+                               base + HDR_BYTES + align_up(ws.flag_cap * 4, 256), st);
 }
 
 template <typename Tin, int MODE>
 int dispatch_n(const Args& a, const csscan_options_t& o, cudaStream_t st) {
   switch (a.N) {
-    case 2: return launch<2, 1, Tin, MODE>(a, o, st);
-    case 4: return launch<4, 1, Tin, MODE>(a, o, st);
-    case 8: return launch<8, 1, Tin, MODE>(a, o, st);
-    case 16: return launch<16, 1, Tin, MODE>(a, o, st);
-    case 32: return launch<32, 2, Tin, MODE>(a, o, st);
-    case 64: return launch<64, 4, Tin, MODE>(a, o, st);
+    case 2: return launch<2, Tin, MODE>(a, o, st);
+    case 4: return launch<4, Tin, MODE>(a, o, st);
+    case 8: return launch<8, Tin, MODE>(a, o, st);
+    case 16: return launch<16, Tin, MODE>(a, o, st);
+    case 32: return launch<32, Tin, MODE>(a, o, st);
+    case 64: return launch<64, Tin, MODE>(a, o, st);
     default: return CSSCAN_ERR_UNSUPPORTED;
   }
 }
@@ -262,8 +372,8 @@ int validate(const Args& a, const csscan_options_t& o) {
   if (!a.x || !a.delta || !a.A || !a.Bc || !a.Cc || !a.theta || !a.Dskip || !a.y) return CSSCAN_ERR_INVALID_ARG;
   if (a.mode == CSSCAN_MODE_EXP_TRAPEZOID && !a.lam) return CSSCAN_ERR_INVALID_ARG;
   if ((a.x_prev == nullptr) != (a.Bc_prev == nullptr)) return CSSCAN_ERR_INVALID_ARG;
-  if (o.rows_per_cta != 0 || o.carry < 0 || o.carry > 2 || o.chunk_len < 0 || (o.chunk_len % T_SUB) != 0 ||
-      o.poll_limit < 0)
+  if (o.cta_warps != 0 || o.carry < 0 || o.carry > 2 || o.chunk_len < 0 ||
+      (o.chunk_len % T_SUB) != 0 || o.poll_limit < 0)
     return CSSCAN_ERR_INVALID_ARG;
   if (a.N != 2 && a.N != 4 && a.N != 8 && a.N != 16 && a.N != 32 && a.N != 64) return CSSCAN_ERR_UNSUPPORTED;
   if (a.B > (int64_t(1) << 31) - 1 || a.L > (int64_t(1) << 30) || a.D > (int64_t(1) << 30)) return CSSCAN_ERR_UNSUPPORTED;
@@ -277,11 +387,15 @@ int validate(const Args& a, const csscan_options_t& o) {
   return CSSCAN_OK;
 }
 
-int forward_impl(const Args& a, const csscan_options_t* opts, cudaStream_t st) {
+csscan_options_t default_options() {
   csscan_options_t o;
   std::memset(&o, 0, sizeof(o));
   o.silent_chunk = -1;
-  if (opts) o = *opts;
+  return o;
+}
+
+int forward_impl(const Args& a, const csscan_options_t* opts, cudaStream_t st) {
+  csscan_options_t o = opts ? *opts : default_options();
   int rc = validate(a, o);
   if (rc != CSSCAN_OK) return rc;
   if (a.B == 0 || a.L == 0 || a.D == 0) return CSSCAN_OK;
@@ -294,7 +408,7 @@ int forward_impl(const Args& a, const csscan_options_t* opts, cudaStream_t st) {
 // ----------------------------------------------------------------------------- no-allocation entry
 // csscan_forward_noalloc runs the same two kernels with its scratch in one fixed array that
 // is part of the library's device code, so it never calls cudaMalloc. Layout of the array:
-// [header 256 B][flags: NOALLOC_FLAG_CAP words][the rest, laid out per call as in launch()].
+// [header 256 B][flags: NOALLOC_FLAG_CAP words][the rest, laid out per call by the plan].
 constexpr size_t NOALLOC_FLAG_CAP = 1 << 16;
 constexpr size_t NOALLOC_REST_OFF = HDR_BYTES + NOALLOC_FLAG_CAP * 4;
 static_assert(NOALLOC_REST_OFF < CSSCAN_NOALLOC_SCRATCH_BYTES, "scratch too small");
@@ -304,120 +418,26 @@ std::map<int, char*> g_noalloc_addr;   // device -> device address of the scratc
 
 int noalloc_scratch_address(int dev, char** out);   // defined after the array below
 
-template <int N, int NG, typename Tin, int MODE>
+template <int N, typename Tin, int MODE>
 int launch_noalloc(const Args& a, uint32_t* device_status, cudaStream_t st) {
-  using SL = StageLayout<N, NG, Tin, MODE>;
-  constexpr int DT = SL::DT;
-  auto kern = scan_kernel<N, NG, Tin, MODE>;
   int dev = 0;
   CSSCAN_CUDA(cudaGetDevice(&dev));
-  static std::mutex mu;
-  static std::map<int, int> occ_cache;
-  int nsm = 0, occ = 0;
-  CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-  {
-    std::lock_guard<std::mutex> lk(mu);
-    auto it = occ_cache.find(dev);
-    if (it == occ_cache.end()) {
-      CSSCAN_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SL::SMEM));
-      CSSCAN_CUDA(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, THREADS, SL::SMEM));
-      occ_cache[dev] = occ;
-    } else {
-      occ = it->second;
-    }
-  }
-  const int64_t conc = int64_t(nsm) * std::max(occ, 1);
-  const int64_t n_dtiles = (a.D + DT - 1) / DT;
-  const int64_t n_tiles = a.B * n_dtiles;
-  const int64_t S = (a.L + T_SUB - 1) / T_SUB;
-  const int carry = (n_tiles >= conc) ? CARRY_SERIAL : CARRY_DECOUPLED;
-  const int64_t want = carry == CARRY_SERIAL ? (4 * conc + n_tiles - 1) / n_tiles : (2 * conc + n_tiles - 1) / n_tiles;
-  const int64_t chunks = std::max<int64_t>(1, std::min<int64_t>(S, want));
-  const int64_t TC = (S + chunks - 1) / chunks * T_SUB;
-  const int64_t n_chunks = (a.L + TC - 1) / TC;
-  const int64_t n_units = n_tiles * n_chunks;
-
-  size_t off = 0;
-  auto take = [&](size_t bytes) { size_t r = off; off = align_up(off + bytes, 256); return r; };
-  const size_t o_inc = take(size_t(n_units) * DT * N * 8);
-  const size_t o_agg = carry == CARRY_DECOUPLED ? take(size_t(n_units) * DT * N * 8) : 0;
-  const size_t o_sdt = carry == CARRY_DECOUPLED ? take(size_t(n_units) * DT * 4) : 0;
-  const size_t o_crot = carry == CARRY_DECOUPLED ? take(size_t(n_units) * N * 8) : 0;
-  const size_t o_tab = take(size_t(a.B) * a.L * 4 * N * 4);
-  const size_t o_aux = MODE == 1 ? take(size_t(a.B) * a.L * 16) : 0;
-  const size_t o_rot = take(size_t(a.B) * S * 2 * N * 4);
-  if (size_t(n_units) > NOALLOC_FLAG_CAP || off > CSSCAN_NOALLOC_SCRATCH_BYTES - NOALLOC_REST_OFF)
+  const csscan_options_t o = default_options();
+  Plan pl;
+  int rc = make_plan<N, Tin, MODE>(a, o, dev, &pl);
+  if (rc != CSSCAN_OK) return rc;
+  if (size_t(pl.n_units) > NOALLOC_FLAG_CAP || pl.rest_bytes > CSSCAN_NOALLOC_SCRATCH_BYTES - NOALLOC_REST_OFF)
     return CSSCAN_ERR_SCRATCH_LIMIT;
 
   char* base = nullptr;
-  int rc = noalloc_scratch_address(dev, &base);
+  rc = noalloc_scratch_address(dev, &base);
   if (rc != CSSCAN_OK) return rc;
-  char* rest = base + NOALLOC_REST_OFF;
   uint32_t* hdr = reinterpret_cast<uint32_t*>(base);
   // the ticket and finished-block counters and the status words must start at zero; the
   // epoch (word 0) keeps counting so that flags left by earlier calls are never current
   CSSCAN_CUDA(cudaMemsetAsync(hdr + H_TICKET, 0, 5 * sizeof(uint32_t), st));
-
-  TableParams tp;
-  tp.Bc = a.Bc;
-  tp.Cc = a.Cc;
-  tp.theta = a.theta;
-  tp.lam = a.lam;
-  tp.tab = reinterpret_cast<float*>(rest + o_tab);
-  tp.aux = MODE == 1 ? reinterpret_cast<float*>(rest + o_aux) : nullptr;
-  tp.rot = reinterpret_cast<float*>(rest + o_rot);
-  tp.B = int(a.B);
-  tp.L = int(a.L);
-  tp.N = N;
-  tp.S = int(S);
-
-  ScanParams sp;
-  std::memset(&sp, 0, sizeof(sp));
-  const CUtensorMapDataType tin = sizeof(Tin) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t s_in = sizeof(Tin);
-  bool ok = make_map(&sp.tm_x, tin, a.x, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, DT, T_SUB, 1) &&
-            make_map(&sp.tm_dt, tin, a.delta, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, DT, T_SUB + 1, 1) &&
-            make_map(&sp.tm_tab, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.tab, 4 * N, a.L, a.B, 16 * N, a.L * 16 * N, 4 * N,
-                     T_SUB, 1) &&
-            make_map(&sp.tm_rot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.rot, 2 * N, S, a.B, 8 * N, S * 8 * N, 2 * N, 1, 1);
-  if (ok && MODE == 1)
-    ok = make_map(&sp.tm_aux, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.aux, 4, a.L, a.B, 16, a.L * 16, 4, T_SUB, 1);
-  if (!ok) {
-    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "cuTensorMapEncodeTiled failed or unavailable");
-    return CSSCAN_ERR_CUDA;
-  }
-  sp.A = a.A;
-  sp.Dskip = a.Dskip;
-  sp.y = a.y;
-  sp.x = a.x;
-  sp.dt = a.delta;
-  sp.Bc = a.Bc;
-  sp.lam = a.lam;
-  sp.ws.hdr = hdr;
-  sp.ws.flags = reinterpret_cast<uint32_t*>(base + HDR_BYTES);
-  sp.ws.inc = reinterpret_cast<float2*>(rest + o_inc);
-  sp.ws.agg = carry == CARRY_DECOUPLED ? reinterpret_cast<float2*>(rest + o_agg) : nullptr;
-  sp.ws.sdt = carry == CARRY_DECOUPLED ? reinterpret_cast<float*>(rest + o_sdt) : nullptr;
-  sp.ws.crot = carry == CARRY_DECOUPLED ? reinterpret_cast<float2*>(rest + o_crot) : nullptr;
-  sp.B = int(a.B);
-  sp.L = int(a.L);
-  sp.D = int(a.D);
-  sp.N = N;
-  sp.S = int(S);
-  sp.n_dtiles = int(n_dtiles);
-  sp.n_tiles = int(n_tiles);
-  sp.TC = int(TC);
-  sp.n_chunks = int(n_chunks);
-  sp.n_units = int(n_units);
-  sp.carry = carry;
-  sp.silent_chunk = -1;
-  sp.poll_limit = int64_t(1) << 22;
-
-  const int64_t table_threads = a.B * S * N;
-  table_kernel<Tin, MODE><<<unsigned((table_threads + 255) / 256), 256, 0, st>>>(tp);
-  CSSCAN_CUDA(cudaGetLastError());
-  kern<<<unsigned(n_units), THREADS, SL::SMEM, st>>>(sp);
-  CSSCAN_CUDA(cudaGetLastError());
+  rc = enqueue<N, Tin, MODE>(a, o, pl, hdr, reinterpret_cast<uint32_t*>(base + HDR_BYTES), base + NOALLOC_REST_OFF, st);
+  if (rc != CSSCAN_OK) return rc;
   if (device_status)
     CSSCAN_CUDA(cudaMemcpyAsync(device_status, hdr + H_ERROR, sizeof(uint32_t), cudaMemcpyDeviceToDevice, st));
   return CSSCAN_OK;
@@ -426,12 +446,12 @@ int launch_noalloc(const Args& a, uint32_t* device_status, cudaStream_t st) {
 template <typename Tin, int MODE>
 int dispatch_noalloc(const Args& a, uint32_t* device_status, cudaStream_t st) {
   switch (a.N) {
-    case 2: return launch_noalloc<2, 1, Tin, MODE>(a, device_status, st);
-    case 4: return launch_noalloc<4, 1, Tin, MODE>(a, device_status, st);
-    case 8: return launch_noalloc<8, 1, Tin, MODE>(a, device_status, st);
-    case 16: return launch_noalloc<16, 1, Tin, MODE>(a, device_status, st);
-    case 32: return launch_noalloc<32, 2, Tin, MODE>(a, device_status, st);
-    case 64: return launch_noalloc<64, 4, Tin, MODE>(a, device_status, st);
+    case 2: return launch_noalloc<2, Tin, MODE>(a, device_status, st);
+    case 4: return launch_noalloc<4, Tin, MODE>(a, device_status, st);
+    case 8: return launch_noalloc<8, Tin, MODE>(a, device_status, st);
+    case 16: return launch_noalloc<16, Tin, MODE>(a, device_status, st);
+    case 32: return launch_noalloc<32, Tin, MODE>(a, device_status, st);
+    case 64: return launch_noalloc<64, Tin, MODE>(a, device_status, st);
     default: return CSSCAN_ERR_UNSUPPORTED;
   }
 }
@@ -479,9 +499,7 @@ int csscan_forward_noalloc(const void* x, const void* delta, const float* A, con
                            const void* theta, const void* lambda, const float* Dskip, float* y, int64_t B, int64_t L,
                            int64_t D, int64_t N, int mode, int dtype, uint32_t* device_status, cudaStream_t stream) {
   Args a{x, delta, Bc, Cc, theta, lambda, A, Dskip, y, nullptr, nullptr, nullptr, nullptr, B, L, D, N, mode, dtype};
-  csscan_options_t o;
-  std::memset(&o, 0, sizeof(o));
-  o.silent_chunk = -1;
+  const csscan_options_t o = default_options();
   int rc = validate(a, o);
   if (rc != CSSCAN_OK) return rc;
   if (device_status && (reinterpret_cast<uintptr_t>(device_status) % 4) != 0) return CSSCAN_ERR_MISALIGNED;

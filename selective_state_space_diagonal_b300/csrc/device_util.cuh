@@ -21,6 +21,8 @@ __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b
 // Packed float32x2 fused multiply-add / multiply (one instruction for two lanes).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+// 2^z for both halves of a pair.
+__device__ __forceinline__ float2 ex2_pair(float2 z) { return make_float2(ex2_approx(z.x), ex2_approx(z.y)); }
 
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
 

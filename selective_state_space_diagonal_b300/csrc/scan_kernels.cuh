@@ -17,7 +17,11 @@
 //        k_{t+1} = r_t k_t + (q_t + p_{t+1}) Bt_t,
 //        y_t = Re(sum_n Ct_t k_{t+1}) - p_{t+1} E_t + Dskip x_t,  E_t = sum_n Re(Cc_t Bc_t),
 //    the same per-element cost as exp-Euler (which is the case p = 0, q = dt x).
-// 3. Chunks. A thread block owns DT channels of one batch row for one chunk of TC steps.
+// 3. Thread tile. A block has 4 warps (one per SM sub-partition). A thread owns CH = 2
+//    adjacent channels and NS consecutive states of each; NG = N / NS neighbouring lanes
+//    share one channel pair and sum their partial outputs with a shuffle. Every table value
+//    a thread loads from shared memory serves both of its channels.
+// 4. Chunks. A thread block owns DT channels of one batch row for one chunk of TC steps.
 //    The chunk's map h_in -> h_end is affine: h_end = P h_in + U with
 //    P = exp(A sum dt) e^{i sum theta} (the combine of the step operators), so a chunk can
 //    publish U before it knows h_in, and successors combine predecessors' (P, U) pairs
@@ -33,11 +37,53 @@
 namespace csscan {
 
 constexpr int T_SUB = 32;       // sub-chunk: one rotation frame and one staged tile
-constexpr int THREADS = 128;    // threads per block
+constexpr int CH = 2;           // channels per thread
+constexpr int WARPS = 4;        // warps per block
+constexpr int THREADS = WARPS * 32;
+constexpr int MAX_STAGES = 4;   // depth of the shared-memory ring
+constexpr int RING_BYTES = 56 * 1024;   // shared memory for the ring of one block
 constexpr float LOG2E_F = 1.4426950408889634f;
 
+// Thread tile for N states: NS states per thread, NG lanes per channel pair, CPW channels
+// per warp, DT channels per block.
+template <int N>
+struct Tile {
+  static constexpr int NS = N >= 8 ? 8 : N;
+  static constexpr int NG = N / NS;
+  static constexpr int NPAIR = NS / 2;
+  static constexpr int CPW = 32 / NG * CH;
+  static constexpr int DT = WARPS * CPW;
+  static_assert(NS % 2 == 0 && NG >= 1 && NG <= 32 && (NG & (NG - 1)) == 0, "unsupported N");
+};
+
+// Shared-memory stage: one sub-chunk of one block. Rows past the sub-chunk (one of x, aux and
+// the table, two of dt) feed the software pipeline's look-ahead and the trapezoid's dt_{t+1}.
+constexpr int align128(int v) { return (v + 127) & ~127; }
+template <int N, typename Tin, int MODE>
+struct Stage {
+  static constexpr int DT = Tile<N>::DT;
+  static constexpr int SIN = int(sizeof(Tin));
+  static constexpr int X_ROWS = T_SUB + 1, DT_ROWS = T_SUB + 2, AUX_ROWS = T_SUB + 1, TAB_ROWS = T_SUB + 1;
+  static constexpr int AUX_W = 8;                       // floats per aux row
+  static constexpr int X_BYTES = X_ROWS * DT * SIN;
+  static constexpr int DT_BYTES = DT_ROWS * DT * SIN;
+  static constexpr int TAB_BYTES = TAB_ROWS * 4 * N * 4;
+  static constexpr int AUX_BYTES = MODE == 1 ? AUX_ROWS * AUX_W * 4 : 0;
+  static constexpr int ROT_BYTES = 2 * N * 4;
+  static constexpr int OFF_X = 0;
+  static constexpr int OFF_DT = align128(OFF_X + X_BYTES);
+  static constexpr int OFF_TAB = align128(OFF_DT + DT_BYTES);
+  static constexpr int OFF_AUX = align128(OFF_TAB + TAB_BYTES);
+  static constexpr int OFF_ROT = align128(OFF_AUX + AUX_BYTES);
+  static constexpr int BYTES = align128(OFF_ROT + ROT_BYTES);
+  static constexpr int TX_BYTES = X_BYTES + DT_BYTES + TAB_BYTES + AUX_BYTES + ROT_BYTES;
+  static constexpr int FIT = RING_BYTES / BYTES;
+  static constexpr int NST = FIT >= MAX_STAGES ? MAX_STAGES : (FIT >= 2 ? FIT : 2);
+  static constexpr int SMEM = NST * BYTES + 128;        // + alignment slack
+};
+
 enum : uint32_t { ST_NONE = 0, ST_AGG = 1, ST_INCL = 2 };
-enum : int { CARRY_SERIAL = 1, CARRY_DECOUPLED = 2 };
+enum : int { CARRY_NONE = 0, CARRY_SERIAL = 1, CARRY_DECOUPLED = 2 };
 enum : uint32_t { ERR_LOOKBACK = 1u, ERR_PIPELINE = 2u };
 enum { H_EPOCH = 0, H_TICKET = 1, H_DONE = 2, H_ERROR = 3, H_ERR_UNIT = 4, H_ERR_PRED = 5 };
 
@@ -59,7 +105,8 @@ struct TableParams {
   const void* theta;
   const void* lam;
   float* tab;  // (B, L, N/2, 8): per state pair (Btr, Btr', Bti, Bti', Ctr, Ctr', -Cti, -Cti')
-  float* aux;  // (B, L, 4): lam_t, 1 - lam_{t+1} (0 at t = L-1), E_t, 0   (trapezoid only)
+  float* aux;  // (B, L, 8): lam_t, lam_t, mu, mu, E_t, E_t, 0, 0 with mu = 1 - lam_{t+1}
+               // (0 at t = L-1) (trapezoid only)
   float* rot;  // (B, S, N, 2): e^{i Phi} at the last step of sub-chunk s
   int B, L, N, S;
 };
@@ -103,18 +150,21 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
         const int64_t tm = tb * p.N + m;
         E += load_in<Tin>(Cc, 2 * tm) * load_in<Tin>(Bc, 2 * tm) - load_in<Tin>(Cc, 2 * tm + 1) * load_in<Tin>(Bc, 2 * tm + 1);
       }
-      const float mu_next = (t + 1 < p.L) ? 1.f - load_in<Tin>(lam, tb + 1) : 0.f;
-      reinterpret_cast<float4*>(p.aux)[tb] = make_float4(load_in<Tin>(lam, tb), mu_next, E, 0.f);
+      const float lt = load_in<Tin>(lam, tb);
+      const float mu = (t + 1 < p.L) ? 1.f - load_in<Tin>(lam, tb + 1) : 0.f;
+      float4* a = reinterpret_cast<float4*>(p.aux) + 2 * tb;
+      a[0] = make_float4(lt, lt, mu, mu);
+      a[1] = make_float4(E, E, 0.f, 0.f);
     }
   }
 }
 
 // ------------------------------------------------------------------------- scan kernel
 struct ScanParams {
-  CUtensorMap tm_x;    // (D, L, B) input dtype, box (DT, T_SUB, 1)
-  CUtensorMap tm_dt;   // (D, L, B) input dtype, box (DT, T_SUB + 1, 1)
-  CUtensorMap tm_tab;  // (4N, L, B) f32, box (4N, T_SUB, 1)
-  CUtensorMap tm_aux;  // (4, L, B) f32, box (4, T_SUB, 1)
+  CUtensorMap tm_x;    // (D, L, B) input dtype, box (DT, T_SUB + 1, 1)
+  CUtensorMap tm_dt;   // (D, L, B) input dtype, box (DT, T_SUB + 2, 1)
+  CUtensorMap tm_tab;  // (4N, L, B) f32, box (4N, T_SUB + 1, 1)
+  CUtensorMap tm_aux;  // (8, L, B) f32, box (8, T_SUB + 1, 1)
   CUtensorMap tm_rot;  // (2N, S, B) f32, box (2N, 1, 1)
   const float* A;
   const float* Dskip;
@@ -131,30 +181,9 @@ struct ScanParams {
   int B, L, D, N, S;
   int n_dtiles, n_tiles, TC, n_chunks, n_units;
   int carry;
+  int y_vec2;           // y is 8-byte aligned: store channel pairs as float2
   int silent_chunk;
   long long poll_limit;
-};
-
-__host__ __device__ constexpr int align128(int v) { return (v + 127) & ~127; }
-
-template <int N, int NG, typename Tin, int MODE>
-struct StageLayout {
-  static constexpr int DT = THREADS / NG;
-  static constexpr int X_OFF = 0;
-  static constexpr int X_BYTES = T_SUB * DT * int(sizeof(Tin));
-  static constexpr int DT_OFF = align128(X_OFF + X_BYTES);
-  static constexpr int DT_BYTES = (T_SUB + 1) * DT * int(sizeof(Tin));
-  static constexpr int TAB_OFF = align128(DT_OFF + DT_BYTES);
-  static constexpr int TAB_BYTES = T_SUB * 4 * N * 4;
-  static constexpr int AUX_OFF = align128(TAB_OFF + TAB_BYTES);
-  static constexpr int AUX_BYTES = MODE == 1 ? T_SUB * 16 : 0;
-  static constexpr int ROT_OFF = align128(AUX_OFF + AUX_BYTES);
-  static constexpr int ROT_BYTES = 2 * N * 4;
-  static constexpr int STAGE = align128(ROT_OFF + ROT_BYTES);
-  static constexpr int TX_BYTES = X_BYTES + DT_BYTES + TAB_BYTES + AUX_BYTES + ROT_BYTES;
-  static constexpr int BUDGET = 112 * 1024;
-  static constexpr int NS = STAGE * 4 <= BUDGET ? 4 : (STAGE * 3 <= BUDGET ? 3 : 2);
-  static constexpr int SMEM = NS * STAGE + 128;   // + alignment slack
 };
 
 __device__ __forceinline__ bool flag_ready(uint32_t f, uint32_t epoch, uint32_t need) {
@@ -176,33 +205,60 @@ __device__ __forceinline__ bool wait_bar_bounded(uint64_t* bar, uint32_t parity)
   return false;
 }
 
-template <int N, int NG, typename Tin, int MODE>
-__global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ ScanParams p) {
-  using SL = StageLayout<N, NG, Tin, MODE>;
-  constexpr int NPT = N / NG;       // states per thread
-  constexpr int NPAIR = NPT / 2;    // packed pairs per thread
-  constexpr int DT = SL::DT;        // channels per block
-  constexpr int NS = SL::NS;
-  static_assert(NPT % 2 == 0 && NPT >= 2, "states per thread must be even");
+// Two adjacent channels (c0, c1) of one staged row, each widened to float32 and broadcast to
+// both halves of a pair: returns (c0, c0) and (c1, c1). The bf16 case widens with byte
+// permutes (two different selectors, so the two halves are not merged into one value plus a
+// register copy).
+template <typename Tin> struct PairLoad;
+template <> struct PairLoad<float> {
+  static __device__ __forceinline__ void bcast(const float* p, float2& a, float2& b) {
+    const float2 v = *reinterpret_cast<const float2*>(p);
+    a = f2(v.x, v.x);
+    b = f2(v.y, v.y);
+  }
+};
+template <> struct PairLoad<uint16_t> {
+  static __device__ __forceinline__ void bcast(const uint16_t* p, float2& a, float2& b) {
+    const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+    uint32_t l0, l1, h0, h1;
+    asm("prmt.b32 %0, %1, 0, 0x1044;" : "=r"(l0) : "r"(v));   // low half << 16
+    asm("prmt.b32 %0, %1, 0, 0x1055;" : "=r"(l1) : "r"(v));   // the same, other selector
+    asm("prmt.b32 %0, %1, 0, 0x3244;" : "=r"(h0) : "r"(v));   // high half in place
+    asm("prmt.b32 %0, %1, 0, 0x3255;" : "=r"(h1) : "r"(v));
+    a = f2(__uint_as_float(l0), __uint_as_float(l1));
+    b = f2(__uint_as_float(h0), __uint_as_float(h1));
+  }
+};
+
+// CARRY (== p.carry) selects what is compiled in: CARRY_NONE (one chunk per row), CARRY_SERIAL
+// (each chunk waits for its predecessor's final state) or CARRY_DECOUPLED (aggregate pass,
+// then look-back); the lighter variants keep no registers for the heavier ones.
+template <int N, typename Tin, int MODE, int CARRY>
+__global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant__ ScanParams p) {
+  using TL = Tile<N>;
+  using SG = Stage<N, Tin, MODE>;
+  constexpr int NS = TL::NS, NG = TL::NG, NPAIR = TL::NPAIR, CPW = TL::CPW, DT = TL::DT;
+  constexpr int NST = SG::NST;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // stage buffers start on a 128-byte boundary (the host requests 128 spare bytes)
   unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
-  __shared__ __align__(8) uint64_t full_bar[NS];
+  __shared__ __align__(8) uint64_t full_bar[MAX_STAGES];
   __shared__ int s_ctl[8];
   __shared__ int s_abort;
 
   const int tid = threadIdx.x;
-  const int g = tid % NG;           // state group of this thread
-  const int dl = tid / NG;          // channel within the tile
-  const int n0 = g * NPT;           // first state of this thread
+  const int lane = tid & 31;
+  const int g = lane % NG;                              // state group of this thread
+  const int cl = (tid >> 5) * CPW + (lane / NG) * CH;   // first of this thread's two channels
+  const int n0 = g * NS;                                // first state of this thread
   uint32_t* hdr = p.ws.hdr;
 
   if (tid == 0) {
     s_ctl[0] = int(atomicAdd(&hdr[H_TICKET], 1u));
     s_ctl[1] = int(ld_relaxed_gpu(&hdr[H_EPOCH]) & 0x3FFFFFFFu);
     s_abort = 0;
-    for (int i = 0; i < NS; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < NST; ++i) mbar_init(&full_bar[i], 1);
     fence_mbar_init();
     prefetch_tmap(&p.tm_x);
     prefetch_tmap(&p.tm_dt);
@@ -231,7 +287,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
   const int j = unit % p.n_tiles;
   const int b = j / p.n_dtiles;
   const int d0 = (j % p.n_dtiles) * DT;
-  const int d = d0 + dl;
+  const int d = d0 + cl;                 // channels d and d + 1 (D is even, so both or neither exist)
   const bool dvalid = d < p.D;
   const int tc = c * p.TC;
   const int te = min(tc + p.TC, p.L);
@@ -243,7 +299,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
   // ---- which passes: decoupled chunks first compute their aggregate, unless the
   // predecessor's final state is already visible.
   bool pass1 = false;
-  if (p.carry == CARRY_DECOUPLED) {
+  if (CARRY == CARRY_DECOUPLED) {
     if (c == 0) {
       pass1 = true;
     } else {
@@ -255,32 +311,33 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
   const int total_stages = n_sub * (pass1 ? 2 : 1);
 
   auto issue = [&](int gs) {
-    const int slot = gs % NS;
+    const int slot = gs % NST;
     const int sub = s_begin + (gs % n_sub);
-    unsigned char* base = smem + slot * SL::STAGE;
-    mbar_arrive_expect_tx(&full_bar[slot], SL::TX_BYTES);
-    tma_load_3d(base + SL::X_OFF, &p.tm_x, d0, sub * T_SUB, b, &full_bar[slot]);
-    tma_load_3d(base + SL::DT_OFF, &p.tm_dt, d0, sub * T_SUB, b, &full_bar[slot]);
-    tma_load_3d(base + SL::TAB_OFF, &p.tm_tab, 0, sub * T_SUB, b, &full_bar[slot]);
-    if (MODE == 1) tma_load_3d(base + SL::AUX_OFF, &p.tm_aux, 0, sub * T_SUB, b, &full_bar[slot]);
-    tma_load_3d(base + SL::ROT_OFF, &p.tm_rot, 0, sub, b, &full_bar[slot]);
+    unsigned char* base = smem + slot * SG::BYTES;
+    mbar_arrive_expect_tx(&full_bar[slot], uint32_t(SG::TX_BYTES));
+    tma_load_3d(base + SG::OFF_X, &p.tm_x, d0, sub * T_SUB, b, &full_bar[slot]);
+    tma_load_3d(base + SG::OFF_DT, &p.tm_dt, d0, sub * T_SUB, b, &full_bar[slot]);
+    tma_load_3d(base + SG::OFF_TAB, &p.tm_tab, 0, sub * T_SUB, b, &full_bar[slot]);
+    if (MODE == 1) tma_load_3d(base + SG::OFF_AUX, &p.tm_aux, 0, sub * T_SUB, b, &full_bar[slot]);
+    tma_load_3d(base + SG::OFF_ROT, &p.tm_rot, 0, sub, b, &full_bar[slot]);
   };
   if (tid == 0) {
-    for (int gs = 0; gs < min(NS, total_stages); ++gs) issue(gs);
+    for (int gs = 0; gs < min(NST, total_stages); ++gs) issue(gs);
   }
 
-  // ---- per-thread constants
-  float2 Ap[NPAIR];
+  // ---- per-thread constants: log2(e) A for both channels, Dskip
+  float2 Ap[CH][NPAIR];
 #pragma unroll
-  for (int q = 0; q < NPAIR; ++q) {
-    Ap[q] = dvalid ? f2(p.A[int64_t(d) * p.N + n0 + 2 * q] * LOG2E_F,
-                        p.A[int64_t(d) * p.N + n0 + 2 * q + 1] * LOG2E_F)
-                   : f2(0.f, 0.f);
-  }
-  const float Ds = dvalid ? p.Dskip[d] : 0.f;
+  for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+    for (int q = 0; q < NPAIR; ++q)
+      Ap[ch][q] = dvalid ? f2(p.A[int64_t(d + ch) * p.N + n0 + 2 * q] * LOG2E_F,
+                              p.A[int64_t(d + ch) * p.N + n0 + 2 * q + 1] * LOG2E_F)
+                         : f2(0.f, 0.f);
+  const float2 Ds = dvalid ? f2(p.Dskip[d], p.Dskip[d + 1]) : f2(0.f, 0.f);
 
   // trapezoid halo: k at the chunk start is h_in + p_tc Bc_{tc-1}, p_tc = (1-lam_tc) dt_tc x_{tc-1}
-  float halo_p = 0.f;
+  float2 halo_p = f2(0.f, 0.f);
   float2 hbr[NPAIR], hbi[NPAIR];
 #pragma unroll
   for (int q = 0; q < NPAIR; ++q) { hbr[q] = f2(0.f, 0.f); hbi[q] = f2(0.f, 0.f); }
@@ -289,16 +346,19 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
     const Tin* dtin = static_cast<const Tin*>(p.dt);
     const Tin* lamin = static_cast<const Tin*>(p.lam);
     const Tin* bsrc;
-    float xprev = 0.f;
+    float2 xprev = f2(0.f, 0.f);
     if (tc > 0) {
-      if (dvalid) xprev = load_in<Tin>(xin, (b * L + tc - 1) * D + d);
+      if (dvalid) xprev = f2(load_in<Tin>(xin, (b * L + tc - 1) * D + d), load_in<Tin>(xin, (b * L + tc - 1) * D + d + 1));
       bsrc = static_cast<const Tin*>(p.Bc) + (b * L + tc - 1) * p.N * 2;
     } else {
-      if (dvalid) xprev = load_in<Tin>(static_cast<const Tin*>(p.x_prev), int64_t(b) * D + d);
+      const Tin* xp = static_cast<const Tin*>(p.x_prev);
+      if (dvalid) xprev = f2(load_in<Tin>(xp, int64_t(b) * D + d), load_in<Tin>(xp, int64_t(b) * D + d + 1));
       bsrc = static_cast<const Tin*>(p.Bc_prev) + int64_t(b) * p.N * 2;
     }
-    const float dt_tc = dvalid ? load_in<Tin>(dtin, (b * L + tc) * D + d) : 0.f;
-    halo_p = (1.f - load_in<Tin>(lamin, b * L + tc)) * dt_tc * xprev;
+    const float2 dt_tc = dvalid ? f2(load_in<Tin>(dtin, (b * L + tc) * D + d), load_in<Tin>(dtin, (b * L + tc) * D + d + 1))
+                                : f2(0.f, 0.f);
+    const float mu = 1.f - load_in<Tin>(lamin, b * L + tc);
+    halo_p = f2(mu * dt_tc.x * xprev.x, mu * dt_tc.y * xprev.y);
 #pragma unroll
     for (int q = 0; q < NPAIR; ++q) {
       const int n = n0 + 2 * q;
@@ -307,78 +367,177 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
     }
   }
 
-  float2 kr[NPAIR], ki[NPAIR];   // state pairs (re), (im) in the current frame
-  float2 Rr[NPAIR], Ri[NPAIR];   // chunk rotation product (pass 1)
-  float sdt_acc = 0.f;           // sum of dt over the chunk (pass 1)
+  float2 kr[CH][NPAIR], ki[CH][NPAIR];   // state pairs (re), (im) in the current frame
+  float2 Rr[NPAIR], Ri[NPAIR];           // chunk rotation product (pass 1)
+  float2 sdt_acc = f2(0.f, 0.f);         // sum of dt over the chunk, both channels (pass 1)
   int gstage = 0;
   bool aborted = false;
 
+  // What a step needs from its scalars: the injection weight of each channel broadcast to a
+  // pair (exp-Euler: dt x; trapezoid: lam dt x + pc), dt (aggregate pass), and for the output
+  // x, pc and E.
+  struct StepIn {
+    float4 tb[2 * NPAIR];  // this step's table entries of the thread's states (Bt, Ct per pair)
+    float2 w0, w1;         // (w_c0, w_c0), (w_c1, w_c1)
+    float2 dv;             // (dt_c0, dt_c1)
+    float2 x, pc;          // (x_c0, x_c1), (pc_c0, pc_c1)
+    float E;
+  };
+  // The output of a finished step: the NG lanes' partial sums of Re(Ct k) are combined, the
+  // trapezoid correction and the D-skip added, and the lanes with g < 2 store the result.
+  const bool odd = (g & 1) != 0;
+  const float Dk = odd ? Ds.y : Ds.x;
+  const bool store_one = NG > 1 && g < 2 && dvalid;
+  auto finish_y = [&](float2 yp, const StepIn& sc, float* yrow, bool ok) {
+    if (NG == 1) {
+      const float o0 = fmaf(Ds.x, sc.x.x, fmaf(-sc.pc.x, sc.E, yp.x));
+      const float o1 = fmaf(Ds.y, sc.x.y, fmaf(-sc.pc.y, sc.E, yp.y));
+      if (ok && dvalid) {
+        if (p.y_vec2) {
+          __stcs(reinterpret_cast<float2*>(yrow), f2(o0, o1));
+        } else {
+          __stcs(yrow, o0);
+          __stcs(yrow + 1, o1);
+        }
+      }
+    } else {
+      // lanes g and g^1 trade the channel they do not keep, then the group sums
+      float keep = odd ? yp.y : yp.x;
+      keep += __shfl_xor_sync(0xffffffffu, odd ? yp.x : yp.y, 1);
+#pragma unroll
+      for (int o = 2; o < NG; o <<= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+      const float o = fmaf(Dk, odd ? sc.x.y : sc.x.x, fmaf(-(odd ? sc.pc.y : sc.pc.x), sc.E, keep));
+      if (ok && store_one) __stcs(yrow + g, o);
+    }
+  };
+
   // One pass over the chunk's sub-chunks. WITH_Y: write y; otherwise accumulate the
-  // aggregate's sum of dt and rotation.
+  // aggregate's sum of dt and rotation. The time loop is software-pipelined: step t+1's
+  // scalars and decays are computed during step t, and step t's output is reduced and
+  // stored during step t+1; two steps per iteration with the register sets swapped, so no
+  // value is copied at the loop edge.
   auto run_pass = [&](auto with_y_tag) {
     constexpr bool WITH_Y = decltype(with_y_tag)::value;
     for (int i = 0; i < n_sub; ++i, ++gstage) {
-      const int slot = gstage % NS;
-      if (!wait_bar_bounded(&full_bar[slot], uint32_t(gstage / NS) & 1u)) s_abort = 1;
-      const unsigned char* base = smem + slot * SL::STAGE;
-      const Tin* sx = reinterpret_cast<const Tin*>(base + SL::X_OFF);
-      const Tin* sdtp = reinterpret_cast<const Tin*>(base + SL::DT_OFF);
-      const float4* stab = reinterpret_cast<const float4*>(base + SL::TAB_OFF);
-      const float4* saux = reinterpret_cast<const float4*>(base + SL::AUX_OFF);
-      const float4* srot = reinterpret_cast<const float4*>(base + SL::ROT_OFF);
+      const int slot = gstage % NST;
+      if (!wait_bar_bounded(&full_bar[slot], uint32_t(gstage / NST) & 1u)) s_abort = 1;
+      const unsigned char* base = smem + slot * SG::BYTES;
+      const Tin* sx = reinterpret_cast<const Tin*>(base + SG::OFF_X) + cl;
+      const Tin* sdtp = reinterpret_cast<const Tin*>(base + SG::OFF_DT) + cl;
+      const float4* stab = reinterpret_cast<const float4*>(base + SG::OFF_TAB) + g * NS;
+      const float4* saux = reinterpret_cast<const float4*>(base + SG::OFF_AUX);
+      const float4* srot = reinterpret_cast<const float4*>(base + SG::OFF_ROT);
       const int t_sub0 = (s_begin + i) * T_SUB;
       const int nt = min(T_SUB, te - t_sub0);
-      float dt_next = smem_in<Tin>(sdtp, dl);
-#pragma unroll 2
-      for (int tt = 0; tt < nt; ++tt) {
-        const float xv = smem_in<Tin>(sx, tt * DT + dl);
-        float dv, w, pc = 0.f, E = 0.f;
+      // local index of the chunk's last step, where the trapezoid look-ahead p_{t+1} is left
+      // to the next chunk's halo (-1 when that step lies in a later sub-chunk)
+      const int t_last = te - 1 - t_sub0 < T_SUB ? te - 1 - t_sub0 : -1;
+      float* yrow = p.y + (b * L + t_sub0) * D + d;
+
+      // table entries and scalars of step tt (rows tt of x, aux and the table, tt and tt + 1 of
+      // dt; all staged) and the decays' dt broadcast pairs
+      auto load_step = [&](int tt, StepIn& s, float2& dd0, float2& dd1) {
+        const float4* trow = stab + tt * N;
+#pragma unroll
+        for (int k = 0; k < 2 * NPAIR; ++k) s.tb[k] = trow[k];
+        float2 xx0, xx1;
+        PairLoad<Tin>::bcast(sx + tt * DT, xx0, xx1);
+        PairLoad<Tin>::bcast(sdtp + tt * DT, dd0, dd1);
+        s.x = f2(xx0.x, xx1.x);
+        s.dv = f2(dd0.x, dd1.x);
         if (MODE == 0) {
-          dv = smem_in<Tin>(sdtp, tt * DT + dl);
-          w = dv * xv;
+          s.w0 = mul2(dd0, xx0);
+          s.w1 = mul2(dd1, xx1);
+          s.pc = f2(0.f, 0.f);
+          s.E = 0.f;
         } else {
-          dv = dt_next;
-          dt_next = smem_in<Tin>(sdtp, (tt + 1) * DT + dl);
-          const float4 a = saux[tt];
-          const bool last = (t_sub0 + tt == te - 1);
-          pc = last ? 0.f : a.y * dt_next * xv;
-          w = fmaf(a.x * dv, xv, pc);
-          E = a.z;
+          float2 nn0, nn1;
+          PairLoad<Tin>::bcast(sdtp + (tt + 1) * DT, nn0, nn1);
+          const float4 a = saux[2 * tt];
+          const float4 e = saux[2 * tt + 1];
+          const float2 lam2 = f2(a.x, a.y), mu2 = f2(a.z, a.w);
+          float2 pc0 = mul2(mu2, mul2(nn0, xx0));
+          float2 pc1 = mul2(mu2, mul2(nn1, xx1));
+          if (tt == t_last) { pc0 = f2(0.f, 0.f); pc1 = f2(0.f, 0.f); }
+          s.w0 = fma2(mul2(lam2, dd0), xx0, pc0);
+          s.w1 = fma2(mul2(lam2, dd1), xx1, pc1);
+          s.pc = f2(pc0.x, pc1.x);
+          s.E = e.x;
         }
-        if (!WITH_Y) sdt_acc += dv;
-        const float2 dd = f2(dv, dv), ww = f2(w, w);
+      };
+
+      float2 ypend = f2(0.f, 0.f);
+      // One step with this step's scalars `cur` and decays `rc`; loads step tt + 1's into
+      // `nxt` / `rn` and finishes step tt - 1's output, whose scalars `nxt` held.
+      auto step = [&](int tt, const StepIn& cur, const float2 (&rc)[CH][NPAIR], StepIn& nxt,
+                      float2 (&rn)[CH][NPAIR]) {
+        const StepIn prev = nxt;
+        float2 dd0, dd1;
+        load_step(tt + 1, nxt, dd0, dd1);
+        if (WITH_Y) {
+          finish_y(ypend, prev, yrow, tt > 0);
+          if (tt > 0) yrow += D;
+        } else {
+          sdt_acc = f2(sdt_acc.x + cur.dv.x, sdt_acc.y + cur.dv.y);
+        }
         float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
-        const float4* trow = stab + tt * N + 2 * g * NPAIR;
 #pragma unroll
         for (int q = 0; q < NPAIR; ++q) {
-          const float4 bt = trow[2 * q];
-          const float2 z = mul2(dd, Ap[q]);
-          const float2 r = f2(ex2_approx(z.x), ex2_approx(z.y));
-          kr[q] = fma2(r, kr[q], mul2(ww, f2(bt.x, bt.y)));
-          ki[q] = fma2(r, ki[q], mul2(ww, f2(bt.z, bt.w)));
+          rn[0][q] = ex2_pair(mul2(dd0, Ap[0][q]));
+          rn[1][q] = ex2_pair(mul2(dd1, Ap[1][q]));
+          const float4 bt = cur.tb[2 * q];
+          const float2 btr = f2(bt.x, bt.y), bti = f2(bt.z, bt.w);
+          kr[0][q] = fma2(rc[0][q], kr[0][q], mul2(cur.w0, btr));
+          ki[0][q] = fma2(rc[0][q], ki[0][q], mul2(cur.w0, bti));
+          kr[1][q] = fma2(rc[1][q], kr[1][q], mul2(cur.w1, btr));
+          ki[1][q] = fma2(rc[1][q], ki[1][q], mul2(cur.w1, bti));
           if (WITH_Y) {
-            const float4 ct = trow[2 * q + 1];
-            acc0 = fma2(f2(ct.x, ct.y), kr[q], acc0);
-            acc1 = fma2(f2(ct.z, ct.w), ki[q], acc1);
+            const float4 ct = cur.tb[2 * q + 1];
+            const float2 ctr = f2(ct.x, ct.y), cti = f2(ct.z, ct.w);
+            acc0 = fma2(cti, ki[0][q], fma2(ctr, kr[0][q], acc0));
+            acc1 = fma2(cti, ki[1][q], fma2(ctr, kr[1][q], acc1));
           }
         }
-        if (WITH_Y) {
-          float yv = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        if (WITH_Y) ypend = f2(acc0.x + acc0.y, acc1.x + acc1.y);
+      };
+
+      StepIn sa, sb;
+      float2 ra[CH][NPAIR], rb[CH][NPAIR];
+      {
+        float2 dd0, dd1;
+        load_step(0, sa, dd0, dd1);
 #pragma unroll
-          for (int o = NG / 2; o > 0; o >>= 1) yv += __shfl_xor_sync(0xffffffffu, yv, o);
-          yv = fmaf(Ds, xv, fmaf(-pc, E, yv));
-          if (g == 0 && dvalid) __stcs(p.y + (b * L + t_sub0 + tt) * D + d, yv);
+        for (int q = 0; q < NPAIR; ++q) {
+          ra[0][q] = ex2_pair(mul2(dd0, Ap[0][q]));
+          ra[1][q] = ex2_pair(mul2(dd1, Ap[1][q]));
         }
+        sb = sa;
+      }
+      int tt = 0;
+#pragma unroll 1
+      for (; tt + 1 < nt; tt += 2) {
+        step(tt, sa, ra, sb, rb);
+        step(tt + 1, sb, rb, sa, ra);
+      }
+      // yrow now points at the row of the last step taken, whose output is still pending
+      if (tt < nt) {
+        step(tt, sa, ra, sb, rb);
+        if (WITH_Y) finish_y(ypend, sa, yrow, true);
+      } else if (WITH_Y) {
+        finish_y(ypend, sb, yrow, true);
       }
       // frame reset: rotate the state by e^{i Phi_last} of this sub-chunk
 #pragma unroll
       for (int q = 0; q < NPAIR; ++q) {
         const float4 rr = srot[n0 / 2 + q];
         const float2 cc = f2(rr.x, rr.z), ss = f2(rr.y, rr.w), nss = f2(-rr.y, -rr.w);
-        const float2 nr = fma2(cc, kr[q], mul2(nss, ki[q]));
-        const float2 ni = fma2(cc, ki[q], mul2(ss, kr[q]));
-        kr[q] = nr;
-        ki[q] = ni;
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) {
+          const float2 nr = fma2(cc, kr[ch][q], mul2(nss, ki[ch][q]));
+          const float2 ni = fma2(cc, ki[ch][q], mul2(ss, kr[ch][q]));
+          kr[ch][q] = nr;
+          ki[ch][q] = ni;
+        }
         if (!WITH_Y) {
           const float2 r2 = fma2(cc, Rr[q], mul2(nss, Ri[q]));
           const float2 i2 = fma2(cc, Ri[q], mul2(ss, Rr[q]));
@@ -388,13 +547,14 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
       }
       __syncthreads();
       if (s_abort) { aborted = true; return; }
-      if (tid == 0 && gstage + NS < total_stages) issue(gstage + NS);
+      if (tid == 0 && gstage + NST < total_stages) issue(gstage + NST);
     }
   };
 
   // ---- per-state helpers on the workspace records (float2 per state, states contiguous)
+  auto rec_of = [&](float2* base, int u, int ch) { return base + (int64_t(u) * DT + cl + ch) * p.N + n0; };
   auto load_states = [&](const float2* rec, float2* re, float2* im) {
-    const float4* r4 = reinterpret_cast<const float4*>(rec + n0);
+    const float4* r4 = reinterpret_cast<const float4*>(rec);
 #pragma unroll
     for (int q = 0; q < NPAIR; ++q) {
       const float4 v = __ldcg(r4 + q);
@@ -403,7 +563,7 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
     }
   };
   auto store_states = [&](float2* rec, const float2* re, const float2* im) {
-    float4* r4 = reinterpret_cast<float4*>(rec + n0);
+    float4* r4 = reinterpret_cast<float4*>(rec);
 #pragma unroll
     for (int q = 0; q < NPAIR; ++q) __stcg(r4 + q, make_float4(re[q].x, im[q].x, re[q].y, im[q].y));
   };
@@ -414,56 +574,60 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
     if (tid == 0 && !silent) st_release_gpu(&p.ws.flags[unit], (epoch << 2) | status);
   };
 
-  float2 hr[NPAIR], hi[NPAIR];   // carry-in h_{tc-1}
+  float2 hr[CH][NPAIR], hi[CH][NPAIR];   // carry-in h_{tc-1}
 #pragma unroll
-  for (int q = 0; q < NPAIR; ++q) { hr[q] = f2(0.f, 0.f); hi[q] = f2(0.f, 0.f); }
+  for (int ch = 0; ch < CH; ++ch)
+#pragma unroll
+    for (int q = 0; q < NPAIR; ++q) { hr[ch][q] = f2(0.f, 0.f); hi[ch][q] = f2(0.f, 0.f); }
   bool incl_published = false;
   const bool has_h0 = (p.h0 != nullptr) && dvalid;
-  const float2* h0rec = p.h0 ? reinterpret_cast<const float2*>(p.h0) + (int64_t(b) * p.D + (dvalid ? d : 0)) * p.N : nullptr;
+  auto h0rec = [&](int ch) {
+    return reinterpret_cast<const float2*>(p.h0) + (int64_t(b) * p.D + d + ch) * p.N + n0;
+  };
 
-  if (pass1) {
+  if (CARRY == CARRY_DECOUPLED && pass1) {
     // ---- pass 1: aggregate from a zero carry-in
 #pragma unroll
     for (int q = 0; q < NPAIR; ++q) {
-      kr[q] = mul2(f2(halo_p, halo_p), hbr[q]);
-      ki[q] = mul2(f2(halo_p, halo_p), hbi[q]);
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch) {
+        const float hp = ch ? halo_p.y : halo_p.x;
+        kr[ch][q] = mul2(f2(hp, hp), hbr[q]);
+        ki[ch][q] = mul2(f2(hp, hp), hbi[q]);
+      }
       Rr[q] = f2(1.f, 1.f);
       Ri[q] = f2(0.f, 0.f);
     }
     run_pass(std::false_type{});
     if (!aborted) {
-      float2* aggrec = p.ws.agg + (int64_t(unit) * DT + dl) * p.N;
       if (!silent) {
-        store_states(aggrec, kr, ki);
-        if (g == 0) __stcg(p.ws.sdt + int64_t(unit) * DT + dl, sdt_acc);
-        if (dl == 0) store_states(p.ws.crot + int64_t(unit) * p.N, Rr, Ri);
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) store_states(rec_of(p.ws.agg, unit, ch), kr[ch], ki[ch]);
+        if (g == 0) __stcg(reinterpret_cast<float2*>(p.ws.sdt + int64_t(unit) * DT + cl), sdt_acc);
+        if (cl == 0) store_states(p.ws.crot + int64_t(unit) * p.N + n0, Rr, Ri);
       }
       publish(ST_AGG);
 
       // ---- decoupled look-back over windows of 32 predecessors
-      float Sd = 0.f;
+      float2 Sd = f2(0.f, 0.f);
       float2 Qr[NPAIR], Qi[NPAIR];
 #pragma unroll
       for (int q = 0; q < NPAIR; ++q) { Qr[q] = f2(1.f, 1.f); Qi[q] = f2(0.f, 0.f); }
       // h_in += exp(A Sd) Q * rec   (the accumulated multiplier of the chunks seen so far)
-      auto accumulate = [&](const float2* rec, bool is_h0) {
+      auto accumulate = [&](int u2, bool is_h0, bool is_incl) {
 #pragma unroll
-        for (int q = 0; q < NPAIR; ++q) {
-          float2 ur, ui;
-          if (is_h0) {
-            const float2 a = h0rec[n0 + 2 * q], bb = h0rec[n0 + 2 * q + 1];
-            ur = f2(a.x, bb.x);
-            ui = f2(a.y, bb.y);
-          } else {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(rec + n0) + q);
-            ur = f2(v.x, v.z);
-            ui = f2(v.y, v.w);
+        for (int ch = 0; ch < CH; ++ch) {
+          const float2* rec = is_h0 ? h0rec(ch) : rec_of(is_incl ? p.ws.inc : p.ws.agg, u2, ch);
+          const float sd = ch ? Sd.y : Sd.x;
+#pragma unroll
+          for (int q = 0; q < NPAIR; ++q) {
+            const float4 v = is_h0 ? reinterpret_cast<const float4*>(rec)[q] : __ldcg(reinterpret_cast<const float4*>(rec) + q);
+            const float2 ur = f2(v.x, v.z), ui = f2(v.y, v.w);
+            const float2 e = ex2_pair(mul2(f2(sd, sd), Ap[ch][q]));
+            const float2 mr = mul2(e, Qr[q]), mi = mul2(e, Qi[q]);
+            hr[ch][q] = fma2(mr, ur, fma2(f2(-mi.x, -mi.y), ui, hr[ch][q]));
+            hi[ch][q] = fma2(mr, ui, fma2(mi, ur, hi[ch][q]));
           }
-          const float2 zz = mul2(f2(Sd, Sd), Ap[q]);
-          const float2 e = f2(ex2_approx(zz.x), ex2_approx(zz.y));
-          const float2 mr = mul2(e, Qr[q]), mi = mul2(e, Qi[q]);
-          hr[q] = fma2(mr, ur, fma2(f2(-mi.x, -mi.y), ui, hr[q]));
-          hi[q] = fma2(mr, ui, fma2(mi, ur, hi[q]));
         }
       };
       int pred = c - 1;
@@ -501,8 +665,9 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
         const int count = s_ctl[3], found = s_ctl[4], tout = s_ctl[5];
         for (int i = 0; i < count; ++i) {
           const int u2 = unit_of(pred - i);
-          accumulate(p.ws.agg + (int64_t(u2) * DT + dl) * p.N, false);
-          Sd += __ldcg(p.ws.sdt + int64_t(u2) * DT + dl);
+          accumulate(u2, false, false);
+          const float2 sd2 = __ldcg(reinterpret_cast<const float2*>(p.ws.sdt + int64_t(u2) * DT + cl));
+          Sd = f2(Sd.x + sd2.x, Sd.y + sd2.y);
           const float4* cr4 = reinterpret_cast<const float4*>(p.ws.crot + int64_t(u2) * p.N + n0);
 #pragma unroll
           for (int q = 0; q < NPAIR; ++q) {
@@ -518,9 +683,9 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
         if (found) {
           const int cp = pred - count;
           if (cp < 0) {
-            if (has_h0) accumulate(nullptr, true);
+            if (has_h0) accumulate(0, true, false);
           } else {
-            accumulate(p.ws.inc + (int64_t(unit_of(cp)) * DT + dl) * p.N, false);
+            accumulate(unit_of(cp), false, true);
           }
           break;
         }
@@ -529,21 +694,25 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
       }
       // ---- publish this chunk's final state: h_end = P h_in + U, P = exp(A sum dt) R
 #pragma unroll
-      for (int q = 0; q < NPAIR; ++q) {
-        const float2 zz = mul2(f2(sdt_acc, sdt_acc), Ap[q]);
-        const float2 e = f2(ex2_approx(zz.x), ex2_approx(zz.y));
-        const float2 pr = mul2(e, Rr[q]), pi = mul2(e, Ri[q]);
-        const float2 er = fma2(pr, hr[q], fma2(f2(-pi.x, -pi.y), hi[q], kr[q]));
-        const float2 ei = fma2(pr, hi[q], fma2(pi, hr[q], ki[q]));
-        kr[q] = er;   // reuse as scratch for the store
-        ki[q] = ei;
+      for (int ch = 0; ch < CH; ++ch) {
+        const float sd = ch ? sdt_acc.y : sdt_acc.x;
+#pragma unroll
+        for (int q = 0; q < NPAIR; ++q) {
+          const float2 e = ex2_pair(mul2(f2(sd, sd), Ap[ch][q]));
+          const float2 pr = mul2(e, Rr[q]), pi = mul2(e, Ri[q]);
+          const float2 er = fma2(pr, hr[ch][q], fma2(f2(-pi.x, -pi.y), hi[ch][q], kr[ch][q]));
+          const float2 ei = fma2(pr, hi[ch][q], fma2(pi, hr[ch][q], ki[ch][q]));
+          kr[ch][q] = er;   // reuse as scratch for the store
+          ki[ch][q] = ei;
+        }
+        if (!silent) store_states(rec_of(p.ws.inc, unit, ch), kr[ch], ki[ch]);
       }
-      if (!silent) store_states(p.ws.inc + (int64_t(unit) * DT + dl) * p.N, kr, ki);
       publish(ST_INCL);
       incl_published = true;
     }
-  } else if (c > 0) {
-    // ---- serial carry: wait for the predecessor's final state
+  } else if (CARRY != CARRY_NONE && c > 0) {
+    // ---- serial carry, or a decoupled chunk whose predecessor had already published its
+    // final state when this block started: wait for (or take) that final state
     if (tid == 0) {
       const uint32_t* fp = &p.ws.flags[unit_of(c - 1)];
       long long polls = 0;
@@ -556,38 +725,55 @@ __global__ void __launch_bounds__(THREADS) scan_kernel(const __grid_constant__ S
       if (tout) record_error(hdr, ERR_LOOKBACK, unit, c - 1);
     }
     __syncthreads();
-    if (!s_ctl[5]) load_states(p.ws.inc + (int64_t(unit_of(c - 1)) * DT + dl) * p.N, hr, hi);
+    if (!s_ctl[5]) {
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch) load_states(rec_of(p.ws.inc, unit_of(c - 1), ch), hr[ch], hi[ch]);
+    }
   } else if (has_h0) {
 #pragma unroll
-    for (int q = 0; q < NPAIR; ++q) {
-      const float2 a = h0rec[n0 + 2 * q], bb = h0rec[n0 + 2 * q + 1];
-      hr[q] = f2(a.x, bb.x);
-      hi[q] = f2(a.y, bb.y);
+    for (int ch = 0; ch < CH; ++ch) {
+      const float4* r4 = reinterpret_cast<const float4*>(h0rec(ch));
+#pragma unroll
+      for (int q = 0; q < NPAIR; ++q) {
+        const float4 v = r4[q];
+        hr[ch][q] = f2(v.x, v.z);
+        hi[ch][q] = f2(v.y, v.w);
+      }
     }
   }
 
   if (!aborted) {
     // ---- pass 2: from the carry-in, writing y
 #pragma unroll
-    for (int q = 0; q < NPAIR; ++q) {
-      kr[q] = fma2(f2(halo_p, halo_p), hbr[q], hr[q]);
-      ki[q] = fma2(f2(halo_p, halo_p), hbi[q], hi[q]);
+    for (int ch = 0; ch < CH; ++ch) {
+      const float hp = ch ? halo_p.y : halo_p.x;
+#pragma unroll
+      for (int q = 0; q < NPAIR; ++q) {
+        kr[ch][q] = fma2(f2(hp, hp), hbr[q], hr[ch][q]);
+        ki[ch][q] = fma2(f2(hp, hp), hbi[q], hi[ch][q]);
+      }
     }
     run_pass(std::true_type{});
   }
   if (!aborted) {
-    if (!incl_published) {
-      if (!silent) store_states(p.ws.inc + (int64_t(unit) * DT + dl) * p.N, kr, ki);
+    if (CARRY != CARRY_NONE && !incl_published) {
+      if (!silent) {
+#pragma unroll
+        for (int ch = 0; ch < CH; ++ch) store_states(rec_of(p.ws.inc, unit, ch), kr[ch], ki[ch]);
+      }
       publish(ST_INCL);
     }
-    if (c == p.n_chunks - 1 && p.h_last != nullptr && dvalid)
-      store_states(reinterpret_cast<float2*>(p.h_last) + (int64_t(b) * p.D + d) * p.N, kr, ki);
+    if (c == p.n_chunks - 1 && p.h_last != nullptr && dvalid) {
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch)
+        store_states(reinterpret_cast<float2*>(p.h_last) + (int64_t(b) * p.D + d + ch) * p.N + n0, kr[ch], ki[ch]);
+    }
   } else {
     // a tile copy never arrived: report, drain what is still in flight (bounded), leave
     if (tid == 0) {
       record_error(hdr, ERR_PIPELINE, unit, -1);
-      for (int gs = gstage; gs < min(gstage + NS, total_stages); ++gs)
-        wait_bar_bounded(&full_bar[gs % NS], uint32_t(gs / NS) & 1u);
+      for (int gs = gstage; gs < min(gstage + NST, total_stages); ++gs)
+        wait_bar_bounded(&full_bar[gs % NST], uint32_t(gs / NST) & 1u);
     }
   }
 

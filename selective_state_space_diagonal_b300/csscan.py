@@ -38,7 +38,7 @@ class CsscanError(RuntimeError):
 
 
 class csscan_options_t(ctypes.Structure):
-    _fields_ = [("rows_per_cta", ctypes.c_int32), ("chunk_len", ctypes.c_int32), ("carry", ctypes.c_int32),
+    _fields_ = [("cta_warps", ctypes.c_int32), ("chunk_len", ctypes.c_int32), ("carry", ctypes.c_int32),
                 ("silent_chunk", ctypes.c_int32), ("poll_limit", ctypes.c_int64),
                 ("scan_begin", ctypes.c_void_p), ("scan_end", ctypes.c_void_p)]
 
@@ -112,11 +112,11 @@ def csscan_forward(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode: int, stream=
 
 def csscan_forward_ex(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode: int, stream=None, *, chunk_len: int = 0,
                       carry: int = 0, silent_chunk: int = -1, poll_limit: int = 0, scan_begin=None,
-                      scan_end=None) -> int:
+                      scan_end=None, cta_warps: int = 0) -> int:
     """csscan_forward with launch options; returns the status instead of raising. scan_begin /
     scan_end are optional torch.cuda.Event objects recorded around the scan kernel."""
     ev = lambda e: None if e is None else e.cuda_event
-    o = csscan_options_t(0, chunk_len, carry, silent_chunk, poll_limit, ev(scan_begin), ev(scan_end))
+    o = csscan_options_t(cta_warps, chunk_len, carry, silent_chunk, poll_limit, ev(scan_begin), ev(scan_end))
     return load_library().csscan_forward_ex(*_args(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode),
                                             ctypes.byref(o), _stream_handle(stream))
 

@@ -99,6 +99,17 @@ def test_forced_carry(carry, chunk_len, mode, dtype):
     check(inp, y, f"carry{carry}:chunk{chunk_len}:m{mode}:{dtype}")
 
 
+@pytest.mark.parametrize("carry", [1, 2])
+def test_more_chunks_than_block_slots(carry):
+    """More chunk-units (8 rows x 66 chunks) than the GPU holds blocks at once, so later
+    chunks start after their predecessors have finished: the decoupled carry then takes the
+    predecessor's published final state instead of computing its own aggregate."""
+    w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=8, L=2100, D=24)
+    inp = wl.generate(w)
+    y = gu.run_gpu(gu.to_device(inp), w.mode, carry=carry, chunk_len=32)
+    check(inp, y, f"late-start:carry{carry}")
+
+
 def test_dskip_zero():
     w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=2, L=400, D=32)
     inp = wl.generate(w)
