@@ -91,6 +91,12 @@ def aggregate_value(elements_per_rank_step: int, steps: int, world: int, max_sec
     return elements_per_rank_step * steps * world / max_seconds / 1e9
 
 
+def rank_workload(w: wl.Workload, rank: int) -> wl.Workload:
+    """The problem rank `rank` scans: the same shape and distributions with its own seed, so
+    that the ranks' problems are independent (rank 0 keeps the workload's own seed)."""
+    return w if rank == 0 else w.with_shape(seed=w.seed + 1009 * rank)
+
+
 def barrier():
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
@@ -263,7 +269,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     csscan.load_library()
-    w = wl.WORKLOADS[args.workload]
+    w = rank_workload(wl.WORKLOADS[args.workload], rank)
     inp = wl.generate(w)
 
     def pinned(a):

@@ -18,7 +18,7 @@
  *     alpha = exp(dt A), gamma = dt; Exp-Trapezoidal row: beta = (1 - lam) dt exp(dt A),
  *     gamma = lam dt) and the complex-state section (real decay A, input-dependent phase
  *     e^{i theta});
- *   - "状态空间模型的对偶谱理论 2026" (blog.lonae.com), section 3.1: the sequential loop, y read
+ *   - "状态空间模型的对偶谱理论 2026" (blog.lonae.com), section 3.2 (pseudocode listing): the sequential loop, y read
  *     from the updated state and summed over the state index;
  *   - "Mamba-3: 选择性状态空间模型的下一代架构" (metaphor-xennon), section 2.2: y = C h + D x.
  *   The exponential in beta is read as the full complex a_t of the current step, and theta

@@ -12,7 +12,7 @@ computes and which page it follows:
 * the transition factor and the two injection rules follow the discretisation table and the
   complex-state section of "Mamba-3 paper story" (ai.tomabc.com);
 * the loop shape (update h, then read y from the updated h) follows the sequential
-  pseudocode of "状态空间模型的对偶谱理论 2026" (blog.lonae.com), section 3.1, and the
+  pseudocode listing of "状态空间模型的对偶谱理论 2026" (blog.lonae.com), section 3.2, and the
   D-skip follows "Mamba-3: 选择性状态空间模型的下一代架构" (metaphor-xennon), section 2.2.
 
 This module only marshals numpy arrays into that library (``ctypes``) and builds it.

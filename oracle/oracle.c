@@ -15,7 +15,7 @@
  *  - "Mamba-3 paper story" (ai.tomabc.com), the discretisation table (rows Exp-Euler and
  *    Exp-Trapezoidal: alpha_t, beta_t, gamma_t) and the section on the complex state space
  *    (real decay A times an input-dependent phase e^{i theta}).
- *  - "状态空间模型的对偶谱理论 2026" (blog.lonae.com), section 3.1, the sequential pseudocode
+ *  - "状态空间模型的对偶谱理论 2026" (blog.lonae.com), section 3.2, the sequential pseudocode listing
  *    (update h first, then read y from the updated h, summing over the state index).
  *  - "Mamba-3: 选择性状态空间模型的下一代架构" (metaphor-xennon), sections 2.1-2.2:
  *    y = C h + D x.
@@ -106,7 +106,7 @@ typedef struct {
 } job_t;
 
 /* One (b, d) row: the sequential recurrence over t for every state n, then the output.
- * Loop form as in the sequential pseudocode of "状态空间模型的对偶谱理论 2026", section 3.1:
+ * Loop form as in the sequential pseudocode listing of "状态空间模型的对偶谱理论 2026", section 3.2:
  * h is updated first and y_t is read from the updated h_t, summed over n; the D-skip term
  * follows "Mamba-3: 选择性状态空间模型的下一代架构", section 2.2 (y = C h + D x). */
 static void run_row(const job_t* j, int64_t b, int64_t d, cplx* h) {
