@@ -205,28 +205,38 @@ __device__ __forceinline__ bool wait_bar_bounded(uint64_t* bar, uint32_t parity)
   return false;
 }
 
-// Two adjacent channels (c0, c1) of one staged row, each widened to float32 and broadcast to
-// both halves of a pair: returns (c0, c0) and (c1, c1). The bf16 case widens with byte
-// permutes (two different selectors, so the two halves are not merged into one value plus a
-// register copy).
+// Two adjacent channels of one staged row, widened to float32 and broadcast to both halves of
+// a pair: returns (kept, kept) and (other, other), where a lane with swap = 1 keeps the second
+// channel. The bf16 case widens with byte permutes whose selectors the lane holds in registers
+// (two equivalent selectors per half, so that the two copies are not merged into one value plus
+// a register copy).
+struct Selectors {
+  uint32_t k1, k2, o1, o2;   // kept channel (twice), other channel (twice)
+};
+__device__ __forceinline__ Selectors make_selectors(int swap) {
+  // 0x1044 / 0x1055: the low 16 bits moved to the top (bytes 4, 5 are the zero operand);
+  // 0x3244 / 0x3255: the high 16 bits in place
+  return swap ? Selectors{0x3244u, 0x3255u, 0x1044u, 0x1055u} : Selectors{0x1044u, 0x1055u, 0x3244u, 0x3255u};
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t v, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(v), "r"(sel));
+  return d;
+}
 template <typename Tin> struct PairLoad;
 template <> struct PairLoad<float> {
-  static __device__ __forceinline__ void bcast(const float* p, float2& a, float2& b) {
+  static __device__ __forceinline__ void bcast(const float* p, const Selectors& sl, int swap, float2& a, float2& b) {
     const float2 v = *reinterpret_cast<const float2*>(p);
-    a = f2(v.x, v.x);
-    b = f2(v.y, v.y);
+    const float k = swap ? v.y : v.x, o = swap ? v.x : v.y;
+    a = f2(k, k);
+    b = f2(o, o);
   }
 };
 template <> struct PairLoad<uint16_t> {
-  static __device__ __forceinline__ void bcast(const uint16_t* p, float2& a, float2& b) {
+  static __device__ __forceinline__ void bcast(const uint16_t* p, const Selectors& sl, int, float2& a, float2& b) {
     const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
-    uint32_t l0, l1, h0, h1;
-    asm("prmt.b32 %0, %1, 0, 0x1044;" : "=r"(l0) : "r"(v));   // low half << 16
-    asm("prmt.b32 %0, %1, 0, 0x1055;" : "=r"(l1) : "r"(v));   // the same, other selector
-    asm("prmt.b32 %0, %1, 0, 0x3244;" : "=r"(h0) : "r"(v));   // high half in place
-    asm("prmt.b32 %0, %1, 0, 0x3255;" : "=r"(h1) : "r"(v));
-    a = f2(__uint_as_float(l0), __uint_as_float(l1));
-    b = f2(__uint_as_float(h0), __uint_as_float(h1));
+    a = f2(__uint_as_float(prmt(v, sl.k1)), __uint_as_float(prmt(v, sl.k2)));
+    b = f2(__uint_as_float(prmt(v, sl.o1)), __uint_as_float(prmt(v, sl.o2)));
   }
 };
 
@@ -252,6 +262,10 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   const int g = lane % NG;                              // state group of this thread
   const int cl = (tid >> 5) * CPW + (lane / NG) * CH;   // first of this thread's two channels
   const int n0 = g * NS;                                // first state of this thread
+  // Lanes g and g^1 split a channel pair's states; the odd one keeps (outputs) the second
+  // channel, and every per-channel pair of this thread is ordered (kept, other).
+  const int swp = NG > 1 ? (g & 1) : 0;
+  const Selectors sel = make_selectors(swp);
   uint32_t* hdr = p.ws.hdr;
 
   if (tid == 0) {
@@ -289,6 +303,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   const int d0 = (j % p.n_dtiles) * DT;
   const int d = d0 + cl;                 // channels d and d + 1 (D is even, so both or neither exist)
   const bool dvalid = d < p.D;
+  auto chan = [&](int ch) { return d + (ch ^ swp); };   // channel of this thread's pair slot ch
   const int tc = c * p.TC;
   const int te = min(tc + p.TC, p.L);
   const int s_begin = tc / T_SUB;
@@ -331,10 +346,10 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   for (int ch = 0; ch < CH; ++ch)
 #pragma unroll
     for (int q = 0; q < NPAIR; ++q)
-      Ap[ch][q] = dvalid ? f2(p.A[int64_t(d + ch) * p.N + n0 + 2 * q] * LOG2E_F,
-                              p.A[int64_t(d + ch) * p.N + n0 + 2 * q + 1] * LOG2E_F)
+      Ap[ch][q] = dvalid ? f2(p.A[int64_t(chan(ch)) * p.N + n0 + 2 * q] * LOG2E_F,
+                              p.A[int64_t(chan(ch)) * p.N + n0 + 2 * q + 1] * LOG2E_F)
                          : f2(0.f, 0.f);
-  const float2 Ds = dvalid ? f2(p.Dskip[d], p.Dskip[d + 1]) : f2(0.f, 0.f);
+  const float2 Ds = dvalid ? f2(p.Dskip[chan(0)], p.Dskip[chan(1)]) : f2(0.f, 0.f);
 
   // trapezoid halo: k at the chunk start is h_in + p_tc Bc_{tc-1}, p_tc = (1-lam_tc) dt_tc x_{tc-1}
   float2 halo_p = f2(0.f, 0.f);
@@ -348,14 +363,14 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
     const Tin* bsrc;
     float2 xprev = f2(0.f, 0.f);
     if (tc > 0) {
-      if (dvalid) xprev = f2(load_in<Tin>(xin, (b * L + tc - 1) * D + d), load_in<Tin>(xin, (b * L + tc - 1) * D + d + 1));
+      if (dvalid) xprev = f2(load_in<Tin>(xin, (b * L + tc - 1) * D + chan(0)), load_in<Tin>(xin, (b * L + tc - 1) * D + chan(1)));
       bsrc = static_cast<const Tin*>(p.Bc) + (b * L + tc - 1) * p.N * 2;
     } else {
       const Tin* xp = static_cast<const Tin*>(p.x_prev);
-      if (dvalid) xprev = f2(load_in<Tin>(xp, int64_t(b) * D + d), load_in<Tin>(xp, int64_t(b) * D + d + 1));
+      if (dvalid) xprev = f2(load_in<Tin>(xp, int64_t(b) * D + chan(0)), load_in<Tin>(xp, int64_t(b) * D + chan(1)));
       bsrc = static_cast<const Tin*>(p.Bc_prev) + int64_t(b) * p.N * 2;
     }
-    const float2 dt_tc = dvalid ? f2(load_in<Tin>(dtin, (b * L + tc) * D + d), load_in<Tin>(dtin, (b * L + tc) * D + d + 1))
+    const float2 dt_tc = dvalid ? f2(load_in<Tin>(dtin, (b * L + tc) * D + chan(0)), load_in<Tin>(dtin, (b * L + tc) * D + chan(1)))
                                 : f2(0.f, 0.f);
     const float mu = 1.f - load_in<Tin>(lamin, b * L + tc);
     halo_p = f2(mu * dt_tc.x * xprev.x, mu * dt_tc.y * xprev.y);
@@ -378,15 +393,14 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   // x, pc and E.
   struct StepIn {
     float4 tb[2 * NPAIR];  // this step's table entries of the thread's states (Bt, Ct per pair)
-    float2 w0, w1;         // (w_c0, w_c0), (w_c1, w_c1)
-    float2 dv;             // (dt_c0, dt_c1)
-    float2 x, pc;          // (x_c0, x_c1), (pc_c0, pc_c1)
+    float2 w0, w1;         // injection weights (w_kept, w_kept), (w_other, w_other)
+    float2 dv;             // (dt_kept, dt_other), for the aggregate pass
+    float2 x, pc;          // (x_kept, x_other), (pc_kept, pc_other)
+    float2 nk, no;         // trapezoid: the next step's dt, broadcast pairs (kept, other)
     float E;
   };
   // The output of a finished step: the NG lanes' partial sums of Re(Ct k) are combined, the
   // trapezoid correction and the D-skip added, and the lanes with g < 2 store the result.
-  const bool odd = (g & 1) != 0;
-  const float Dk = odd ? Ds.y : Ds.x;
   const bool store_one = NG > 1 && g < 2 && dvalid;
   auto finish_y = [&](float2 yp, const StepIn& sc, float* yrow, bool ok) {
     if (NG == 1) {
@@ -401,12 +415,11 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
         }
       }
     } else {
-      // lanes g and g^1 trade the channel they do not keep, then the group sums
-      float keep = odd ? yp.y : yp.x;
-      keep += __shfl_xor_sync(0xffffffffu, odd ? yp.x : yp.y, 1);
+      // lanes g and g^1 trade the partial of the channel they do not keep, then the group sums
+      float keep = yp.x + __shfl_xor_sync(0xffffffffu, yp.y, 1);
 #pragma unroll
       for (int o = 2; o < NG; o <<= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
-      const float o = fmaf(Dk, odd ? sc.x.y : sc.x.x, fmaf(-(odd ? sc.pc.y : sc.pc.x), sc.E, keep));
+      const float o = fmaf(Ds.x, sc.x.x, fmaf(-sc.pc.x, sc.E, keep));
       if (ok && store_one) __stcs(yrow + g, o);
     }
   };
@@ -434,15 +447,16 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
       const int t_last = te - 1 - t_sub0 < T_SUB ? te - 1 - t_sub0 : -1;
       float* yrow = p.y + (b * L + t_sub0) * D + d;
 
-      // table entries and scalars of step tt (rows tt of x, aux and the table, tt and tt + 1 of
-      // dt; all staged) and the decays' dt broadcast pairs
-      auto load_step = [&](int tt, StepIn& s, float2& dd0, float2& dd1) {
+      // Table entries and scalars of step tt (rows tt of x, aux and the table; row tt of dt, or,
+      // in the trapezoid mode, the pairs dd0/dd1 carried from the previous step, and row tt + 1
+      // of dt; all staged), and the decays' dt broadcast pairs dd0/dd1.
+      auto load_step = [&](int tt, StepIn& s, float2& dd0, float2& dd1, bool dd_given) {
         const float4* trow = stab + tt * N;
 #pragma unroll
         for (int k = 0; k < 2 * NPAIR; ++k) s.tb[k] = trow[k];
         float2 xx0, xx1;
-        PairLoad<Tin>::bcast(sx + tt * DT, xx0, xx1);
-        PairLoad<Tin>::bcast(sdtp + tt * DT, dd0, dd1);
+        PairLoad<Tin>::bcast(sx + tt * DT, sel, swp, xx0, xx1);
+        if (!dd_given) PairLoad<Tin>::bcast(sdtp + tt * DT, sel, swp, dd0, dd1);
         s.x = f2(xx0.x, xx1.x);
         s.dv = f2(dd0.x, dd1.x);
         if (MODE == 0) {
@@ -451,17 +465,16 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
           s.pc = f2(0.f, 0.f);
           s.E = 0.f;
         } else {
-          float2 nn0, nn1;
-          PairLoad<Tin>::bcast(sdtp + (tt + 1) * DT, nn0, nn1);
+          PairLoad<Tin>::bcast(sdtp + (tt + 1) * DT, sel, swp, s.nk, s.no);
           const float4 a = saux[2 * tt];
           const float4 e = saux[2 * tt + 1];
           const float2 lam2 = f2(a.x, a.y), mu2 = f2(a.z, a.w);
-          float2 pc0 = mul2(mu2, mul2(nn0, xx0));
-          float2 pc1 = mul2(mu2, mul2(nn1, xx1));
-          if (tt == t_last) { pc0 = f2(0.f, 0.f); pc1 = f2(0.f, 0.f); }
-          s.w0 = fma2(mul2(lam2, dd0), xx0, pc0);
-          s.w1 = fma2(mul2(lam2, dd1), xx1, pc1);
-          s.pc = f2(pc0.x, pc1.x);
+          // m = (1 - lam_{t+1}) dt_{t+1}; w = (lam_t dt_t + m) x_t; pc = m x_t
+          float2 m0 = mul2(mu2, s.nk), m1 = mul2(mu2, s.no);
+          if (tt == t_last) { m0 = f2(0.f, 0.f); m1 = f2(0.f, 0.f); }
+          s.w0 = mul2(fma2(lam2, dd0, m0), xx0);
+          s.w1 = mul2(fma2(lam2, dd1, m1), xx1);
+          s.pc = f2(m0.x * xx0.x, m1.x * xx1.x);
           s.E = e.x;
         }
       };
@@ -471,15 +484,14 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
       // `nxt` / `rn` and finishes step tt - 1's output, whose scalars `nxt` held.
       auto step = [&](int tt, const StepIn& cur, const float2 (&rc)[CH][NPAIR], StepIn& nxt,
                       float2 (&rn)[CH][NPAIR]) {
-        const StepIn prev = nxt;
-        float2 dd0, dd1;
-        load_step(tt + 1, nxt, dd0, dd1);
         if (WITH_Y) {
-          finish_y(ypend, prev, yrow, tt > 0);
+          finish_y(ypend, nxt, yrow, tt > 0);
           if (tt > 0) yrow += D;
         } else {
           sdt_acc = f2(sdt_acc.x + cur.dv.x, sdt_acc.y + cur.dv.y);
         }
+        float2 dd0 = cur.nk, dd1 = cur.no;
+        load_step(tt + 1, nxt, dd0, dd1, MODE == 1);
         float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
 #pragma unroll
         for (int q = 0; q < NPAIR; ++q) {
@@ -505,7 +517,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
       float2 ra[CH][NPAIR], rb[CH][NPAIR];
       {
         float2 dd0, dd1;
-        load_step(0, sa, dd0, dd1);
+        load_step(0, sa, dd0, dd1, false);
 #pragma unroll
         for (int q = 0; q < NPAIR; ++q) {
           ra[0][q] = ex2_pair(mul2(dd0, Ap[0][q]));
@@ -552,7 +564,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   };
 
   // ---- per-state helpers on the workspace records (float2 per state, states contiguous)
-  auto rec_of = [&](float2* base, int u, int ch) { return base + (int64_t(u) * DT + cl + ch) * p.N + n0; };
+  auto rec_of = [&](float2* base, int u, int ch) { return base + (int64_t(u) * DT + cl + (ch ^ swp)) * p.N + n0; };
   auto load_states = [&](const float2* rec, float2* re, float2* im) {
     const float4* r4 = reinterpret_cast<const float4*>(rec);
 #pragma unroll
@@ -582,7 +594,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   bool incl_published = false;
   const bool has_h0 = (p.h0 != nullptr) && dvalid;
   auto h0rec = [&](int ch) {
-    return reinterpret_cast<const float2*>(p.h0) + (int64_t(b) * p.D + d + ch) * p.N + n0;
+    return reinterpret_cast<const float2*>(p.h0) + (int64_t(b) * p.D + chan(ch)) * p.N + n0;
   };
 
   if (CARRY == CARRY_DECOUPLED && pass1) {
@@ -667,7 +679,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
           const int u2 = unit_of(pred - i);
           accumulate(u2, false, false);
           const float2 sd2 = __ldcg(reinterpret_cast<const float2*>(p.ws.sdt + int64_t(u2) * DT + cl));
-          Sd = f2(Sd.x + sd2.x, Sd.y + sd2.y);
+          Sd = swp ? f2(Sd.x + sd2.y, Sd.y + sd2.x) : f2(Sd.x + sd2.x, Sd.y + sd2.y);
           const float4* cr4 = reinterpret_cast<const float4*>(p.ws.crot + int64_t(u2) * p.N + n0);
 #pragma unroll
           for (int q = 0; q < NPAIR; ++q) {
@@ -766,7 +778,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
     if (c == p.n_chunks - 1 && p.h_last != nullptr && dvalid) {
 #pragma unroll
       for (int ch = 0; ch < CH; ++ch)
-        store_states(reinterpret_cast<float2*>(p.h_last) + (int64_t(b) * p.D + d + ch) * p.N + n0, kr[ch], ki[ch]);
+        store_states(reinterpret_cast<float2*>(p.h_last) + (int64_t(b) * p.D + chan(ch)) * p.N + n0, kr[ch], ki[ch]);
     }
   } else {
     // a tile copy never arrived: report, drain what is still in flight (bounded), leave
