@@ -128,6 +128,46 @@ int csscan_forward_ex(const void* x, const void* delta, const float* A, const vo
                       const csscan_options_t* opts, cudaStream_t stream);
 
 /*
+ * Forward scan that continues from a given state and returns the final state, so that a long
+ * sequence can be scanned in pieces (or a prompt prefilled before single-step decoding): the
+ * recurrent, constant-state form of the model that "Mamba-3 paper story" contrasts with
+ * attention's growing cache, and the associativity of the step operator ("Complex parallel
+ * scan", section 并行扫描的数学本质) that makes the pieces compose exactly.
+ * Arguments as csscan_forward, plus:
+ *   h0      : device float32 (B, D, N, 2), the state h_{-1} before the first step, or NULL for zero
+ *   x_prev, Bc_prev : trapezoid mode only (ignored in exp-Euler mode): the step before the first,
+ *             x (B, D) and Bc (B, N, 2) in `dtype`, which the first step's beta term uses;
+ *             both NULL means there is no previous step (Bc_{-1} x_{-1} = 0); one NULL is invalid
+ *   h_last  : device float32 (B, D, N, 2), receives h_{L-1}, or NULL
+ * h0 and h_last must be 16-byte aligned and may not overlap. Scanning [0, t0) and then [t0, L)
+ * with h0 = the first call's h_last and (x_prev, Bc_prev) = its last step's x and Bc gives the
+ * same y and final state as one call over [0, L).
+ */
+int csscan_forward_state(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                         const void* theta, const void* lambda, const float* Dskip, float* y, const float* h0,
+                         const void* x_prev, const void* Bc_prev, float* h_last, int64_t B, int64_t L, int64_t D,
+                         int64_t N, int mode, int dtype, cudaStream_t stream);
+
+/*
+ * One decode step for B x D sequences whose state lives in device memory (the single-token,
+ * constant-state regime of "Mamba-3 paper story"; one step of the recurrence above):
+ *   x, delta          : (B, D) in `dtype`, this step's input and step size
+ *   Bc, Cc            : (B, N, 2) in `dtype`;  theta : (B, N) in `dtype`
+ *   lambda            : (B) in `dtype`, trapezoid mode only (may be NULL in exp-Euler mode)
+ *   A, Dskip          : device float32 (D, N) and (D)
+ *   y                 : device float32 (B, D), written
+ *   h                 : device float32 (B, D, N, 2), the state, updated in place (16-byte aligned)
+ *   x_prev, Bc_prev   : trapezoid mode: the previous step's x (B, D) and Bc (B, N, 2), both NULL
+ *                       for the first step of a sequence; ignored in exp-Euler mode
+ * The caller keeps the previous step's x and Bc for the trapezoid rule. One kernel launch; the
+ * state is read and written once, so the step is bound by memory bandwidth.
+ */
+int csscan_decode_step(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                       const void* theta, const void* lambda, const float* Dskip, float* y, float* h,
+                       const void* x_prev, const void* Bc_prev, int64_t B, int64_t D, int64_t N, int mode, int dtype,
+                       cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device-side status of the calls made on it since
  * the last query (CSSCAN_OK, CSSCAN_ERR_LOOKBACK_TIMEOUT or CSSCAN_ERR_PIPELINE_TIMEOUT), or
  * CSSCAN_ERR_CUDA if the stream reports an error. Clears the device status.

@@ -13,6 +13,7 @@
 #include <utility>
 
 #include "csscan.h"
+#include "decode_kernel.cuh"
 #include "scan_kernels.cuh"
 
 using namespace csscan;
@@ -405,6 +406,66 @@ int forward_impl(const Args& a, const csscan_options_t* opts, cudaStream_t st) {
 }
 
 
+// ----------------------------------------------------------------------------- decode step
+template <typename Tin, int MODE, int NP>
+int launch_decode(const DecodeParams& dp, cudaStream_t st) {
+  const long long threads = dp.rows * NP;
+  decode_kernel<Tin, MODE, NP><<<unsigned((threads + 255) / 256), 256, 0, st>>>(dp);
+  CSSCAN_CUDA(cudaGetLastError());
+  return CSSCAN_OK;
+}
+
+template <typename Tin, int MODE>
+int dispatch_decode(const DecodeParams& dp, cudaStream_t st) {
+  switch (dp.N) {
+    case 2: return launch_decode<Tin, MODE, 1>(dp, st);
+    case 4: return launch_decode<Tin, MODE, 2>(dp, st);
+    case 8: return launch_decode<Tin, MODE, 4>(dp, st);
+    case 16: return launch_decode<Tin, MODE, 8>(dp, st);
+    case 32: return launch_decode<Tin, MODE, 16>(dp, st);
+    case 64: return launch_decode<Tin, MODE, 32>(dp, st);
+    default: return CSSCAN_ERR_UNSUPPORTED;
+  }
+}
+
+int decode_impl(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc, const void* theta,
+                const void* lambda, const float* Dskip, float* y, float* h, const void* x_prev, const void* Bc_prev,
+                int64_t B, int64_t D, int64_t N, int mode, int dtype, cudaStream_t stream) {
+  if (mode != CSSCAN_MODE_EXP_EULER && mode != CSSCAN_MODE_EXP_TRAPEZOID) return CSSCAN_ERR_INVALID_ARG;
+  if (dtype != CSSCAN_F32 && dtype != CSSCAN_BF16) return CSSCAN_ERR_INVALID_ARG;
+  if (B < 0 || D < 0 || N <= 0) return CSSCAN_ERR_INVALID_ARG;
+  if (!x || !delta || !A || !Bc || !Cc || !theta || !Dskip || !y || !h) return CSSCAN_ERR_INVALID_ARG;
+  if (mode == CSSCAN_MODE_EXP_TRAPEZOID && !lambda) return CSSCAN_ERR_INVALID_ARG;
+  if ((x_prev == nullptr) != (Bc_prev == nullptr)) return CSSCAN_ERR_INVALID_ARG;
+  if (N != 2 && N != 4 && N != 8 && N != 16 && N != 32 && N != 64) return CSSCAN_ERR_UNSUPPORTED;
+  if (B > (int64_t(1) << 31) - 1 || D > (int64_t(1) << 30) || B * D > (int64_t(1) << 40)) return CSSCAN_ERR_UNSUPPORTED;
+  const size_t s = dtype == CSSCAN_F32 ? 4 : 2;
+  if (!aligned(h, 16) || !aligned(x, s) || !aligned(delta, s) || !aligned(Bc, s) || !aligned(Cc, s) ||
+      !aligned(theta, s) || (lambda && !aligned(lambda, s)) || !aligned(A, 4) || !aligned(Dskip, 4) ||
+      !aligned(y, 4) || (x_prev && !aligned(x_prev, s)) || (Bc_prev && !aligned(Bc_prev, s)))
+    return CSSCAN_ERR_MISALIGNED;
+  if (B == 0 || D == 0) return CSSCAN_OK;
+  DecodeParams dp;
+  dp.x = x;
+  dp.dt = delta;
+  dp.A = A;
+  dp.Bc = Bc;
+  dp.Cc = Cc;
+  dp.theta = theta;
+  dp.lam = lambda;
+  dp.Dskip = Dskip;
+  dp.y = y;
+  dp.h = reinterpret_cast<float4*>(h);
+  dp.x_prev = mode == CSSCAN_MODE_EXP_TRAPEZOID ? x_prev : nullptr;
+  dp.Bc_prev = mode == CSSCAN_MODE_EXP_TRAPEZOID ? Bc_prev : nullptr;
+  dp.rows = B * D;
+  dp.D = int(D);
+  dp.N = int(N);
+  if (dtype == CSSCAN_F32)
+    return mode == 0 ? dispatch_decode<float, 0>(dp, stream) : dispatch_decode<float, 1>(dp, stream);
+  return mode == 0 ? dispatch_decode<uint16_t, 0>(dp, stream) : dispatch_decode<uint16_t, 1>(dp, stream);
+}
+
 // ----------------------------------------------------------------------------- no-allocation entry
 // csscan_forward_noalloc runs the same two kernels with its scratch in one fixed array that
 // is part of the library's device code, so it never calls cudaMalloc. Layout of the array:
@@ -493,6 +554,25 @@ int csscan_forward_ex(const void* x, const void* delta, const float* A, const vo
                       int64_t D, int64_t N, int mode, int dtype, const csscan_options_t* opts, cudaStream_t stream) {
   Args a{x, delta, Bc, Cc, theta, lambda, A, Dskip, y, nullptr, nullptr, nullptr, nullptr, B, L, D, N, mode, dtype};
   return forward_impl(a, opts, stream);
+}
+
+int csscan_forward_state(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                         const void* theta, const void* lambda, const float* Dskip, float* y, const float* h0,
+                         const void* x_prev, const void* Bc_prev, float* h_last, int64_t B, int64_t L, int64_t D,
+                         int64_t N, int mode, int dtype, cudaStream_t stream) {
+  if (mode == CSSCAN_MODE_EXP_EULER) {   // the halo only enters the trapezoid rule
+    x_prev = nullptr;
+    Bc_prev = nullptr;
+  }
+  Args a{x, delta, Bc, Cc, theta, lambda, A, Dskip, y, h0, h_last, x_prev, Bc_prev, B, L, D, N, mode, dtype};
+  return forward_impl(a, nullptr, stream);
+}
+
+int csscan_decode_step(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                       const void* theta, const void* lambda, const float* Dskip, float* y, float* h,
+                       const void* x_prev, const void* Bc_prev, int64_t B, int64_t D, int64_t N, int mode, int dtype,
+                       cudaStream_t stream) {
+  return decode_impl(x, delta, A, Bc, Cc, theta, lambda, Dskip, y, h, x_prev, Bc_prev, B, D, N, mode, dtype, stream);
 }
 
 int csscan_forward_noalloc(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,

@@ -66,6 +66,10 @@ def load_library(path: str = LIBRARY) -> ctypes.CDLL:
     lib.csscan_status_string.restype = ctypes.c_char_p
     lib.csscan_release_workspace.argtypes = []
     lib.csscan_release_workspace.restype = i32
+    lib.csscan_forward_state.argtypes = [vp] * 13 + [i64] * 4 + [i32, i32, vp]
+    lib.csscan_forward_state.restype = i32
+    lib.csscan_decode_step.argtypes = [vp] * 12 + [i64] * 3 + [i32, i32, vp]
+    lib.csscan_decode_step.restype = i32
     _lib = lib
     return lib
 
@@ -119,6 +123,34 @@ def csscan_forward_ex(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode: int, stre
     o = csscan_options_t(cta_warps, chunk_len, carry, silent_chunk, poll_limit, ev(scan_begin), ev(scan_end))
     return load_library().csscan_forward_ex(*_args(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode),
                                             ctypes.byref(o), _stream_handle(stream))
+
+
+def csscan_forward_state(x, delta, A, Bc, Cc, theta, lam, Dskip, y, mode: int, h0=None, x_prev=None, Bc_prev=None,
+                         h_last=None, stream=None) -> None:
+    """csscan_forward continuing from state ``h0`` ((B, D, N, 2) float32, or None for zero) and
+    writing the final state into ``h_last`` (same shape, or None). In the trapezoid mode
+    ``x_prev`` (B, D) and ``Bc_prev`` (B, N, 2) are the step before the first (None: none)."""
+    B, L, D = x.shape
+    N = A.shape[1]
+    rc = load_library().csscan_forward_state(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(Bc), _ptr(Cc), _ptr(theta), _ptr(lam), _ptr(Dskip), _ptr(y), _ptr(h0),
+        _ptr(x_prev), _ptr(Bc_prev), _ptr(h_last), B, L, D, N, int(mode), _dtype_code(x), _stream_handle(stream))
+    if rc != CSSCAN_OK:
+        raise CsscanError(rc, "csscan_forward_state")
+
+
+def csscan_decode_step(x, delta, A, Bc, Cc, theta, lam, Dskip, y, h, mode: int, x_prev=None, Bc_prev=None,
+                       stream=None) -> None:
+    """One decode step: x, delta (B, D); Bc, Cc (B, N, 2); theta (B, N); lam (B) or None;
+    y (B, D) float32 out; h (B, D, N, 2) float32 state, updated in place; trapezoid mode:
+    the previous step's x (B, D) and Bc (B, N, 2), or None for a sequence's first step."""
+    B, D = x.shape
+    N = A.shape[1]
+    rc = load_library().csscan_decode_step(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(Bc), _ptr(Cc), _ptr(theta), _ptr(lam), _ptr(Dskip), _ptr(y), _ptr(h),
+        _ptr(x_prev), _ptr(Bc_prev), B, D, N, int(mode), _dtype_code(x), _stream_handle(stream))
+    if rc != CSSCAN_OK:
+        raise CsscanError(rc, "csscan_decode_step")
 
 
 def csscan_get_device_status(stream=None) -> int:

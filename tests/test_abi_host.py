@@ -75,3 +75,21 @@ def test_empty_problem_is_a_noop(lib):
     assert call(lib, L=0) == csscan.CSSCAN_OK
     assert call(lib, D=0) == csscan.CSSCAN_OK
     assert call(lib, mode=1, B=0) == csscan.CSSCAN_OK
+
+
+def test_state_and_decode_reject_bad_arguments_on_host(lib):
+    st = lib.csscan_forward_state
+    # one of x_prev / Bc_prev given without the other, in trapezoid mode
+    assert st(A16, A16, A16, A16, A16, A16, A16, A16, A16, None, A16, None, None, 1, 64, 16, 8, 1, 0, None) \
+        == csscan.CSSCAN_ERR_INVALID_ARG
+    # misaligned initial state
+    assert st(A16, A16, A16, A16, A16, A16, None, A16, A16, A16 + 8, None, None, None, 1, 64, 16, 8, 0, 0, None) \
+        == csscan.CSSCAN_ERR_MISALIGNED
+    dec = lib.csscan_decode_step
+    args = lambda **k: [k.get("x", A16), A16, A16, A16, A16, A16, k.get("lam", A16), A16, A16, k.get("h", A16),
+                        k.get("xp", None), k.get("bp", None), 2, 16, k.get("N", 8), k.get("mode", 0), 0, None]
+    assert dec(*args(N=3)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert dec(*args(h=A16 + 4)) == csscan.CSSCAN_ERR_MISALIGNED
+    assert dec(*args(x=None)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert dec(*args(mode=1, lam=None)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert dec(*args(mode=1, xp=A16)) == csscan.CSSCAN_ERR_INVALID_ARG
