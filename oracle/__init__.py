@@ -1,4 +1,4 @@
-"""Float64 CPU oracle for the forward complex diagonal selective scan.
+"""Float64 CPU oracle for the complex diagonal selective scan (forward and backward).
 
 TEST INFRASTRUCTURE ONLY. Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline
 leg of ``bench.py`` may import this package. The CUDA library never calls it and shares no
@@ -14,6 +14,10 @@ computes and which page it follows:
 * the loop shape (update h, then read y from the updated h) follows the sequential
   pseudocode listing of "状态空间模型的对偶谱理论 2026" (blog.lonae.com), section 3.2, and the
   D-skip follows "Mamba-3: 选择性状态空间模型的下一代架构" (metaphor-xennon), section 2.2.
+
+The backward (``backward``) is reverse-mode differentiation of that recurrence written out
+step by step in ``oracle.c``; the pages name a backward pass with recomputed states
+("Complex parallel scan", sections 一个问题，两种命运 and 硬件落地的挑战) but give no formulas.
 
 This module only marshals numpy arrays into that library (``ctypes``) and builds it.
 """
@@ -60,6 +64,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.oracle_apply.restype = None
     lib.oracle_forward.argtypes = [dp] * 14 + [i64] * 4 + [ctypes.c_int, ctypes.c_int]
     lib.oracle_forward.restype = ctypes.c_int
+    lib.oracle_backward.argtypes = [dp] * 17 + [i64] * 4 + [ctypes.c_int, ctypes.c_int]
+    lib.oracle_backward.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ctypes.c_int
     _lib_cache[path] = lib
@@ -123,6 +129,38 @@ def forward(x, delta, A, Bc, Cc, theta, lam, Dskip, mode: int, *, h0=None, x_pre
     if want_traj:
         out.append(h_traj)
     return out[0] if len(out) == 1 else tuple(out)
+
+
+def backward(x, delta, A, Bc, Cc, theta, lam, Dskip, dy, mode: int, *, nthreads: int = 0, lib=None) -> dict:
+    """Reverse-mode gradients of l = sum(dy * y) for ``forward`` from the zero state (no halo).
+
+    Same input shapes as ``forward``, plus dy (B,L,D) real. Returns a dict with dx, ddelta
+    (B,L,D), dA (D,N), dBc, dCc (B,L,N) complex (d/dRe + i d/dIm), dtheta (B,L,N),
+    dlam (B,L) (mode 1, else None) and dDskip (D,), all float64 / complex128.
+    """
+    lib = lib or load()
+    x = _f64(x)
+    Bsz, L, D = x.shape
+    N = np.asarray(A).shape[1]
+    delta = _f64(delta, (Bsz, L, D))
+    A = _f64(A, (D, N))
+    Bc = _f64(np.asarray(Bc, dtype=np.complex128), (Bsz, L, N))
+    Cc = _f64(np.asarray(Cc, dtype=np.complex128), (Bsz, L, N))
+    theta = _f64(theta, (Bsz, L, N))
+    lam = _f64(lam, (Bsz, L)) if lam is not None else None
+    Dskip = _f64(Dskip, (D,))
+    dy = _f64(dy, (Bsz, L, D))
+    out = dict(dx=np.zeros((Bsz, L, D)), ddelta=np.zeros((Bsz, L, D)), dA=np.zeros((D, N)),
+               dBc=np.zeros((Bsz, L, N), dtype=np.complex128), dCc=np.zeros((Bsz, L, N), dtype=np.complex128),
+               dtheta=np.zeros((Bsz, L, N)), dlam=np.zeros((Bsz, L)) if mode == 1 else None,
+               dDskip=np.zeros(D))
+    rc = lib.oracle_backward(_ptr(x), _ptr(delta), _ptr(A), _ptr(Bc), _ptr(Cc), _ptr(theta), _ptr(lam),
+                             _ptr(Dskip), _ptr(dy), _ptr(out["dx"]), _ptr(out["ddelta"]), _ptr(out["dA"]),
+                             _ptr(out["dBc"]), _ptr(out["dCc"]), _ptr(out["dtheta"]), _ptr(out["dlam"]),
+                             _ptr(out["dDskip"]), Bsz, L, D, N, int(mode), int(nthreads))
+    if rc <= 0:
+        raise RuntimeError(f"oracle_backward failed with code {rc}")
+    return out
 
 
 def last_thread_count(nthreads: int = 0, rows: int = 1 << 30, lib=None) -> int:

@@ -190,3 +190,186 @@ int oracle_forward(const double* x, const double* dt, const double* A, const dou
   free(jobs);
   return rc < 0 ? rc : nthreads;
 }
+
+/* ===================================================================================== *
+ * Backward (reverse mode) of the scan above, for a sequence that starts from the zero
+ * state with no step -1 halo.
+ *
+ * The pages name the backward pass and its recompute strategy without formulas ("Complex
+ * parallel scan", sections 一个问题，两种命运 and 硬件落地的挑战: one reverse sweep after
+ * the forward, states regenerated instead of stored, a backward kernel beside the forward
+ * one). What follows is reverse-mode differentiation of the recurrence written out step by
+ * step. For a complex quantity z the gradient is G(z) = dl/dRe z + i dl/dIm z, where
+ * l = sum_{b,t,d} dy[b,t,d] y[b,t,d]. Two rules give every line below:
+ *   w = p z (p fixed)          =>  G(z) += conj(p) G(w)
+ *   w = exp(z)                 =>  G(z)  = conj(exp(z)) G(w)
+ * and for y = Re(C h): G(h) += dy conj(C), G(C) += dy conj(h).
+ * The adjoint of the state obeys the reversed recurrence
+ *   ghat_t = dy_t conj(Cc_t) + conj(a_{t+1}) ghat_{t+1},  ghat_L = 0,
+ * and ghat_t is the gradient of the step-t injection u_t; the transition a_t = exp(z_t),
+ * z_t = dt_t A + i theta_t, receives G(a_t) = ghat_t conj(h_{t-1}) (plus, in the trapezoid
+ * mode, ghat_t conj((1 - lam_t) dt_t x_{t-1} Bc_{t-1}) from beta_t), so that
+ * d l / d(dt_t A) = Re G(z_t) and d l / d theta_t = Im G(z_t).
+ *
+ * Outputs are fully written (zeroed first); complex gradients are (d/dRe, d/dIm) pairs in the
+ * layouts of their inputs: dx, ddt (B,L,D); dA (D,N); dBc, dCc (B,L,N) complex;
+ * dtheta (B,L,N); dlam (B,L) (mode 1; may be NULL in mode 0); dDskip (D).
+ * ===================================================================================== */
+typedef struct {
+  const double *x, *dt, *A, *Bc, *Cc, *theta, *lam, *Dskip, *dy;
+  double *dx, *ddt;                          /* per row, written by the row's owner only */
+  double *dA, *dBc, *dCc, *dtheta, *dlam, *dD; /* shared: private copies per worker */
+  int64_t B, L, D, N;
+  int mode;
+  int64_t row_begin, row_step;
+} bjob_t;
+
+static void backward_row(const bjob_t* j, int64_t b, int64_t d, cplx* hs, cplx* as, cplx* carry) {
+  const int64_t L = j->L, D = j->D, N = j->N;
+  /* forward sweep: keep every state h_t and transition a_t of this row */
+  for (int64_t n = 0; n < N; ++n) carry[n] = 0.0;   /* used as h here */
+  for (int64_t t = 0; t < L; ++t) {
+    const int64_t td = (b * L + t) * D + d;
+    const double xt = j->x[td], dtt = j->dt[td];
+    const double x_prev = t > 0 ? j->x[td - D] : 0.0;
+    const double lam = j->mode == 1 ? j->lam[b * L + t] : 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      const int64_t tn = (b * L + t) * N + n;
+      double B_prev[2] = {0.0, 0.0};
+      if (t > 0) { B_prev[0] = j->Bc[2 * (tn - N)]; B_prev[1] = j->Bc[2 * (tn - N) + 1]; }
+      double op[4];
+      oracle_operator(j->mode, dtt, j->A[d * N + n], j->theta[tn], lam, xt, x_prev, &j->Bc[2 * tn], B_prev, op);
+      carry[n] = (op[0] + I * op[1]) * carry[n] + (op[2] + I * op[3]);
+      hs[t * N + n] = carry[n];
+      as[t * N + n] = op[0] + I * op[1];
+    }
+  }
+  /* reverse sweep */
+  for (int64_t n = 0; n < N; ++n) carry[n] = 0.0;   /* conj(a_{t+1}) ghat_{t+1} */
+  for (int64_t t = L - 1; t >= 0; --t) {
+    const int64_t td = (b * L + t) * D + d;
+    const double xt = j->x[td], dtt = j->dt[td], dyt = j->dy[td];
+    const double x_prev = t > 0 ? j->x[td - D] : 0.0;
+    const double lam = j->mode == 1 ? j->lam[b * L + t] : 0.0;
+    double P = 0.0;   /* sum_n Re(conj(Bc_t) ghat_t): d l / d(coefficient of Bc_t) */
+    double R = 0.0;   /* sum_n Re(conj(a_t Bc_{t-1}) ghat_t): the same for beta_t's term */
+    double dz_re = 0.0;
+    for (int64_t n = 0; n < N; ++n) {
+      const int64_t tn = (b * L + t) * N + n;
+      const cplx a = as[t * N + n];
+      const cplx h = hs[t * N + n];
+      const cplx h_prev = t > 0 ? hs[(t - 1) * N + n] : 0.0;
+      const cplx ghat = dyt * conj(load_c(j->Cc, tn)) + carry[n];
+      /* output y_t = Re(Cc_t h_t) */
+      store_c(j->dCc, tn, load_c(j->dCc, tn) + dyt * conj(h));
+      /* injection */
+      const cplx Bt = load_c(j->Bc, tn);
+      cplx Ga = ghat * conj(h_prev);
+      if (j->mode == 0) {
+        store_c(j->dBc, tn, load_c(j->dBc, tn) + (dtt * xt) * ghat);
+        P += creal(conj(Bt) * ghat);
+      } else {
+        store_c(j->dBc, tn, load_c(j->dBc, tn) + (lam * dtt * xt) * ghat);
+        P += creal(conj(Bt) * ghat);
+        if (t > 0) {
+          const cplx Bp = load_c(j->Bc, tn - N);
+          const double c2 = (1.0 - lam) * dtt * x_prev;     /* beta_t's term is c2 a_t Bc_{t-1} */
+          R += creal(conj(a * Bp) * ghat);
+          store_c(j->dBc, tn - N, load_c(j->dBc, tn - N) + c2 * conj(a) * ghat);
+          Ga += ghat * conj(c2 * Bp);
+        }
+      }
+      /* transition a_t = exp(dt_t A + i theta_t) */
+      const cplx Gz = conj(a) * Ga;
+      j->dA[d * N + n] += dtt * creal(Gz);
+      dz_re += j->A[d * N + n] * creal(Gz);
+      j->dtheta[tn] += cimag(Gz);
+      carry[n] = conj(a) * ghat;
+    }
+    double gx, gdt;
+    if (j->mode == 0) {
+      gx = dtt * P;
+      gdt = xt * P;
+    } else {
+      gx = lam * dtt * P;
+      gdt = lam * xt * P + (1.0 - lam) * x_prev * R;
+      j->dlam[b * L + t] += dtt * xt * P - dtt * x_prev * R;
+      if (t > 0) j->dx[td - D] += (1.0 - lam) * dtt * R;
+    }
+    j->dx[td] += gx + j->Dskip[d] * dyt;
+    j->ddt[td] += gdt + dz_re;
+    j->dD[d] += dyt * xt;
+  }
+}
+
+static void* bworker(void* arg) {
+  const bjob_t* j = (const bjob_t*)arg;
+  const size_t LN = (size_t)(j->L > 0 ? j->L : 1) * (size_t)(j->N > 0 ? j->N : 1);
+  cplx* hs = (cplx*)malloc(sizeof(cplx) * LN);
+  cplx* as = (cplx*)malloc(sizeof(cplx) * LN);
+  cplx* carry = (cplx*)malloc(sizeof(cplx) * (size_t)(j->N > 0 ? j->N : 1));
+  if (!hs || !as || !carry) { free(hs); free(as); free(carry); return (void*)1; }
+  for (int64_t r = j->row_begin; r < j->B * j->D; r += j->row_step) backward_row(j, r / j->D, r % j->D, hs, as, carry);
+  free(hs); free(as); free(carry);
+  return NULL;
+}
+
+/* Reverse-mode gradients of l = sum dy * y for oracle_forward with h0 = 0 and no halo, rows
+ * split across `nthreads` POSIX threads (<= 0: all online cores); the shared gradients are
+ * summed from private per-thread copies. Returns the number of threads used (> 0), or a
+ * negative value on bad arguments or allocation failure. */
+int oracle_backward(const double* x, const double* dt, const double* A, const double* Bc, const double* Cc,
+                    const double* theta, const double* lam, const double* Dskip, const double* dy,
+                    double* dx, double* ddt, double* dA, double* dBc, double* dCc, double* dtheta, double* dlam,
+                    double* dDskip, int64_t B, int64_t L, int64_t D, int64_t N, int mode, int nthreads) {
+  if (B < 0 || L < 0 || D < 0 || N < 0) return -1;
+  if (mode != 0 && mode != 1) return -2;
+  if (mode == 1 && (!lam || !dlam) && B * L > 0) return -3;
+  const size_t nBLD = (size_t)(B * L * D), nDN = (size_t)(D * N), nBLN = (size_t)(B * L * N), nBL = (size_t)(B * L);
+  for (size_t i = 0; i < nBLD; ++i) { dx[i] = 0.0; ddt[i] = 0.0; }
+  for (size_t i = 0; i < nDN; ++i) dA[i] = 0.0;
+  for (size_t i = 0; i < 2 * nBLN; ++i) { dBc[i] = 0.0; dCc[i] = 0.0; }
+  for (size_t i = 0; i < nBLN; ++i) dtheta[i] = 0.0;
+  if (dlam) for (size_t i = 0; i < nBL; ++i) dlam[i] = 0.0;
+  for (int64_t i = 0; i < D; ++i) dDskip[i] = 0.0;
+  if (nthreads <= 0) nthreads = oracle_default_threads();
+  if ((int64_t)nthreads > B * D) nthreads = (int)(B * D > 0 ? B * D : 1);
+  /* per-thread private copies of the shared gradients: dA, dBc, dCc, dtheta, dlam, dD */
+  const size_t priv = nDN + 4 * nBLN + nBLN + nBL + (size_t)D;
+  double* buf = (double*)calloc(priv * (size_t)nthreads + 1, sizeof(double));
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  bjob_t* jobs = (bjob_t*)malloc(sizeof(bjob_t) * (size_t)nthreads);
+  if (!buf || !th || !jobs) { free(buf); free(th); free(jobs); return -4; }
+  int rc = 0, started = 0;
+  for (int i = 0; i < nthreads; ++i) {
+    double* p = buf + priv * (size_t)i;
+    bjob_t jb = {x, dt, A, Bc, Cc, theta, lam, Dskip, dy, dx, ddt,
+                 p, p + nDN, p + nDN + 2 * nBLN, p + nDN + 4 * nBLN, p + nDN + 5 * nBLN, p + nDN + 5 * nBLN + nBL,
+                 B, L, D, N, mode, i, nthreads};
+    jobs[i] = jb;
+    if (nthreads == 1) {
+      if (bworker(&jobs[i])) rc = -4;
+      started = 0;
+      break;
+    }
+    if (pthread_create(&th[i], NULL, bworker, &jobs[i]) != 0) { rc = -5; break; }
+    ++started;
+  }
+  for (int i = 0; i < started; ++i) {
+    void* ret = NULL;
+    pthread_join(th[i], &ret);
+    if (ret) rc = -4;
+  }
+  if (rc == 0) {
+    for (int i = 0; i < nthreads; ++i) {
+      const bjob_t* jb = &jobs[i];
+      for (size_t k = 0; k < nDN; ++k) dA[k] += jb->dA[k];
+      for (size_t k = 0; k < 2 * nBLN; ++k) { dBc[k] += jb->dBc[k]; dCc[k] += jb->dCc[k]; }
+      for (size_t k = 0; k < nBLN; ++k) dtheta[k] += jb->dtheta[k];
+      if (dlam) for (size_t k = 0; k < nBL; ++k) dlam[k] += jb->dlam[k];
+      for (int64_t k = 0; k < D; ++k) dDskip[k] += jb->dD[k];
+    }
+  }
+  free(buf); free(th); free(jobs);
+  return rc < 0 ? rc : nthreads;
+}

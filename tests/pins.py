@@ -288,6 +288,87 @@ def pin_golden(lib):
         assert np.max(np.abs(y - y_expect)) <= 1e-12, (name, y, y_expect)
 
 
+# ---------------------------------------------------------------------------- backward
+GRAD_OF = {"x": "dx", "delta": "ddelta", "A": "dA", "Bc": "dBc", "Cc": "dCc", "theta": "dtheta",
+           "lam": "dlam", "Dskip": "dDskip"}
+
+
+def run_backward(lib, c, dy, mode):
+    return oracle.backward(c["x"], c["delta"], c["A"], c["Bc"], c["Cc"], c["theta"], c["lam"], c["Dskip"], dy,
+                           mode, lib=lib)
+
+
+def pin_backward_finite_differences(lib):
+    """Every gradient of l = sum(dy * y) equals the central finite difference of the forward
+    oracle (itself pinned above), entry by entry, for both modes on tiny inputs. The
+    backward's formulas come from differentiating the recurrence; this checks them against
+    the definition of a derivative, with no shared arithmetic."""
+    rng = np.random.default_rng(23)
+    for mode in (0, 1):
+        c = random_case(rng, 2, 6, 2, 3, mode)
+        dy = rng.standard_normal((2, 6, 2))
+        g = run_backward(lib, c, dy, mode)
+        loss = lambda cc: float(np.sum(dy * run(lib, cc, mode)))
+        for key, gname in GRAD_OF.items():
+            if c[key] is None:
+                continue
+            units = [1.0, 1j] if np.iscomplexobj(c[key]) else [1.0]
+            for unit in units:
+                fd = np.zeros(c[key].shape)
+                for idx in np.ndindex(c[key].shape):
+                    h = 1e-6 * max(1.0, abs(c[key][idx]))
+                    cp = dict(c)
+                    cp[key] = c[key].copy()
+                    cp[key][idx] += h * unit
+                    lp = loss(cp)
+                    cp[key][idx] -= 2 * h * unit
+                    lm = loss(cp)
+                    fd[idx] = (lp - lm) / (2 * h)
+                an = g[gname]
+                if np.iscomplexobj(an):
+                    an = an.real if unit == 1.0 else an.imag
+                e = rel_err(an, fd)
+                assert e < 1e-6, f"mode {mode}: d/d{key} {'re' if unit == 1.0 else 'im'} differs from finite differences: {e:.2e}"
+
+
+def pin_backward_identities(lib):
+    """Exact identities of the gradients at a size beyond the finite-difference pin.
+    y is homogeneous of degree one in x, and y - Dskip x is so in Bc and in Cc (the
+    injection is linear in x and Bc, the output linear in Cc), so by Euler's theorem
+    <dx, x> = <dy, y>, <dBc, Bc> = <dCc, Cc> = <dy, y - Dskip x>, <dDskip, Dskip> = <dy, Dskip x>.
+    Scaling A by c and dt by 1/c leaves every a_t unchanged and scales every injection
+    (both modes carry one factor dt_t) by 1/c, so sum A dA - sum dt ddt = -<dy, y - Dskip x>.
+    y is affine in each lam_t, so a central difference of any step is exact: checked on a
+    few steps with a large step size."""
+    rng = np.random.default_rng(29)
+    for mode in (0, 1):
+        c = random_case(rng, 2, 40, 5, 4, mode)
+        dy = rng.standard_normal((2, 40, 5))
+        y = run(lib, c, mode)
+        g = run_backward(lib, c, dy, mode)
+        dskip_x = c["Dskip"][None, None, :] * c["x"]
+        ssm = float(np.sum(dy * (y - dskip_x)))
+        scale = float(np.sum(np.abs(dy * y)))
+        def close(a, b, what):
+            assert abs(a - b) <= 1e-10 * scale, f"mode {mode}: {what}: {a!r} vs {b!r}"
+        close(float(np.sum(g["dx"] * c["x"])), float(np.sum(dy * y)), "<dx, x> = <dy, y>")
+        cdot = lambda gz, z: float(np.sum(gz.real * z.real + gz.imag * z.imag))
+        close(cdot(g["dBc"], c["Bc"]), ssm, "<dBc, Bc> = <dy, y - Dx>")
+        close(cdot(g["dCc"], c["Cc"]), ssm, "<dCc, Cc> = <dy, y - Dx>")
+        close(float(np.sum(g["dDskip"] * c["Dskip"])), float(np.sum(dy * dskip_x)), "<dD, D> = <dy, Dx>")
+        close(float(np.sum(g["dA"] * c["A"]) - np.sum(g["ddelta"] * c["delta"])), -ssm,
+              "sum A dA - sum dt ddt = -<dy, y - Dx>")
+        if mode == 1:
+            for (b, t) in [(0, 0), (1, 17), (0, 39)]:
+                cp = dict(c)
+                cp["lam"] = c["lam"].copy()
+                cp["lam"][b, t] += 0.5
+                lp = float(np.sum(dy * run(lib, cp, mode)))
+                cp["lam"][b, t] -= 1.0
+                lm = float(np.sum(dy * run(lib, cp, mode)))
+                close(g["dlam"][b, t], lp - lm, f"dlam[{b},{t}] (y is affine in lam)")
+
+
 ALL_PINS = [pin_combine_associative, pin_combine_is_composition, pin_bruteforce, pin_closed_form,
             pin_real_reduction, pin_rotation, pin_lambda_one, pin_linearity_and_causality,
-            pin_split_invariance, pin_golden]
+            pin_split_invariance, pin_golden, pin_backward_finite_differences, pin_backward_identities]

@@ -50,6 +50,27 @@ MUTANTS = [
     ("initial state ignored", "h[n] = j->h0 ? load_c(j->h0, (b * D + d) * N + n) : 0.0;", "h[n] = 0.0;"),
     ("halo x ignored", "else if (j->x_prev) x_prev = j->x_prev[b * D + d];", "else if (j->x_prev) x_prev = 0.0;"),
     ("apply drops the multiplier", "cplx r = a * hh + u;", "cplx r = hh + u;"),
+    # backward
+    ("adjoint carried by a instead of conj(a)", "carry[n] = conj(a) * ghat;", "carry[n] = a * ghat;"),
+    ("adjoint reads C unconjugated", "const cplx ghat = dyt * conj(load_c(j->Cc, tn)) + carry[n];",
+     "const cplx ghat = dyt * load_c(j->Cc, tn) + carry[n];"),
+    ("adjoint drops the carry", "const cplx ghat = dyt * conj(load_c(j->Cc, tn)) + carry[n];",
+     "const cplx ghat = dyt * conj(load_c(j->Cc, tn));"),
+    ("transition gradient from h_t", "cplx Ga = ghat * conj(h_prev);", "cplx Ga = ghat * conj(h);"),
+    ("exp chain rule without conj(a)", "const cplx Gz = conj(a) * Ga;", "const cplx Gz = Ga;"),
+    ("theta gradient from the real part", "j->dtheta[tn] += cimag(Gz);", "j->dtheta[tn] += creal(Gz);"),
+    ("A gradient without dt", "j->dA[d * N + n] += dtt * creal(Gz);", "j->dA[d * N + n] += creal(Gz);"),
+    ("C gradient unconjugated", "load_c(j->dCc, tn) + dyt * conj(h)", "load_c(j->dCc, tn) + dyt * h"),
+    ("exp-Euler B gradient without dt", "load_c(j->dBc, tn) + (dtt * xt) * ghat", "load_c(j->dBc, tn) + xt * ghat"),
+    ("beta's x gradient sent to x_t", "if (t > 0) j->dx[td - D] += (1.0 - lam) * dtt * R;",
+     "j->dx[td] += (1.0 - lam) * dtt * R;"),
+    ("beta's B gradient without conj(a)", "c2 * conj(a) * ghat", "c2 * ghat"),
+    ("beta's transition gradient dropped", "Ga += ghat * conj(c2 * Bp);", "Ga += 0.0;"),
+    ("lam gradient sign", "j->dlam[b * L + t] += dtt * xt * P - dtt * x_prev * R;",
+     "j->dlam[b * L + t] += dtt * xt * P + dtt * x_prev * R;"),
+    ("D-skip gradient without dy", "j->dD[d] += dyt * xt;", "j->dD[d] += xt;"),
+    ("x gradient misses the D-skip", "j->dx[td] += gx + j->Dskip[d] * dyt;", "j->dx[td] += gx;"),
+    ("dt gradient misses the decay", "j->ddt[td] += gdt + dz_re;", "j->ddt[td] += gdt;"),
 ]
 
 
