@@ -168,6 +168,30 @@ int csscan_decode_step(const void* x, const void* delta, const float* A, const v
                        cudaStream_t stream);
 
 /*
+ * Backward pass of csscan_forward (sequence from the zero state, no step -1 halo): the
+ * gradients of l = sum_{b,t,d} dy[b,t,d] y[b,t,d] with respect to every input. The pages call
+ * for this pass and for regenerating the states during it instead of storing them ("Complex
+ * parallel scan", sections 一个问题，两种命运 and 硬件落地的挑战); the formulas are reverse-mode
+ * differentiation of the recurrence above. States are recomputed from checkpoints taken every
+ * 8 steps; the (B, L, D, N) state is never stored.
+ *   x .. Dskip, B, L, D, N, mode, dtype : exactly as passed to csscan_forward
+ *   dy      : device float32 (B, L, D), the gradient of the loss with respect to y
+ * Outputs (device float32, caller-owned, fully written by the call, any alignment of 4 bytes):
+ *   dx, ddelta : (B, L, D)          dA : (D, N)          dDskip : (D)
+ *   dBc, dCc   : (B, L, N, 2), (d/dRe, d/dIm) of each complex entry
+ *   dtheta     : (B, L, N)          dlambda : (B, L), trapezoid mode only (may be NULL in exp-Euler mode)
+ * Inputs need only their element alignment (no 16-byte rule). N must be 2, 4, 8, 16 or 32
+ * (CSSCAN_ERR_UNSUPPORTED otherwise) and B <= 65535. The library grows its per-stream
+ * workspace to B*L*N*8 + B*ceil(L/8)*D*N*8 bytes (rotation table and checkpoints). Sums over
+ * rows use float32 atomic adds, so the summed gradients (dA, dBc, dCc, dtheta, dlambda,
+ * dDskip) can differ in the last bits from run to run.
+ */
+int csscan_backward(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                    const void* theta, const void* lambda, const float* Dskip, const float* dy, float* dx,
+                    float* ddelta, float* dA, float* dBc, float* dCc, float* dtheta, float* dlambda, float* dDskip,
+                    int64_t B, int64_t L, int64_t D, int64_t N, int mode, int dtype, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device-side status of the calls made on it since
  * the last query (CSSCAN_OK, CSSCAN_ERR_LOOKBACK_TIMEOUT or CSSCAN_ERR_PIPELINE_TIMEOUT), or
  * CSSCAN_ERR_CUDA if the stream reports an error. Clears the device status.

@@ -1,7 +1,8 @@
 // csscan.cu -- host side of the C ABI declared in include/csscan.h: argument checks,
 // launch planning (block width, sequence chunks, shared-memory ring), the per-(device,
 // stream) workspace, tile-copy descriptors, and the launches of the rotation-table kernel
-// and the scan kernel (scan_kernels.cuh).
+// and the scan kernel (scan_kernels.cuh), the decode step (decode_kernel.cuh) and the
+// backward pass (backward_kernels.cuh).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -13,6 +14,7 @@
 #include <utility>
 
 #include "csscan.h"
+#include "backward_kernels.cuh"
 #include "decode_kernel.cuh"
 #include "scan_kernels.cuh"
 
@@ -466,6 +468,125 @@ int decode_impl(const void* x, const void* delta, const float* A, const void* Bc
   return mode == 0 ? dispatch_decode<uint16_t, 0>(dp, stream) : dispatch_decode<uint16_t, 1>(dp, stream);
 }
 
+// ----------------------------------------------------------------------------- backward
+struct BwdArgs {
+  const void *x, *delta, *Bc, *Cc, *theta, *lam;
+  const float *A, *Dskip, *dy;
+  float *dx, *ddelta, *dA, *dBc, *dCc, *dtheta, *dlam, *dDskip;
+  int64_t B, L, D, N;
+  int mode, dtype;
+};
+
+template <typename Tin, int MODE, int N>
+int launch_backward(const BwdArgs& a, cudaStream_t st) {
+  int dev = 0;
+  CSSCAN_CUDA(cudaGetDevice(&dev));
+  const int64_t S = (a.L + bwd::SEG - 1) / bwd::SEG;
+  const size_t rot_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float2), 256);
+  const size_t ckpt_bytes = size_t(a.B * S * a.D * N) * sizeof(float2);
+  WsEntry ws;
+  int rc = get_workspace(dev, st, 1, rot_bytes + ckpt_bytes, &ws);
+  if (rc != CSSCAN_OK) return rc;
+  char* rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
+
+  // gradients that are sums over several rows are accumulated and start at zero
+  CSSCAN_CUDA(cudaMemsetAsync(a.dA, 0, size_t(a.D * N) * 4, st));
+  CSSCAN_CUDA(cudaMemsetAsync(a.dBc, 0, size_t(a.B * a.L * N) * 8, st));
+  CSSCAN_CUDA(cudaMemsetAsync(a.dCc, 0, size_t(a.B * a.L * N) * 8, st));
+  CSSCAN_CUDA(cudaMemsetAsync(a.dtheta, 0, size_t(a.B * a.L * N) * 4, st));
+  if (MODE == 1) CSSCAN_CUDA(cudaMemsetAsync(a.dlam, 0, size_t(a.B * a.L) * 4, st));
+  CSSCAN_CUDA(cudaMemsetAsync(a.dDskip, 0, size_t(a.D) * 4, st));
+
+  bwd::Params p;
+  p.x = a.x;
+  p.dt = a.delta;
+  p.Bc = a.Bc;
+  p.Cc = a.Cc;
+  p.lam = MODE == 1 ? a.lam : nullptr;
+  p.A = a.A;
+  p.Dskip = a.Dskip;
+  p.dy = a.dy;
+  p.dx = a.dx;
+  p.ddt = a.ddelta;
+  p.dA = a.dA;
+  p.dBc = a.dBc;
+  p.dCc = a.dCc;
+  p.dtheta = a.dtheta;
+  p.dlam = MODE == 1 ? a.dlam : nullptr;
+  p.dD = a.dDskip;
+  p.rot = reinterpret_cast<const float2*>(rest);
+  p.ckpt = reinterpret_cast<float2*>(rest + rot_bytes);
+  p.B = int(a.B);
+  p.L = int(a.L);
+  p.D = int(a.D);
+  p.N = N;
+  p.S = int(S);
+
+  const long long n_rot = (long long)a.B * a.L * N;
+  bwd::rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest), n_rot);
+  CSSCAN_CUDA(cudaGetLastError());
+  if (S > 1) {
+    const long long n_ck = (long long)a.B * a.D * N;
+    bwd::ckpt_kernel<Tin, MODE><<<unsigned((n_ck + 255) / 256), 256, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+  }
+  const dim3 grid{unsigned((a.D + bwd::GradTile<N>::CB - 1) / bwd::GradTile<N>::CB), unsigned(a.B)};
+  bwd::grad_kernel<Tin, MODE, N><<<grid, bwd::THREADS, 0, st>>>(p);
+  CSSCAN_CUDA(cudaGetLastError());
+  return CSSCAN_OK;
+}
+
+template <typename Tin, int MODE>
+int dispatch_backward(const BwdArgs& a, cudaStream_t st) {
+  switch (a.N) {
+    case 2: return launch_backward<Tin, MODE, 2>(a, st);
+    case 4: return launch_backward<Tin, MODE, 4>(a, st);
+    case 8: return launch_backward<Tin, MODE, 8>(a, st);
+    case 16: return launch_backward<Tin, MODE, 16>(a, st);
+    case 32: return launch_backward<Tin, MODE, 32>(a, st);
+    default: return CSSCAN_ERR_UNSUPPORTED;
+  }
+}
+
+int backward_impl(const BwdArgs& a, cudaStream_t st) {
+  if (a.mode != CSSCAN_MODE_EXP_EULER && a.mode != CSSCAN_MODE_EXP_TRAPEZOID) return CSSCAN_ERR_INVALID_ARG;
+  if (a.dtype != CSSCAN_F32 && a.dtype != CSSCAN_BF16) return CSSCAN_ERR_INVALID_ARG;
+  if (a.B < 0 || a.L < 0 || a.D < 0 || a.N <= 0) return CSSCAN_ERR_INVALID_ARG;
+  // arrays with no elements may be NULL (an empty tensor has no storage)
+  const bool rows = a.B > 0 && a.L > 0, chans = a.D > 0;
+  if (chans && (!a.A || !a.Dskip || !a.dA || !a.dDskip)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && (!a.Bc || !a.Cc || !a.theta || !a.dBc || !a.dCc || !a.dtheta)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && chans && (!a.x || !a.delta || !a.dy || !a.dx || !a.ddelta)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && a.mode == CSSCAN_MODE_EXP_TRAPEZOID && (!a.lam || !a.dlam)) return CSSCAN_ERR_INVALID_ARG;
+  if (a.N != 2 && a.N != 4 && a.N != 8 && a.N != 16 && a.N != 32) return CSSCAN_ERR_UNSUPPORTED;
+  if (a.B > 65535 || a.L > (int64_t(1) << 30) || a.D > (int64_t(1) << 30) ||
+      a.B * a.L * a.D > (int64_t(1) << 40))
+    return CSSCAN_ERR_UNSUPPORTED;
+  const size_t s = a.dtype == CSSCAN_F32 ? 4 : 2;
+  if (!aligned(a.x, s) || !aligned(a.delta, s) || !aligned(a.Bc, s) || !aligned(a.Cc, s) || !aligned(a.theta, s) ||
+      (a.lam && !aligned(a.lam, s)) || !aligned(a.A, 4) || !aligned(a.Dskip, 4) || !aligned(a.dy, 4) ||
+      !aligned(a.dx, 4) || !aligned(a.ddelta, 4) || !aligned(a.dA, 4) || !aligned(a.dBc, 4) || !aligned(a.dCc, 4) ||
+      !aligned(a.dtheta, 4) || (a.dlam && !aligned(a.dlam, 4)) || !aligned(a.dDskip, 4))
+    return CSSCAN_ERR_MISALIGNED;
+  if (a.B == 0 || a.L == 0 || a.D == 0) {
+    // no steps or no channels: every gradient is an empty sum
+    if (a.D > 0) {
+      CSSCAN_CUDA(cudaMemsetAsync(a.dA, 0, size_t(a.D * a.N) * 4, st));
+      CSSCAN_CUDA(cudaMemsetAsync(a.dDskip, 0, size_t(a.D) * 4, st));
+    }
+    if (a.B > 0 && a.L > 0) {
+      CSSCAN_CUDA(cudaMemsetAsync(a.dBc, 0, size_t(a.B * a.L * a.N) * 8, st));
+      CSSCAN_CUDA(cudaMemsetAsync(a.dCc, 0, size_t(a.B * a.L * a.N) * 8, st));
+      CSSCAN_CUDA(cudaMemsetAsync(a.dtheta, 0, size_t(a.B * a.L * a.N) * 4, st));
+      if (a.mode == CSSCAN_MODE_EXP_TRAPEZOID) CSSCAN_CUDA(cudaMemsetAsync(a.dlam, 0, size_t(a.B * a.L) * 4, st));
+    }
+    return CSSCAN_OK;
+  }
+  if (a.dtype == CSSCAN_F32)
+    return a.mode == 0 ? dispatch_backward<float, 0>(a, st) : dispatch_backward<float, 1>(a, st);
+  return a.mode == 0 ? dispatch_backward<uint16_t, 0>(a, st) : dispatch_backward<uint16_t, 1>(a, st);
+}
+
 // ----------------------------------------------------------------------------- no-allocation entry
 // csscan_forward_noalloc runs the same two kernels with its scratch in one fixed array that
 // is part of the library's device code, so it never calls cudaMalloc. Layout of the array:
@@ -589,6 +710,15 @@ int csscan_forward_noalloc(const void* x, const void* delta, const float* A, con
                        : dispatch_noalloc<float, 1>(a, device_status, stream);
   return a.mode == 0 ? dispatch_noalloc<uint16_t, 0>(a, device_status, stream)
                      : dispatch_noalloc<uint16_t, 1>(a, device_status, stream);
+}
+
+int csscan_backward(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
+                    const void* theta, const void* lambda, const float* Dskip, const float* dy, float* dx,
+                    float* ddelta, float* dA, float* dBc, float* dCc, float* dtheta, float* dlambda, float* dDskip,
+                    int64_t B, int64_t L, int64_t D, int64_t N, int mode, int dtype, cudaStream_t stream) {
+  BwdArgs a{x, delta, Bc, Cc, theta, lambda, A, Dskip, dy, dx, ddelta, dA, dBc, dCc, dtheta, dlambda, dDskip,
+            B, L, D, N, mode, dtype};
+  return backward_impl(a, stream);
 }
 
 int csscan_get_device_status(cudaStream_t stream) {

@@ -70,6 +70,8 @@ def load_library(path: str = LIBRARY) -> ctypes.CDLL:
     lib.csscan_forward_state.restype = i32
     lib.csscan_decode_step.argtypes = [vp] * 12 + [i64] * 3 + [i32, i32, vp]
     lib.csscan_decode_step.restype = i32
+    lib.csscan_backward.argtypes = [vp] * 17 + [i64] * 4 + [i32, i32, vp]
+    lib.csscan_backward.restype = i32
     _lib = lib
     return lib
 
@@ -151,6 +153,27 @@ def csscan_decode_step(x, delta, A, Bc, Cc, theta, lam, Dskip, y, h, mode: int, 
         _ptr(x_prev), _ptr(Bc_prev), B, D, N, int(mode), _dtype_code(x), _stream_handle(stream))
     if rc != CSSCAN_OK:
         raise CsscanError(rc, "csscan_decode_step")
+
+
+def csscan_backward(x, delta, A, Bc, Cc, theta, lam, Dskip, dy, mode: int, stream=None, out=None) -> dict:
+    """Gradients of sum(dy * y) for csscan_forward from the zero state. Inputs as
+    csscan_forward plus dy (B, L, D) float32. Returns (or fills ``out``, a dict of float32 CUDA
+    tensors with these keys and shapes) dx, ddelta (B,L,D); dA (D,N); dBc, dCc (B,L,N,2);
+    dtheta (B,L,N); dlam (B,L) in the trapezoid mode (None otherwise); dDskip (D,)."""
+    B, L, D = x.shape
+    N = A.shape[1]
+    if out is None:
+        f = lambda *shape: torch.empty(shape, dtype=torch.float32, device=x.device)
+        out = dict(dx=f(B, L, D), ddelta=f(B, L, D), dA=f(D, N), dBc=f(B, L, N, 2), dCc=f(B, L, N, 2),
+                   dtheta=f(B, L, N), dlam=f(B, L) if mode == CSSCAN_MODE_EXP_TRAPEZOID else None, dDskip=f(D))
+    rc = load_library().csscan_backward(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(Bc), _ptr(Cc), _ptr(theta), _ptr(lam), _ptr(Dskip), _ptr(dy),
+        _ptr(out["dx"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dBc"]), _ptr(out["dCc"]),
+        _ptr(out["dtheta"]), _ptr(out.get("dlam")), _ptr(out["dDskip"]), B, L, D, N, int(mode), _dtype_code(x),
+        _stream_handle(stream))
+    if rc != CSSCAN_OK:
+        raise CsscanError(rc, "csscan_backward")
+    return out
 
 
 def csscan_get_device_status(stream=None) -> int:

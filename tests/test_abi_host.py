@@ -93,3 +93,20 @@ def test_state_and_decode_reject_bad_arguments_on_host(lib):
     assert dec(*args(x=None)) == csscan.CSSCAN_ERR_INVALID_ARG
     assert dec(*args(mode=1, lam=None)) == csscan.CSSCAN_ERR_INVALID_ARG
     assert dec(*args(mode=1, xp=A16)) == csscan.CSSCAN_ERR_INVALID_ARG
+
+
+def test_backward_rejects_bad_arguments_on_host(lib):
+    bw = lib.csscan_backward
+    def args(**k):
+        return [k.get("x", A16), A16, A16, A16, A16, A16, k.get("lam", A16), A16, k.get("dy", A16),
+                k.get("dx", A16), A16, A16, A16, A16, A16, k.get("dlam", A16), A16,
+                k.get("B", 2), 64, 16, k.get("N", 8), k.get("mode", 0), k.get("dtype", 0), None]
+    assert bw(*args(N=64)) == csscan.CSSCAN_ERR_UNSUPPORTED      # the backward covers N <= 32
+    assert bw(*args(N=3)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert bw(*args(B=70000)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert bw(*args(mode=1, dlam=None)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert bw(*args(mode=1, lam=None)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert bw(*args(dy=None)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert bw(*args(mode=3)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert bw(*args(dx=A16 + 2)) == csscan.CSSCAN_ERR_MISALIGNED
+    assert bw(*args(x=A16 + 1, dtype=1)) == csscan.CSSCAN_ERR_MISALIGNED
