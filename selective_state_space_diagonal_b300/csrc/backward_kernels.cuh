@@ -15,10 +15,19 @@
 //                  with P_t = Re(conj(Bc_t) ghat_t) and R_t = Re(conj(a_t Bc_{t-1}) ghat_t)
 //   output         dCc_t += dy_t conj(h_t),  dx_t += Dskip dy_t,  dDskip += dy_t x_t
 //
-// Three kernels:
-//   rot_kernel    e^{i theta} per (b, t, n), shared by every channel;
-//   ckpt_kernel   one thread per (b, d, n) runs the forward recurrence and stores the state
-//                 before every segment of SEG steps;
+// The sequence is cut into C chunks of TC steps so that all chunks run at once. Both sweeps are
+// affine maps per chunk, which is the combine of the step operators ("Complex parallel scan",
+// section 并行扫描的数学本质) applied forwards to the state and backwards to the adjoint:
+//   h_end = P_c h_in + U_c                  P_c = prod of a_t over the chunk
+//   ghat_first = Q_c carry_c + W_c          carry_c = conj(a_te) ghat_te (te: next chunk's first step)
+// Kernels:
+//   rot_kernel        e^{i theta} per (b, t, n), shared by every channel;
+//   chunk_fwd_kernel  per (b, c, d, n): U_c and P_c from a zero state       (only when C > 1)
+//   chunk_adj_kernel  per (b, c, d, n): W_c, Q_c and conj(a_tc) from a zero carry  (C > 1)
+//   chunk_combine_kernel  per (b, d, n): walks the C chunks forwards for each chunk's true
+//                     entry state and backwards for each chunk's true first-step adjoint;
+//   ckpt_kernel       per (b, c, d, n): the forward recurrence over the chunk from its entry
+//                     state, storing the state before every segment of SEG steps;
 //   grad_kernel   a thread owns one state n of K channels of one batch row. For each segment,
 //                 last to first, and each of its channels it recomputes the segment's SEG states
 //                 from the checkpoint into registers, then walks the segment backwards. Sums over
@@ -56,7 +65,9 @@ struct Params {
   float* dD;           // (D)            accumulated
   const float2* rot;   // (B, L, N)      e^{i theta}
   float2* ckpt;        // (B, S, D, N)   state before segment s (s >= 1)
+  float2* chunk;       // (B, C, D, N, 5) per chunk: U | h_in, P, W | ghat_first, Q, conj(a_tc)
   int B, L, D, N, S;
+  int TC, C;           // chunk length (a multiple of SEG) and chunk count
 };
 
 // Channels per block of grad_kernel: K slots per thread x (32 / N) channels per warp x WARPS.
@@ -76,48 +87,228 @@ __global__ void __launch_bounds__(256) rot_kernel(const void* theta, float2* rot
   rot[i] = make_float2(c, s);
 }
 
-// Forward recurrence per (b, d, n), storing h_{s SEG - 1} for s = 1 .. S-1.
+// The forward recurrence of one (b, d, n) over groups of SEG steps: every load of a group is
+// issued before its arithmetic, so that the group's memory latencies overlap.
 template <typename Tin, int MODE>
-__global__ void __launch_bounds__(256) ckpt_kernel(const Params p) {
+struct FwdStep {
+  const Tin *X, *DT, *BC, *LAM;
+  const float2* rot;
+  long long b;
+  int L, D, N, d, n;
+  float a2;
+  // steps t0 .. min(t0 + SEG, te) - 1: h <- a_t h + u_t; xp, bpr, bpi hold x_{t-1}, Bc_{t-1}
+  // (trapezoid) and advance; P (if given) is multiplied by every a_t
+  __device__ __forceinline__ void group(int t0, int te, float& hr, float& hi, float& xp, float& bpr, float& bpi,
+                                        float* Pr = nullptr, float* Pi = nullptr) const {
+    float xs[SEG], ds[SEG], brs[SEG], bis[SEG], ls[SEG];
+    float2 ros[SEG];
+#pragma unroll
+    for (int i = 0; i < SEG; ++i) {
+      const int t = min(t0 + i, te - 1);
+      const long long td = (b * L + t) * D + d;
+      const long long tn = (b * L + t) * N + n;
+      xs[i] = load_in<Tin>(X, td);
+      ds[i] = load_in<Tin>(DT, td);
+      ros[i] = rot[tn];
+      brs[i] = load_in<Tin>(BC, 2 * tn);
+      bis[i] = load_in<Tin>(BC, 2 * tn + 1);
+      ls[i] = MODE == 1 ? load_in<Tin>(LAM, b * L + t) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < SEG; ++i) {
+      if (t0 + i < te) {
+        const float r = ex2_approx(ds[i] * a2);
+        const float ar = r * ros[i].x, ai = r * ros[i].y;
+        float ur, ui;
+        if (MODE == 0) {
+          const float w = ds[i] * xs[i];
+          ur = w * brs[i];
+          ui = w * bis[i];
+        } else {
+          const float w = ls[i] * ds[i] * xs[i], c2 = (1.f - ls[i]) * ds[i] * xp;
+          ur = w * brs[i] + c2 * (ar * bpr - ai * bpi);
+          ui = w * bis[i] + c2 * (ar * bpi + ai * bpr);
+          xp = xs[i];
+          bpr = brs[i];
+          bpi = bis[i];
+        }
+        const float nr = fmaf(ar, hr, fmaf(-ai, hi, ur));
+        const float ni = fmaf(ar, hi, fmaf(ai, hr, ui));
+        hr = nr;
+        hi = ni;
+        if (Pr) {
+          const float qr = ar * *Pr - ai * *Pi, qi = ar * *Pi + ai * *Pr;
+          *Pr = qr;
+          *Pi = qi;
+        }
+      }
+    }
+  }
+  // the trapezoid's step -1 values for a chunk starting at tc
+  __device__ __forceinline__ void halo(int tc, float& xp, float& bpr, float& bpi) const {
+    xp = bpr = bpi = 0.f;
+    if (MODE == 1 && tc > 0) {
+      const long long tn = (b * L + tc - 1) * N + n;
+      xp = load_in<Tin>(X, (b * L + tc - 1) * D + d);
+      bpr = load_in<Tin>(BC, 2 * tn);
+      bpi = load_in<Tin>(BC, 2 * tn + 1);
+    }
+  }
+};
+
+template <typename Tin, int MODE>
+__device__ __forceinline__ FwdStep<Tin, MODE> fwd_step(const Params& p, long long b, int d, int n) {
+  FwdStep<Tin, MODE> f;
+  f.X = static_cast<const Tin*>(p.x);
+  f.DT = static_cast<const Tin*>(p.dt);
+  f.BC = static_cast<const Tin*>(p.Bc);
+  f.LAM = static_cast<const Tin*>(p.lam);
+  f.rot = p.rot;
+  f.b = b;
+  f.L = p.L;
+  f.D = p.D;
+  f.N = p.N;
+  f.d = d;
+  f.n = n;
+  f.a2 = p.A[(long long)d * p.N + n] * LOG2E;
+  return f;
+}
+
+// Thread (b, c, d, n) from a flat index over B * C * D * N.
+struct ChunkThread {
+  long long b;
+  int c, d, n;
+  bool ok;
+};
+__device__ __forceinline__ ChunkThread chunk_thread(const Params& p) {
+  const long long gid = (long long)blockIdx.x * 256 + threadIdx.x;
+  ChunkThread r;
+  r.ok = gid < (long long)p.B * p.C * p.D * p.N;
+  r.n = int(gid % p.N);
+  long long q = gid / p.N;
+  r.d = int(q % p.D);
+  q /= p.D;
+  r.c = int(q % p.C);
+  r.b = q / p.C;
+  return r;
+}
+__device__ __forceinline__ float2* chunk_rec(const Params& p, long long b, int c, int d, int n) {
+  return p.chunk + ((((b * p.C + c) * p.D + d) * p.N) + n) * 5;
+}
+
+// U_c (state at the chunk's end from a zero entry state) and P_c (product of a over the chunk).
+template <typename Tin, int MODE>
+__global__ void __launch_bounds__(256) chunk_fwd_kernel(const Params p) {
+  const ChunkThread th = chunk_thread(p);
+  if (!th.ok) return;
+  const auto f = fwd_step<Tin, MODE>(p, th.b, th.d, th.n);
+  const int tc = th.c * p.TC, te = min(p.L, tc + p.TC);
+  float hr = 0.f, hi = 0.f, xp, bpr, bpi, Pr = 1.f, Pi = 0.f;
+  f.halo(tc, xp, bpr, bpi);
+  for (int t = tc; t < te; t += SEG) f.group(t, te, hr, hi, xp, bpr, bpi, &Pr, &Pi);
+  float2* rec = chunk_rec(p, th.b, th.c, th.d, th.n);
+  rec[0] = make_float2(hr, hi);
+  rec[1] = make_float2(Pr, Pi);
+}
+
+// W_c (adjoint at the chunk's first step with nothing flowing in from later chunks),
+// Q_c = conj(prod of a over the chunk's steps after the first) and conj(a_tc).
+template <typename Tin, int MODE>
+__global__ void __launch_bounds__(256) chunk_adj_kernel(const Params p) {
+  const ChunkThread th = chunk_thread(p);
+  if (!th.ok) return;
+  const Tin* DT = static_cast<const Tin*>(p.dt);
+  const Tin* CC = static_cast<const Tin*>(p.Cc);
+  const float a2 = p.A[(long long)th.d * p.N + th.n] * LOG2E;
+  const long long b = th.b;
+  const int tc = th.c * p.TC, te = min(p.L, tc + p.TC);
+  float cr = 0.f, ci = 0.f, gr = 0.f, gi = 0.f, Qr = 1.f, Qi = 0.f, ar = 1.f, ai = 0.f;
+  for (int t1 = te - 1; t1 >= tc; t1 -= SEG) {   // groups of SEG steps, last to first
+    float dys[SEG], ccr[SEG], cci[SEG], ds[SEG];
+    float2 ros[SEG];
+#pragma unroll
+    for (int i = 0; i < SEG; ++i) {
+      const int t = max(t1 - i, tc);
+      const long long td = (b * p.L + t) * p.D + th.d;
+      const long long tn = (b * p.L + t) * p.N + th.n;
+      dys[i] = p.dy[td];
+      ccr[i] = load_in<Tin>(CC, 2 * tn);
+      cci[i] = load_in<Tin>(CC, 2 * tn + 1);
+      ds[i] = load_in<Tin>(DT, td);
+      ros[i] = p.rot[tn];
+    }
+#pragma unroll
+    for (int i = 0; i < SEG; ++i) {
+      const int t = t1 - i;
+      if (t >= tc) {
+        gr = fmaf(dys[i], ccr[i], cr);
+        gi = fmaf(-dys[i], cci[i], ci);
+        const float r = ex2_approx(ds[i] * a2);
+        ar = r * ros[i].x;
+        ai = r * ros[i].y;
+        if (t > tc) {
+          cr = ar * gr + ai * gi;   // conj(a_t) ghat_t
+          ci = ar * gi - ai * gr;
+          const float nr = ar * Qr + ai * Qi, ni = ar * Qi - ai * Qr;   // conj(a_t) Q
+          Qr = nr;
+          Qi = ni;
+        }
+      }
+    }
+  }
+  float2* rec = chunk_rec(p, b, th.c, th.d, th.n);
+  rec[2] = make_float2(gr, gi);
+  rec[3] = make_float2(Qr, Qi);
+  rec[4] = make_float2(ar, -ai);
+}
+
+// Walk the chunks of (b, d, n): rec[0] <- entry state h_in, rec[2] <- true adjoint at the
+// chunk's first step.
+__global__ void __launch_bounds__(256) chunk_combine_kernel(const Params p) {
   const long long gid = (long long)blockIdx.x * 256 + threadIdx.x;
   if (gid >= (long long)p.B * p.D * p.N) return;
   const int n = int(gid % p.N);
   const long long bd = gid / p.N;
   const int d = int(bd % p.D);
   const long long b = bd / p.D;
-  const Tin* X = static_cast<const Tin*>(p.x);
-  const Tin* DT = static_cast<const Tin*>(p.dt);
-  const Tin* BC = static_cast<const Tin*>(p.Bc);
-  const Tin* LAM = static_cast<const Tin*>(p.lam);
-  const float a2 = p.A[(long long)d * p.N + n] * LOG2E;
-  float hr = 0.f, hi = 0.f, xp = 0.f, bpr = 0.f, bpi = 0.f;
-  for (int t = 0; t < p.L; ++t) {
-    if (t > 0 && t % SEG == 0) p.ckpt[((b * p.S + t / SEG) * p.D + d) * p.N + n] = make_float2(hr, hi);
-    const long long td = (b * p.L + t) * p.D + d;
-    const long long tn = (b * p.L + t) * p.N + n;
-    const float xt = load_in<Tin>(X, td), dtt = load_in<Tin>(DT, td);
-    const float2 ro = p.rot[tn];
-    const float r = ex2_approx(dtt * a2);
-    const float ar = r * ro.x, ai = r * ro.y;
-    const float br = load_in<Tin>(BC, 2 * tn), bi = load_in<Tin>(BC, 2 * tn + 1);
-    float ur, ui;
-    if (MODE == 0) {
-      const float w = dtt * xt;
-      ur = w * br;
-      ui = w * bi;
-    } else {
-      const float lm = load_in<Tin>(LAM, b * p.L + t);
-      const float w = lm * dtt * xt, c2 = (1.f - lm) * dtt * xp;
-      ur = w * br + c2 * (ar * bpr - ai * bpi);
-      ui = w * bi + c2 * (ar * bpi + ai * bpr);
-      xp = xt;
-      bpr = br;
-      bpi = bi;
-    }
-    const float nr = fmaf(ar, hr, fmaf(-ai, hi, ur));
-    const float ni = fmaf(ar, hi, fmaf(ai, hr, ui));
+  float hr = 0.f, hi = 0.f;
+  for (int c = 0; c < p.C; ++c) {
+    float2* rec = chunk_rec(p, b, c, d, n);
+    const float2 U = rec[0], P = rec[1];
+    rec[0] = make_float2(hr, hi);
+    const float nr = P.x * hr - P.y * hi + U.x, ni = P.x * hi + P.y * hr + U.y;
     hr = nr;
     hi = ni;
+  }
+  float cr = 0.f, ci = 0.f;
+  for (int c = p.C - 1; c >= 0; --c) {
+    float2* rec = chunk_rec(p, b, c, d, n);
+    const float2 W = rec[2], Q = rec[3], ca = rec[4];
+    const float gr = Q.x * cr - Q.y * ci + W.x, gi = Q.x * ci + Q.y * cr + W.y;
+    rec[2] = make_float2(gr, gi);
+    cr = ca.x * gr - ca.y * gi;   // conj(a_tc) ghat_tc: the carry into the previous chunk
+    ci = ca.x * gi + ca.y * gr;
+  }
+}
+
+// Forward recurrence per (b, c, d, n) over chunk c from its entry state, storing h_{s SEG - 1}
+// before every segment s that starts inside the chunk.
+template <typename Tin, int MODE>
+__global__ void __launch_bounds__(256) ckpt_kernel(const Params p) {
+  const ChunkThread th = chunk_thread(p);
+  if (!th.ok) return;
+  const auto f = fwd_step<Tin, MODE>(p, th.b, th.d, th.n);
+  const int tc = th.c * p.TC, te = min(p.L, tc + p.TC);
+  float hr = 0.f, hi = 0.f, xp, bpr, bpi;
+  if (p.C > 1) {
+    const float2 h0 = chunk_rec(p, th.b, th.c, th.d, th.n)[0];
+    hr = h0.x;
+    hi = h0.y;
+  }
+  f.halo(tc, xp, bpr, bpi);
+  for (int t = tc; t < te; t += SEG) {   // chunks start on a segment boundary
+    if (t > tc) p.ckpt[((th.b * p.S + t / SEG) * p.D + th.d) * p.N + th.n] = make_float2(hr, hi);
+    f.group(t, te, hr, hi, xp, bpr, bpi);
   }
 }
 
@@ -153,9 +344,21 @@ __device__ __forceinline__ int butterfly(float (&v)[NARR][SEG], int lane) {
   return base;
 }
 
+// Dynamic shared memory of grad_kernel: one segment's inputs, staged once per block.
+// Rows r = 0 .. SEG + 1 stand for steps t = ts - 1 + r (zeros outside 0 .. L-1 and past D).
+template <int N> struct GradStage {
+  static constexpr int CB = GradTile<N>::CB;
+  static constexpr int OFF_TD = 0;                                        // float4 [SEG+2][CB]: x, dt, dy
+  static constexpr int OFF_TN = OFF_TD + (SEG + 2) * CB * 16;             // float4 [SEG+1][N]: rot c, s, Bc re, im
+  static constexpr int OFF_CC = OFF_TN + (SEG + 1) * N * 16;              // float2 [SEG+1][N]: Cc re, im
+  static constexpr int OFF_LAM = OFF_CC + (SEG + 1) * N * 8;              // float [SEG+2]
+  static constexpr int BYTES = OFF_LAM + (SEG + 2) * 4;
+};
+
 template <typename Tin, int MODE, int N>
 __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
   using GT = GradTile<N>;
+  using GS = GradStage<N>;
   constexpr int CPW = GT::CPW, K = GT::K, CB = GT::CB;
   constexpr int HOLD = SEG >= N ? SEG / N : 1;     // t values a lane holds after the butterfly
   constexpr int DUP = N > SEG ? N / SEG : 1;        // lanes holding the same t values
@@ -165,11 +368,20 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
   __shared__ float s_dD[K][THREADS];
   __shared__ float s_acc[SEG][N][5];   // per (t, n): dBc re, im, dCc re, im, dtheta
   __shared__ float s_lam[SEG];
+  extern __shared__ __align__(16) unsigned char g_stage[];
+  float4 (*s_td)[CB] = reinterpret_cast<float4 (*)[CB]>(g_stage + GS::OFF_TD);
+  float4 (*s_tn)[N] = reinterpret_cast<float4 (*)[N]>(g_stage + GS::OFF_TN);
+  float2 (*s_cc)[N] = reinterpret_cast<float2 (*)[N]>(g_stage + GS::OFF_CC);
+  float* s_lv = reinterpret_cast<float*>(g_stage + GS::OFF_LAM);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = lane % N, cl = lane / N;
   const long long b = blockIdx.y;
   const int dbase = blockIdx.x * CB;
+  const int chunk = blockIdx.z;
+  const int s_first = chunk * (p.TC / SEG);
+  const int s_last = min(p.S, (chunk + 1) * (p.TC / SEG)) - 1;
+  const int t_end = min(p.L, (chunk + 1) * p.TC);   // first step after this chunk
   const Tin* X = static_cast<const Tin*>(p.x);
   const Tin* DT = static_cast<const Tin*>(p.dt);
   const Tin* BC = static_cast<const Tin*>(p.Bc);
@@ -177,19 +389,67 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
   const Tin* LAM = static_cast<const Tin*>(p.lam);
   const long long L = p.L, D = p.D;
 
+  // the adjoint entering from the next chunk: carry = conj(a_te) ghat_te and R_te
 #pragma unroll 1
   for (int j = 0; j < K; ++j) {
-    s_state[j][tid] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 st = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int d = dbase + (j * WARPS + warp) * CPW + cl;
+    if (chunk + 1 < p.C && d < p.D) {
+      const float2 g = chunk_rec(p, b, chunk + 1, d, n)[2];
+      const long long td = (b * L + t_end) * D + d;
+      const long long tn = (b * L + t_end) * N + n;
+      const float r = ex2_approx(load_in<Tin>(DT, td) * p.A[(long long)d * N + n] * LOG2E);
+      const float2 ro = p.rot[tn];
+      const float ar = r * ro.x, ai = r * ro.y;
+      st.x = ar * g.x + ai * g.y;
+      st.y = ar * g.y - ai * g.x;
+      if (MODE == 1) {
+        const float bpr = load_in<Tin>(BC, 2 * (tn - N)), bpi = load_in<Tin>(BC, 2 * (tn - N) + 1);
+        const float vr = ar * bpr - ai * bpi, vi = ar * bpi + ai * bpr;   // a_te Bc_{te-1}
+        st.z = vr * g.x + vi * g.y;
+      }
+    }
+    s_state[j][tid] = st;
     s_dD[j][tid] = 0.f;
   }
   for (int k = tid; k < SEG * N * 5; k += THREADS) (&s_acc[0][0][0])[k] = 0.f;
   if (tid < SEG) s_lam[tid] = 0.f;
-  __syncthreads();
 
 #pragma unroll 1
-  for (int s = p.S - 1; s >= 0; --s) {
+  for (int s = s_last; s >= s_first; --s) {
     const int ts = s * SEG;
     const int nt = min(SEG, p.L - ts);
+    // ---- stage this segment's inputs (rows t = ts - 1 .. ts + SEG)
+    for (int k = tid; k < (SEG + 2) * CB; k += THREADS) {
+      const int r = k / CB, c = k % CB;
+      const long long t = ts - 1 + r, d = dbase + c;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t >= 0 && t < L && d < D) {
+        const long long td = (b * L + t) * D + d;
+        v = make_float4(load_in<Tin>(X, td), load_in<Tin>(DT, td), p.dy[td], 0.f);
+      }
+      s_td[r][c] = v;
+    }
+    for (int k = tid; k < (SEG + 1) * N; k += THREADS) {
+      const int r = k / N, nn = k % N;
+      const long long t = ts - 1 + r;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      float2 c = make_float2(0.f, 0.f);
+      if (t >= 0 && t < L) {
+        const long long tn = (b * L + t) * N + nn;
+        const float2 ro = p.rot[tn];
+        v = make_float4(ro.x, ro.y, load_in<Tin>(BC, 2 * tn), load_in<Tin>(BC, 2 * tn + 1));
+        c = make_float2(load_in<Tin>(CC, 2 * tn), load_in<Tin>(CC, 2 * tn + 1));
+      }
+      s_tn[r][nn] = v;
+      s_cc[r][nn] = c;
+    }
+    if (tid < SEG + 2) {
+      const long long t = ts - 1 + tid;
+      s_lv[tid] = (MODE == 1 && t >= 0 && t < L) ? load_in<Tin>(LAM, b * L + t) : 0.f;
+    }
+    __syncthreads();
+
     float acc[SEG][5];
 #pragma unroll
     for (int i = 0; i < SEG; ++i)
@@ -202,59 +462,51 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
 
 #pragma unroll 1
     for (int j = 0; j < K; ++j) {
-      const int d = dbase + (j * WARPS + warp) * CPW + cl;
+      const int cb = (j * WARPS + warp) * CPW + cl;   // channel within the block
+      const int d = dbase + cb;
       const bool valid = d < p.D;
       const long long dd = valid ? d : 0;
-      // an absent channel runs with x = dy = 0, which makes every contribution exactly zero
-      const float vmask = valid ? 1.f : 0.f;
-      const float a2 = p.A[dd * N + n] * LOG2E;
+      // an absent channel was staged with x = dt = dy = 0: every contribution is exactly zero
       const float Ad = p.A[dd * N + n];
+      const float a2 = Ad * LOG2E;
       const float Ds = p.Dskip[dd];
       float4 st = s_state[j][tid];
       float cgr = st.x, cgi = st.y, Rn = st.z, dA_acc = st.w;
       float dD_acc = s_dD[j][tid];
 
-      // ---- forward: the segment's states from the checkpoint
+      // ---- forward: the segment's states from the checkpoint (or the chunk's entry state)
       float h0r = 0.f, h0i = 0.f;
-      if (s > 0 && valid) {
+      if (valid && s > s_first) {
         const float2 c = p.ckpt[((b * p.S + s) * D + dd) * N + n];
+        h0r = c.x;
+        h0i = c.y;
+      } else if (valid && s == s_first && chunk > 0) {
+        const float2 c = chunk_rec(p, b, chunk, int(dd), n)[0];
         h0r = c.x;
         h0i = c.y;
       }
       float hsr[SEG], hsi[SEG];
       {
         float hr = h0r, hi = h0i;
-        float xp = 0.f, bpr = 0.f, bpi = 0.f;
-        if (MODE == 1 && ts > 0) {
-          const long long tn = (b * L + ts - 1) * N + n;
-          xp = vmask * load_in<Tin>(X, (b * L + ts - 1) * D + dd);
-          bpr = load_in<Tin>(BC, 2 * tn);
-          bpi = load_in<Tin>(BC, 2 * tn + 1);
-        }
 #pragma unroll
         for (int i = 0; i < SEG; ++i) {
           if (i < nt) {
-            const long long t = ts + i;
-            const long long td = (b * L + t) * D + dd;
-            const long long tn = (b * L + t) * N + n;
-            const float xt = vmask * load_in<Tin>(X, td), dtt = load_in<Tin>(DT, td);
-            const float2 ro = p.rot[tn];
+            const float4 v = s_td[i + 1][cb];
+            const float4 q = s_tn[i + 1][n];
+            const float xt = v.x, dtt = v.y;
             const float r = ex2_approx(dtt * a2);
-            const float ar = r * ro.x, ai = r * ro.y;
-            const float br = load_in<Tin>(BC, 2 * tn), bi = load_in<Tin>(BC, 2 * tn + 1);
+            const float ar = r * q.x, ai = r * q.y;
             float ur, ui;
             if (MODE == 0) {
               const float w = dtt * xt;
-              ur = w * br;
-              ui = w * bi;
+              ur = w * q.z;
+              ui = w * q.w;
             } else {
-              const float lm = load_in<Tin>(LAM, b * L + t);
-              const float w = lm * dtt * xt, c2 = (1.f - lm) * dtt * xp;
-              ur = w * br + c2 * (ar * bpr - ai * bpi);
-              ui = w * bi + c2 * (ar * bpi + ai * bpr);
-              xp = xt;
-              bpr = br;
-              bpi = bi;
+              const float lm = s_lv[i + 1];
+              const float4 qp = s_tn[i][n];
+              const float w = lm * dtt * xt, c2 = (1.f - lm) * dtt * s_td[i][cb].x;
+              ur = w * q.z + c2 * (ar * qp.z - ai * qp.w);
+              ui = w * q.w + c2 * (ar * qp.w + ai * qp.z);
             }
             const float nr = fmaf(ar, hr, fmaf(-ai, hi, ur));
             const float ni = fmaf(ar, hi, fmaf(ai, hr, ui));
@@ -269,33 +521,26 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
       // ---- backward through the segment
       float g3[3][SEG];   // per t: dx, ddt, dlam partial sums over this lane's state
       // (1 - lam_{t+1}) dt_{t+1}: the next step's beta weight (zero past the end)
-      float mnext = 0.f;
-      if (MODE == 1 && ts + nt < p.L) {
-        const long long t1 = ts + nt;
-        mnext = (1.f - load_in<Tin>(LAM, b * L + t1)) * load_in<Tin>(DT, (b * L + t1) * D + dd);
-      }
+      float mnext = MODE == 1 ? (1.f - s_lv[nt + 1]) * s_td[nt + 1][cb].y : 0.f;
 #pragma unroll
       for (int i = SEG - 1; i >= 0; --i) {
         g3[0][i] = 0.f;
         g3[1][i] = 0.f;
         g3[2][i] = 0.f;
         if (i < nt) {
-          const long long t = ts + i;
-          const long long td = (b * L + t) * D + dd;
-          const long long tn = (b * L + t) * N + n;
-          const float xt = vmask * load_in<Tin>(X, td), dtt = load_in<Tin>(DT, td);
-          const float dyt = vmask * p.dy[td];
-          const float2 ro = p.rot[tn];
+          const float4 v = s_td[i + 1][cb];
+          const float4 q = s_tn[i + 1][n];
+          const float2 cc = s_cc[i + 1][n];
+          const float xt = v.x, dtt = v.y, dyt = v.z;
           const float r = ex2_approx(dtt * a2);
-          const float ar = r * ro.x, ai = r * ro.y;
+          const float ar = r * q.x, ai = r * q.y;
           const float hr = hsr[i], hi = hsi[i];
           const float hpr = i > 0 ? hsr[i > 0 ? i - 1 : 0] : h0r;
           const float hpi = i > 0 ? hsi[i > 0 ? i - 1 : 0] : h0i;
-          const float ccr = load_in<Tin>(CC, 2 * tn), cci = load_in<Tin>(CC, 2 * tn + 1);
-          const float br = load_in<Tin>(BC, 2 * tn), bi = load_in<Tin>(BC, 2 * tn + 1);
+          const float br = q.z, bi = q.w;
           // adjoint of h_t
-          const float gr = fmaf(dyt, ccr, cgr);
-          const float gi = fmaf(-dyt, cci, cgi);
+          const float gr = fmaf(dyt, cc.x, cgr);
+          const float gi = fmaf(-dyt, cc.y, cgi);
           // output: dCc_t += dy conj(h_t)
           acc[i][2] = fmaf(dyt, hr, acc[i][2]);
           acc[i][3] = fmaf(-dyt, hi, acc[i][3]);
@@ -311,22 +556,20 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
             gx = dtt * P;
             gdt = xt * P;
           } else {
-            const float lm = load_in<Tin>(LAM, b * L + t);
+            const float lm = s_lv[i + 1];
             const float coef = lm * dtt * xt;
             const float cn = mnext * xt;   // beta_{t+1} reaches Bc_t through conj(a_{t+1}) ghat_{t+1}
             acc[i][0] += coef * gr + cn * cgr;
             acc[i][1] += coef * gi + cn * cgi;
-            float xp = 0.f;
-            if (t > 0) {
-              const long long tp = tn - N;
-              xp = vmask * load_in<Tin>(X, td - D);
-              const float bpr = load_in<Tin>(BC, 2 * tp), bpi = load_in<Tin>(BC, 2 * tp + 1);
-              const float c2 = (1.f - lm) * dtt * xp;
-              const float vr = ar * bpr - ai * bpi, vi = ar * bpi + ai * bpr;   // a_t Bc_{t-1}
-              R = vr * gr + vi * gi;
-              Gar += c2 * (gr * bpr + gi * bpi);
-              Gai += c2 * (gi * bpr - gr * bpi);
-            }
+            // step t-1 (zeros before the sequence)
+            const float xp = s_td[i][cb].x;
+            const float4 qp = s_tn[i][n];
+            const float bpr = qp.z, bpi = qp.w;
+            const float c2 = (1.f - lm) * dtt * xp;
+            const float vr = ar * bpr - ai * bpi, vi = ar * bpi + ai * bpr;   // a_t Bc_{t-1}
+            R = vr * gr + vi * gi;
+            Gar += c2 * (gr * bpr + gi * bpi);
+            Gai += c2 * (gi * bpr - gr * bpi);
             gx = lm * dtt * P + mnext * Rn;
             gdt = lm * xt * P + (1.f - lm) * xp * R;
             glam = dtt * (xt * P - xp * R);
@@ -405,7 +648,7 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
     __syncthreads();
   }
 
-  // ---- per-(d, n) and per-d sums over this batch row
+  // ---- per-(d, n) and per-d sums over this chunk of this batch row
 #pragma unroll 1
   for (int j = 0; j < K; ++j) {
     const int d = dbase + (j * WARPS + warp) * CPW + cl;

@@ -481,11 +481,23 @@ template <typename Tin, int MODE, int N>
 int launch_backward(const BwdArgs& a, cudaStream_t st) {
   int dev = 0;
   CSSCAN_CUDA(cudaGetDevice(&dev));
+  int nsm = 0;
+  CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
   const int64_t S = (a.L + bwd::SEG - 1) / bwd::SEG;
+  // time chunks, only where the rows leave the GPU short of about two gradient blocks per SM;
+  // then enough chunks for about four per SM (the two chunk passes cost about one forward each)
+  const int64_t row_blocks = a.B * ((a.D + bwd::GradTile<N>::CB - 1) / bwd::GradTile<N>::CB);
+  int64_t C = row_blocks >= 2 * int64_t(nsm)
+                  ? 1
+                  : std::min<int64_t>(S, std::max<int64_t>(1, (4 * int64_t(nsm) + row_blocks - 1) / row_blocks));
+  if (C > 65535) C = 65535;
+  const int64_t TC = (S + C - 1) / C * bwd::SEG;
+  C = (a.L + TC - 1) / TC;
   const size_t rot_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float2), 256);
-  const size_t ckpt_bytes = size_t(a.B * S * a.D * N) * sizeof(float2);
+  const size_t ckpt_bytes = align_up(size_t(a.B * S * a.D * N) * sizeof(float2), 256);
+  const size_t chunk_bytes = C > 1 ? size_t(a.B * C * a.D * N) * 5 * sizeof(float2) : 0;
   WsEntry ws;
-  int rc = get_workspace(dev, st, 1, rot_bytes + ckpt_bytes, &ws);
+  int rc = get_workspace(dev, st, 1, rot_bytes + ckpt_bytes + chunk_bytes, &ws);
   if (rc != CSSCAN_OK) return rc;
   char* rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
 
@@ -516,22 +528,45 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
   p.dD = a.dDskip;
   p.rot = reinterpret_cast<const float2*>(rest);
   p.ckpt = reinterpret_cast<float2*>(rest + rot_bytes);
+  p.chunk = C > 1 ? reinterpret_cast<float2*>(rest + rot_bytes + ckpt_bytes) : nullptr;
   p.B = int(a.B);
   p.L = int(a.L);
   p.D = int(a.D);
   p.N = N;
   p.S = int(S);
+  p.TC = int(TC);
+  p.C = int(C);
 
   const long long n_rot = (long long)a.B * a.L * N;
   bwd::rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest), n_rot);
   CSSCAN_CUDA(cudaGetLastError());
-  if (S > 1) {
-    const long long n_ck = (long long)a.B * a.D * N;
-    bwd::ckpt_kernel<Tin, MODE><<<unsigned((n_ck + 255) / 256), 256, 0, st>>>(p);
+  const long long n_ck = (long long)a.B * C * a.D * N;   // threads of the per-chunk passes
+  const unsigned ck_blocks = unsigned((n_ck + 255) / 256);
+  if (C > 1) {
+    bwd::chunk_fwd_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+    bwd::chunk_adj_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+    const long long n_cb = (long long)a.B * a.D * N;
+    bwd::chunk_combine_kernel<<<unsigned((n_cb + 255) / 256), 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
   }
-  const dim3 grid{unsigned((a.D + bwd::GradTile<N>::CB - 1) / bwd::GradTile<N>::CB), unsigned(a.B)};
-  bwd::grad_kernel<Tin, MODE, N><<<grid, bwd::THREADS, 0, st>>>(p);
+  if (TC > bwd::SEG) {   // some segments start inside a chunk: their checkpoints
+    bwd::ckpt_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+  }
+  const dim3 grid{unsigned((a.D + bwd::GradTile<N>::CB - 1) / bwd::GradTile<N>::CB), unsigned(a.B), unsigned(C)};
+  {
+    static std::mutex mu;
+    static std::map<int, bool> attr_set;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!attr_set[dev]) {
+      CSSCAN_CUDA(cudaFuncSetAttribute(bwd::grad_kernel<Tin, MODE, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       bwd::GradStage<N>::BYTES));
+      attr_set[dev] = true;
+    }
+  }
+  bwd::grad_kernel<Tin, MODE, N><<<grid, bwd::THREADS, bwd::GradStage<N>::BYTES, st>>>(p);
   CSSCAN_CUDA(cudaGetLastError());
   return CSSCAN_OK;
 }
@@ -560,7 +595,7 @@ int backward_impl(const BwdArgs& a, cudaStream_t st) {
   if (rows && a.mode == CSSCAN_MODE_EXP_TRAPEZOID && (!a.lam || !a.dlam)) return CSSCAN_ERR_INVALID_ARG;
   if (a.N != 2 && a.N != 4 && a.N != 8 && a.N != 16 && a.N != 32) return CSSCAN_ERR_UNSUPPORTED;
   if (a.B > 65535 || a.L > (int64_t(1) << 30) || a.D > (int64_t(1) << 30) ||
-      a.B * a.L * a.D > (int64_t(1) << 40))
+      a.B * a.L * a.D > (int64_t(1) << 40) || (a.D + 63) / 64 > 65535)
     return CSSCAN_ERR_UNSUPPORTED;
   const size_t s = a.dtype == CSSCAN_F32 ? 4 : 2;
   if (!aligned(a.x, s) || !aligned(a.delta, s) || !aligned(a.Bc, s) || !aligned(a.Cc, s) || !aligned(a.theta, s) ||

@@ -200,3 +200,12 @@ def test_backward_full_size_batch_workload():
     }
     for k, (a, b) in ident.items():
         assert abs(a - b) <= 1e-4 * s["scale"], f"{k}: {a} vs {b} (scale {s['scale']})"
+
+
+def test_backward_unchunked_row_rich():
+    """Enough (b, d) rows to fill the GPU without time chunks: the single-chunk path."""
+    for mode in (0, 1):
+        w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=16, L=21, D=5000, N=16, mode=mode, dtype="f32")
+        inp = wl.generate(w)
+        dy = make_dy(w, seed=19 + mode)
+        compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"unchunked m{mode}")
