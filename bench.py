@@ -38,6 +38,11 @@ METRIC = "selective-scan Gelem/s (B·L·D·N) and HBM GB/s as % of B300 peak, 1 
 UNIT = "Gelem/s"
 DEFAULT_WORKLOAD = "trap_bf16_batch"
 L2_BYTES = 126 * 1024 * 1024
+# FP32 lane-operations per element of the backward pass (csscan_backward), counted from its
+# kernels: the checkpoint pass (~10 exp-Euler / ~17 trapezoid: decay exponent, rotation,
+# injection, update), the segment recompute (the same again) and the reverse step (~28 /
+# ~45: adjoint, transition gradient, injection gradients, exponential chain rule, carry).
+BWD_ALU_OPS_PER_ELEM = {0: 48, 1: 79}
 # FP32 pipe lane-operations per scanned element in this implementation's formulation: one
 # multiply for the decay exponent, four for the complex decay-and-inject update, two for the
 # real part of C h (plus one MUFU ex2 on its own pipe).
@@ -56,6 +61,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-backward", action="store_true", help="skip the backward-pass measurement")
+    p.add_argument("--backward-steps", type=int, default=5)
     return p.parse_args(argv)
 
 
@@ -360,6 +367,8 @@ def run_ours(args):
     e2e_s = reduce_max(time.perf_counter() - t0)
     e2e_value = aggregate_value(w.elements, e2e_steps, world, e2e_s)
 
+    bwd = None if args.no_backward else measure_backward(w, dev, stream, max(1, args.backward_steps))
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -392,10 +401,52 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
             "gpu_launches": 2 * K, "clocks": clk}
+    if bwd is not None:
+        ms = bwd.pop("ms")
+        alu = BWD_ALU_OPS_PER_ELEM[w.mode] * w.elements / (ms / 1e3) / 1e12
+        gbs = bwd["min_bytes"] / (ms / 1e3) / 1e9
+        bwd.update({"ms_per_step": ms, "value": w.elements / (ms / 1e3) / 1e9, "unit": UNIT,
+                    "alu": {"achieved": alu, "peak": alu_peak, "unit": "Tops/s", "frac": alu / alu_peak,
+                            "ops_per_elem": BWD_ALU_OPS_PER_ELEM[w.mode]},
+                    "hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak}})
+        line["backward"] = bwd
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def backward_min_bytes(w: wl.Workload) -> int:
+    """Minimum HBM bytes of one backward pass: x, dt, dy, Bc, Cc, theta (and lam) read once;
+    dx, ddt (float32) and dBc, dCc, dtheta (and dlam) written once; A, Dskip read and dA,
+    dDskip written once."""
+    s = w.in_bytes
+    per_bt = w.D * (2 * s + 4 + 8) + w.N * (5 * s + 20) + ((s + 4) if w.mode == 1 else 0)
+    return w.B * w.L * per_bt + 2 * (w.D * w.N + w.D) * 4
+
+
+def measure_backward(w: wl.Workload, dev: dict, stream, steps: int) -> dict:
+    """Time csscan_backward on the same inputs (seeded dy ~ N(0, 1) on the device), CUDA
+    events on the launching stream around each call, after two warm-up calls."""
+    import torch
+    from selective_state_space_diagonal_b300 import csscan
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0x5EED0000 + 99)
+    dy = torch.randn((w.B, w.L, w.D), dtype=torch.float32, device="cuda", generator=g)
+    args = (dev["x"], dev["delta"], dev["A"], dev["Bc"], dev["Cc"], dev["theta"], dev["lam"], dev["Dskip"], dy, w.mode)
+    out = csscan.csscan_backward(*args, stream=stream)
+    csscan.csscan_backward(*args, stream=stream, out=out)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        csscan.csscan_backward(*args, stream=stream, out=out)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    del out, dy
+    return {"ms": ms, "steps": steps, "min_bytes": backward_min_bytes(w),
+            "note": "csscan_backward (checkpointed recompute), inputs resident, median of CUDA-event times"}
 
 
 KERNEL_SOURCES = ("selective_state_space_diagonal_b300/csrc/scan_kernels.cuh",

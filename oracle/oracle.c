@@ -28,6 +28,8 @@
  *                                      + lam_t dt_t Bc_t x_t,  Bc_{-1} x_{-1} = 0
  *    (beta_t = (1-lam_t) dt_t exp(dt_t A_t), where the exponential is the full complex
  *     a_t, rotation included, and dt is the current step's).
+ *  - zero-order hold (mode 2): h_t = a_t h_{t-1} + dt_t (e^{z_t} - 1)/z_t Bc_t x_t, z_t the
+ *    exponent of a_t (the rotation included, as for beta_t)
  *  - y[b,t,d] = Re(sum_n Cc[b,t,n] h_t[n]) + Dskip[d] x[b,t,d], from the updated h_t,
  *    with no conjugation.
  *  - the state before t = 0 is zero unless an initial state is passed in.
@@ -60,6 +62,8 @@ static cplx transition(double dt, double A, double theta) { return cexp(dt * A +
  *   mode 0 (exp-Euler, gamma_t = dt_t):  u_t = dt_t x_t Bc_t
  *   mode 1 (exp-trapezoidal): u_t = beta_t Bc_{t-1} x_{t-1} + gamma_t Bc_t x_t with
  *          beta_t = (1 - lam_t) dt_t a_t and gamma_t = lam_t dt_t
+ *   mode 2 (zero-order hold): u_t = gamma_t Bc_t x_t, gamma_t = dt_t (e^{z_t} - 1) / z_t,
+ *          z_t = dt_t A + i theta_t
  * ("Mamba-3 paper story", discretisation table). x_prev and B_prev are step t-1's input;
  * callers pass zero for them at the start of the sequence.
  * out = {Re a, Im a, Re u, Im u}. */
@@ -71,11 +75,20 @@ void oracle_operator(int mode, double dt, double A, double theta, double lam, do
   if (mode == 0) {
     double gamma = dt;
     u = gamma * v;
-  } else {
+  } else if (mode == 1) {
     cplx v_prev = (B_prev[0] + I * B_prev[1]) * x_prev;   /* Bc_{t-1} x_{t-1} */
     cplx beta = (1.0 - lam) * dt * a;
     double gamma = lam * dt;
     u = beta * v_prev + gamma * v;
+  } else {
+    /* mode 2, zero-order hold: gamma = A^{-1}(exp(dt A) - I) ("Mamba-3 paper story",
+     * discretisation table, row ZOH; the same B-bar in "Complex parallel scan", section
+     * 硬件落地的挑战), with the complex exponent z = dt A + i theta in place of dt A as for
+     * alpha_t: gamma = dt (e^z - 1) / z, which tends to dt as z -> 0 */
+    cplx z = dt * A + I * theta;
+    cplx phi = cabs(z) < 1e-6 ? 1.0 + z / 2.0 + z * z / 6.0 : (cexp(z) - 1.0) / z;
+    cplx gamma = dt * phi;
+    u = gamma * v;
   }
   out[0] = creal(a); out[1] = cimag(a); out[2] = creal(u); out[3] = cimag(u);
 }
@@ -161,7 +174,7 @@ int oracle_forward(const double* x, const double* dt, const double* A, const dou
                    const double* x_prev, const double* Bc_prev, double* y, double* h_last, double* h_traj,
                    int64_t B, int64_t L, int64_t D, int64_t N, int mode, int nthreads) {
   if (B < 0 || L < 0 || D < 0 || N < 0) return -1;
-  if (mode != 0 && mode != 1) return -2;
+  if (mode != 0 && mode != 1 && mode != 2) return -2;
   if (mode == 1 && !lam && B * L > 0) return -3;
   if (nthreads <= 0) nthreads = oracle_default_threads();
   if ((int64_t)nthreads > B * D) nthreads = (int)(B * D > 0 ? B * D : 1);

@@ -94,6 +94,15 @@ def _bruteforce_y(c, mode):
                 a = np.exp(dt[b, :, d] * A[d, n] + 1j * th[b, :, n])
                 if mode == 0:
                     u = dt[b, :, d] * x[b, :, d] * Bc[b, :, n]
+                elif mode == 2:
+                    # (e^z - 1)/z by its power series sum_k z^k / (k+1)!
+                    z = dt[b, :, d] * A[d, n] + 1j * th[b, :, n]
+                    phi = np.zeros_like(z)
+                    term = np.ones_like(z)
+                    for k in range(40):
+                        phi = phi + term
+                        term = term * z / (k + 2)
+                    u = dt[b, :, d] * phi * x[b, :, d] * Bc[b, :, n]
                 else:
                     u = lam[b] * dt[b, :, d] * x[b, :, d] * Bc[b, :, n]
                     u[1:] += (1 - lam[b, 1:]) * dt[b, 1:, d] * a[1:] * x[b, :-1, d] * Bc[b, :-1, n]
@@ -108,9 +117,9 @@ def _bruteforce_y(c, mode):
 
 
 def pin_bruteforce(lib):
-    """The recurrence against the unrolled double sum on tiny inputs, both modes."""
+    """The recurrence against the unrolled double sum on tiny inputs, all three modes."""
     rng = np.random.default_rng(13)
-    for mode in (0, 1):
+    for mode in (0, 1, 2):
         c = random_case(rng, 2, 10, 3, 4, mode)
         y = run(lib, c, mode)
         assert rel_err(y, _bruteforce_y(c, mode)) <= 1e-12
@@ -288,6 +297,72 @@ def pin_golden(lib):
         assert np.max(np.abs(y - y_expect)) <= 1e-12, (name, y, y_expect)
 
 
+# ---------------------------------------------------------------------------- zero-order hold
+def pin_zoh_exact_hold(lib):
+    """Mode 2 is the exact solution of the continuous system with the input held over each
+    step (what zero-order hold means: "Mamba-3 paper story", discretisation table, row ZOH):
+    on step t, h' = lambda_t h + Bc_t x_t with lambda_t = A + i theta_t / dt_t for a time dt_t,
+    so that the state is multiplied by exp(dt_t A + i theta_t) over the step. Integrated here
+    with classical Runge-Kutta (RK4, 400 substeps per step), independent of the oracle's
+    closed form; y is read after every step."""
+    rng = np.random.default_rng(31)
+    c = random_case(rng, 1, 12, 2, 3, 2, dt_range=(0.05, 0.8), theta_max=1.5)
+    y = run(lib, c, 2)
+    B, L, D = c["x"].shape
+    N = c["A"].shape[1]
+    y_ode = np.zeros((B, L, D))
+    for d in range(D):
+        h = np.zeros(N, dtype=np.complex128)
+        for t in range(L):
+            dt = c["delta"][0, t, d]
+            lam_c = c["A"][d] + 1j * c["theta"][0, t] / dt
+            f = c["Bc"][0, t] * c["x"][0, t, d]
+            m = 400
+            hs = dt / m
+            for _ in range(m):
+                k1 = lam_c * h + f
+                k2 = lam_c * (h + 0.5 * hs * k1) + f
+                k3 = lam_c * (h + 0.5 * hs * k2) + f
+                k4 = lam_c * (h + hs * k3) + f
+                h = h + hs / 6.0 * (k1 + 2 * k2 + 2 * k3 + k4)
+            y_ode[0, t, d] = float(np.sum((c["Cc"][0, t] * h).real)) + c["Dskip"][d] * c["x"][0, t, d]
+    assert rel_err(y, y_ode) <= 1e-9, rel_err(y, y_ode)
+
+
+def pin_zoh_real_reduction(lib):
+    """theta = 0 with real Bc, Cc: mode 2 is the real ZOH scan h = e^{dt A} h + expm1(dt A)/A Bc x,
+    written separately here with expm1."""
+    rng = np.random.default_rng(37)
+    c = random_case(rng, 2, 30, 3, 4, 2)
+    c["theta"] = np.zeros_like(c["theta"])
+    c["Bc"] = c["Bc"].real.astype(np.complex128)
+    c["Cc"] = c["Cc"].real.astype(np.complex128)
+    y = run(lib, c, 2)
+    B, L, D = c["x"].shape
+    ref = np.zeros((B, L, D))
+    for b in range(B):
+        for d in range(D):
+            h = np.zeros(c["A"].shape[1])
+            for t in range(L):
+                zt = c["delta"][b, t, d] * c["A"][d]
+                h = np.exp(zt) * h + np.expm1(zt) / c["A"][d] * c["Bc"][b, t].real * c["x"][b, t, d]
+                ref[b, t, d] = float(np.sum(c["Cc"][b, t].real * h)) + c["Dskip"][d] * c["x"][b, t, d]
+    assert rel_err(y, ref) <= 1e-12
+
+
+def pin_zoh_small_step_limit(lib):
+    """As dt A and theta go to zero, gamma = dt (e^z - 1)/z -> dt: mode 2 approaches exp-Euler,
+    with a relative difference of the order of |z|."""
+    rng = np.random.default_rng(41)
+    c = random_case(rng, 1, 50, 2, 3, 2, dt_range=(1e-7, 2e-7), theta_max=1e-7)
+    y0 = run(lib, c, 0)
+    y2 = run(lib, c, 2)
+    ssm0 = y0 - c["Dskip"][None, None, :] * c["x"]
+    ssm2 = y2 - c["Dskip"][None, None, :] * c["x"]
+    e = rel_err(ssm2, ssm0)
+    assert 0 < e <= 1e-5, e
+
+
 # ---------------------------------------------------------------------------- backward
 GRAD_OF = {"x": "dx", "delta": "ddelta", "A": "dA", "Bc": "dBc", "Cc": "dCc", "theta": "dtheta",
            "lam": "dlam", "Dskip": "dDskip"}
@@ -371,4 +446,5 @@ def pin_backward_identities(lib):
 
 ALL_PINS = [pin_combine_associative, pin_combine_is_composition, pin_bruteforce, pin_closed_form,
             pin_real_reduction, pin_rotation, pin_lambda_one, pin_linearity_and_causality,
-            pin_split_invariance, pin_golden, pin_backward_finite_differences, pin_backward_identities]
+            pin_split_invariance, pin_golden, pin_zoh_exact_hold, pin_zoh_real_reduction, pin_zoh_small_step_limit,
+            pin_backward_finite_differences, pin_backward_identities]

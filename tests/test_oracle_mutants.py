@@ -50,6 +50,11 @@ MUTANTS = [
     ("initial state ignored", "h[n] = j->h0 ? load_c(j->h0, (b * D + d) * N + n) : 0.0;", "h[n] = 0.0;"),
     ("halo x ignored", "else if (j->x_prev) x_prev = j->x_prev[b * D + d];", "else if (j->x_prev) x_prev = 0.0;"),
     ("apply drops the multiplier", "cplx r = a * hh + u;", "cplx r = hh + u;"),
+    # zero-order hold
+    ("zoh exponent without the rotation", "cplx z = dt * A + I * theta;", "cplx z = dt * A;"),
+    ("zoh gamma without the division", "(cexp(z) - 1.0) / z;", "(cexp(z) - 1.0);"),
+    ("zoh gamma without dt", "cplx gamma = dt * phi;", "cplx gamma = phi;"),
+    ("zoh gamma conjugated", "cplx gamma = dt * phi;", "cplx gamma = dt * conj(phi);"),
     # backward
     ("adjoint carried by a instead of conj(a)", "carry[n] = conj(a) * ghat;", "carry[n] = a * ghat;"),
     ("adjoint reads C unconjugated", "const cplx ghat = dyt * conj(load_c(j->Cc, tn)) + carry[n];",
