@@ -43,6 +43,12 @@ L2_BYTES = 126 * 1024 * 1024
 # injection, update), the segment recompute (the same again) and the reverse step (~28 /
 # ~45: adjoint, transition gradient, injection gradients, exponential chain rule, carry).
 BWD_ALU_OPS_PER_ELEM = {0: 48, 1: 79}
+# FP32 lane-operations per element of the zero-order-hold scan (zoh_kernels.cuh), counted
+# from its source: decay exponent 1, expm1 about 8, transition 3, e^z - 1 and |z|^2 4,
+# (e^z - 1)/z 6, gamma x 3, complex injection 4, update 4, Re(Cc h) 2, plus one MUFU
+# reciprocal; the time-chunk pass adds the update and the chunk product again when the
+# rows alone do not fill the GPU.
+ZOH_ALU_OPS_PER_ELEM = 35
 # FP32 pipe lane-operations per scanned element in this implementation's formulation: one
 # multiply for the decay exponent, four for the complex decay-and-inject update, two for the
 # real part of C h (plus one MUFU ex2 on its own pipe).
@@ -256,9 +262,20 @@ def run_reference(args):
     return 0
 
 
+def launches_per_step(w: wl.Workload) -> int:
+    """Kernels one forward call enqueues: the rotation table and the scan; in the zero-order-hold
+    mode the table, the output pass and, when the rows alone leave under 8192 threads per SM
+    (the library's rule), the time-chunk pass and the chunk sweep."""
+    if w.mode != wl.MODE_ZOH:
+        return 2
+    import torch
+    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return 2 if w.B * w.D * w.N >= nsm * 8192 else 4
+
+
 def workload_config(w: wl.Workload, l2_note: str = ""):
     cfg = {"workload": w.name, "B": w.B, "L": w.L, "D": w.D, "N": w.N,
-           "mode": "exp-trapezoidal" if w.mode == 1 else "exp-Euler", "input_dtype": w.dtype,
+           "mode": {0: "exp-Euler", 1: "exp-trapezoidal", 2: "zero-order hold"}[w.mode], "input_dtype": w.dtype,
            "elements": w.elements, "min_bytes": w.min_bytes()}
     if l2_note:
         cfg["l2"] = l2_note
@@ -367,7 +384,8 @@ def run_ours(args):
     e2e_s = reduce_max(time.perf_counter() - t0)
     e2e_value = aggregate_value(w.elements, e2e_steps, world, e2e_s)
 
-    bwd = None if args.no_backward else measure_backward(w, dev, stream, max(1, args.backward_steps))
+    bwd = None if (args.no_backward or w.mode == wl.MODE_ZOH) else measure_backward(w, dev, stream,
+                                                                                   max(1, args.backward_steps))
 
     if rank != 0:
         if world > 1:
@@ -378,14 +396,16 @@ def run_ours(args):
     scan_mean_s = statistics.mean(scan_ms) / 1e3
     clk = clocks.summary()
     alu_peak = FP32_LANES_PER_SM * N_SM * sm_max_mhz * 1e6 / 1e12           # T lane-ops/s
-    alu_achieved = ALU_OPS_PER_ELEM * w.elements / scan_mean_s / 1e12
+    ops_per_elem = ZOH_ALU_OPS_PER_ELEM if w.mode == wl.MODE_ZOH else ALU_OPS_PER_ELEM
+    alu_achieved = ops_per_elem * w.elements / scan_mean_s / 1e12
     hbm_achieved = w.min_bytes() / scan_mean_s / 1e9
     traffic = traffic_from_profiles(w.name)
     roofline = {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak, "unit": "Tops/s",
                 "frac": alu_achieved / alu_peak, "traffic": traffic,
-                "kernel": "scan_kernel", "ms_per_launch": 1e3 * scan_mean_s,
+                "kernel": "zoh_out_kernel (+ chunk passes)" if w.mode == wl.MODE_ZOH else "scan_kernel",
+                "ms_per_launch": 1e3 * scan_mean_s,
                 "peak_note": f"FP32 pipe: {FP32_LANES_PER_SM} lanes/SM x {N_SM} SMs x {sm_max_mhz:.0f} MHz; "
-                             f"{ALU_OPS_PER_ELEM} lane-ops per element"}
+                             f"{ops_per_elem} lane-ops per element"}
     hbm = {"achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s", "frac": hbm_achieved / hbm_peak,
            "peak_kind": peak_kind, "whole_step_gbs": w.min_bytes() * K / (elapsed_ms / 1e3) / 1e9}
 
@@ -400,7 +420,7 @@ def run_ours(args):
             "roofline": roofline, "hbm": hbm, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
-            "gpu_launches": 2 * K, "clocks": clk}
+            "gpu_launches": launches_per_step(w) * K, "clocks": clk}
     if bwd is not None:
         ms = bwd.pop("ms")
         alu = BWD_ALU_OPS_PER_ELEM[w.mode] * w.elements / (ms / 1e3) / 1e12

@@ -8,6 +8,8 @@
  *   exp-Euler         h_t = a_t h_{t-1} + dt_t Bc[b,t,n] x[b,t,d]
  *   exp-trapezoidal   h_t = a_t h_{t-1} + (1 - lam_t) dt_t a_t Bc[b,t-1,n] x[b,t-1,d]
  *                                       + lam_t dt_t Bc[b,t,n] x[b,t,d],  with Bc_{-1} x_{-1} = 0
+ *   zero-order hold   h_t = a_t h_{t-1} + dt_t (a_t - 1) / z_t Bc[b,t,n] x[b,t,d],
+ *                     z_t = dt_t A[d,n] + i theta[b,t,n]  (a_t = e^{z_t})
  *   y[b,t,d] = Re(sum_n Cc[b,t,n] h_t[n]) + Dskip[d] x[b,t,d]
  *
  * Sources (pages of the reference material, by title and section):
@@ -76,7 +78,14 @@ enum {
                                       its fixed CSSCAN_NOALLOC_SCRATCH_BYTES array holds */
 };
 
-typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1 } csscan_mode_t;
+/* Discretisation of the injection ("Mamba-3 paper story", discretisation table):
+ *   EXP_EULER     gamma_t = dt_t
+ *   EXP_TRAPEZOID beta_t = (1 - lam_t) dt_t a_t on Bc_{t-1} x_{t-1}, gamma_t = lam_t dt_t
+ *   ZOH           gamma_t = dt_t (e^{z_t} - 1) / z_t with z_t = dt_t A + i theta_t (the table's
+ *                 A^{-1}(exp(dt A) - I) with the complex exponent of a_t in place of dt A);
+ *                 csscan_forward and csscan_forward_ex only (without initial state or halo),
+ *                 N <= 32; the other entry points return CSSCAN_ERR_UNSUPPORTED for it */
+typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1, CSSCAN_MODE_ZOH = 2 } csscan_mode_t;
 typedef enum { CSSCAN_F32 = 0, CSSCAN_BF16 = 1 } csscan_dtype_t;
 
 /*

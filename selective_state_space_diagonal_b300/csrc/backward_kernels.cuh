@@ -312,38 +312,6 @@ __global__ void __launch_bounds__(256) ckpt_kernel(const Params p) {
   }
 }
 
-// Reduce-scatter of V[SEG] over the N lanes of a channel group (lane bits below N): rounds
-// with the high masks halve the array (each lane keeps one half and adds its partner's copy of
-// it), rounds with the remaining masks add whole values. Afterwards a lane holds the group sum
-// for t offsets base .. base + HOLD - 1.
-template <int N, int NARR>
-__device__ __forceinline__ int butterfly(float (&v)[NARR][SEG], int lane) {
-  int base = 0;
-  int len = SEG;
-#pragma unroll
-  for (int m = N / 2; m >= 1; m >>= 1) {
-    const bool upper = (lane & m) != 0;
-    if (len > 1) {
-      const int half = len / 2;
-#pragma unroll
-      for (int k = 0; k < NARR; ++k)
-#pragma unroll
-        for (int i = 0; i < SEG / 2; ++i)
-          if (i < half) {
-            const float send = upper ? v[k][i] : v[k][i + half];
-            const float keep = upper ? v[k][i + half] : v[k][i];
-            v[k][i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-          }
-      if (upper) base += half;
-      len = half;
-    } else {
-#pragma unroll
-      for (int k = 0; k < NARR; ++k) v[k][0] += __shfl_xor_sync(0xffffffffu, v[k][0], m);
-    }
-  }
-  return base;
-}
-
 // Dynamic shared memory of grad_kernel: one segment's inputs, staged once per block.
 // Rows r = 0 .. SEG + 1 stand for steps t = ts - 1 + r (zeros outside 0 .. L-1 and past D).
 template <int N> struct GradStage {
@@ -598,7 +566,7 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
       s_dD[j][tid] = dD_acc;
 
       // ---- sums over n: dx and ddt of (t, d) are final; dlam goes on to the sum over d
-      hold_base = butterfly<N, 3>(g3, n);
+      hold_base = butterfly<N, 3, SEG>(g3, n);
       const bool owner = (n % DUP) == 0;
 #pragma unroll
       for (int h = 0; h < HOLD; ++h) {

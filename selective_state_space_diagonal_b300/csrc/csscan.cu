@@ -1,8 +1,8 @@
 // csscan.cu -- host side of the C ABI declared in include/csscan.h: argument checks,
 // launch planning (block width, sequence chunks, shared-memory ring), the per-(device,
 // stream) workspace, tile-copy descriptors, and the launches of the rotation-table kernel
-// and the scan kernel (scan_kernels.cuh), the decode step (decode_kernel.cuh) and the
-// backward pass (backward_kernels.cuh).
+// and the scan kernel (scan_kernels.cuh), the zero-order-hold scan (zoh_kernels.cuh), the
+// decode step (decode_kernel.cuh) and the backward pass (backward_kernels.cuh).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -17,6 +17,7 @@
 #include "backward_kernels.cuh"
 #include "decode_kernel.cuh"
 #include "scan_kernels.cuh"
+#include "zoh_kernels.cuh"
 
 using namespace csscan;
 
@@ -397,8 +398,87 @@ csscan_options_t default_options() {
   return o;
 }
 
+// ----------------------------------------------------------------------------- zero-order hold
+template <typename Tin, int N>
+int launch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
+  int dev = 0, nsm = 0;
+  CSSCAN_CUDA(cudaGetDevice(&dev));
+  CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+  // time chunks until there are about 8192 threads per SM (the recurrence is sequential per thread)
+  const int64_t G = zoh::GROUP;
+  const int64_t S = (a.L + G - 1) / G;
+  const int64_t rows = a.B * a.D * N;
+  const int64_t target = int64_t(nsm) * 8192;
+  int64_t C = std::min<int64_t>(S, std::max<int64_t>(1, (target + rows - 1) / rows));
+  const int64_t TC = (S + C - 1) / C * G;
+  C = (a.L + TC - 1) / TC;
+  const size_t tab_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float4), 256);
+  const size_t chunk_bytes = C > 1 ? size_t(a.B * C * a.D * N) * 2 * sizeof(float2) : 0;
+  WsEntry ws;
+  int rc = get_workspace(dev, st, 1, tab_bytes + chunk_bytes, &ws);
+  if (rc != CSSCAN_OK) return rc;
+  char* rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
+  zoh::Params p;
+  p.x = a.x;
+  p.dt = a.delta;
+  p.Bc = a.Bc;
+  p.Cc = a.Cc;
+  p.A = a.A;
+  p.Dskip = a.Dskip;
+  p.y = a.y;
+  p.tab = reinterpret_cast<const float4*>(rest);
+  p.chunk = C > 1 ? reinterpret_cast<float2*>(rest + tab_bytes) : nullptr;
+  p.B = int(a.B);
+  p.L = int(a.L);
+  p.D = int(a.D);
+  p.N = N;
+  p.TC = int(TC);
+  p.C = int(C);
+  const long long n_tab = (long long)a.B * a.L * N;
+  zoh::zoh_table_kernel<Tin><<<unsigned((n_tab + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float4*>(rest),
+                                                                            n_tab);
+  CSSCAN_CUDA(cudaGetLastError());
+  if (o.scan_begin) CSSCAN_CUDA(cudaEventRecord(o.scan_begin, st));
+  const long long n_thr = (long long)a.B * C * a.D * N;
+  if (C > 1) {
+    zoh::zoh_chunk_kernel<Tin><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+    zoh::zoh_combine_kernel<<<unsigned((rows + 255) / 256), 256, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+  }
+  zoh::zoh_out_kernel<Tin, N><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
+  CSSCAN_CUDA(cudaGetLastError());
+  if (o.scan_end) CSSCAN_CUDA(cudaEventRecord(o.scan_end, st));
+  return CSSCAN_OK;
+}
+
+template <typename Tin>
+int dispatch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
+  switch (a.N) {
+    case 2: return launch_zoh<Tin, 2>(a, o, st);
+    case 4: return launch_zoh<Tin, 4>(a, o, st);
+    case 8: return launch_zoh<Tin, 8>(a, o, st);
+    case 16: return launch_zoh<Tin, 16>(a, o, st);
+    case 32: return launch_zoh<Tin, 32>(a, o, st);
+    default: return CSSCAN_ERR_UNSUPPORTED;
+  }
+}
+
 int forward_impl(const Args& a, const csscan_options_t* opts, cudaStream_t st) {
   csscan_options_t o = opts ? *opts : default_options();
+  if (a.mode == CSSCAN_MODE_ZOH) {
+    // the zero-order-hold scan starts from the zero state and has no chunk options
+    if (a.h0 || a.h_last || a.x_prev || a.Bc_prev) return CSSCAN_ERR_UNSUPPORTED;
+    Args a0 = a;
+    a0.mode = CSSCAN_MODE_EXP_EULER;   // same pointer, size and alignment rules
+    int rc = validate(a0, o);
+    if (rc != CSSCAN_OK) return rc;
+    if (a.N > 32) return CSSCAN_ERR_UNSUPPORTED;
+    const size_t pair = a.dtype == CSSCAN_F32 ? 8 : 4;   // Bc, Cc are read one complex entry at a time
+    if (!aligned(a.Bc, pair) || !aligned(a.Cc, pair)) return CSSCAN_ERR_MISALIGNED;
+    if (a.B == 0 || a.L == 0 || a.D == 0) return CSSCAN_OK;
+    return a.dtype == CSSCAN_F32 ? dispatch_zoh<float>(a, o, st) : dispatch_zoh<uint16_t>(a, o, st);
+  }
   int rc = validate(a, o);
   if (rc != CSSCAN_OK) return rc;
   if (a.B == 0 || a.L == 0 || a.D == 0) return CSSCAN_OK;
@@ -433,6 +513,7 @@ int dispatch_decode(const DecodeParams& dp, cudaStream_t st) {
 int decode_impl(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc, const void* theta,
                 const void* lambda, const float* Dskip, float* y, float* h, const void* x_prev, const void* Bc_prev,
                 int64_t B, int64_t D, int64_t N, int mode, int dtype, cudaStream_t stream) {
+  if (mode == CSSCAN_MODE_ZOH) return CSSCAN_ERR_UNSUPPORTED;
   if (mode != CSSCAN_MODE_EXP_EULER && mode != CSSCAN_MODE_EXP_TRAPEZOID) return CSSCAN_ERR_INVALID_ARG;
   if (dtype != CSSCAN_F32 && dtype != CSSCAN_BF16) return CSSCAN_ERR_INVALID_ARG;
   if (B < 0 || D < 0 || N <= 0) return CSSCAN_ERR_INVALID_ARG;
@@ -584,6 +665,7 @@ int dispatch_backward(const BwdArgs& a, cudaStream_t st) {
 }
 
 int backward_impl(const BwdArgs& a, cudaStream_t st) {
+  if (a.mode == CSSCAN_MODE_ZOH) return CSSCAN_ERR_UNSUPPORTED;
   if (a.mode != CSSCAN_MODE_EXP_EULER && a.mode != CSSCAN_MODE_EXP_TRAPEZOID) return CSSCAN_ERR_INVALID_ARG;
   if (a.dtype != CSSCAN_F32 && a.dtype != CSSCAN_BF16) return CSSCAN_ERR_INVALID_ARG;
   if (a.B < 0 || a.L < 0 || a.D < 0 || a.N <= 0) return CSSCAN_ERR_INVALID_ARG;
@@ -734,6 +816,7 @@ int csscan_decode_step(const void* x, const void* delta, const float* A, const v
 int csscan_forward_noalloc(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
                            const void* theta, const void* lambda, const float* Dskip, float* y, int64_t B, int64_t L,
                            int64_t D, int64_t N, int mode, int dtype, uint32_t* device_status, cudaStream_t stream) {
+  if (mode == CSSCAN_MODE_ZOH) return CSSCAN_ERR_UNSUPPORTED;
   Args a{x, delta, Bc, Cc, theta, lambda, A, Dskip, y, nullptr, nullptr, nullptr, nullptr, B, L, D, N, mode, dtype};
   const csscan_options_t o = default_options();
   int rc = validate(a, o);
@@ -781,7 +864,9 @@ const char* csscan_status_string(int status) {
     case CSSCAN_OK: return "ok";
     case CSSCAN_ERR_INVALID_ARG: return "invalid argument";
     case CSSCAN_ERR_MISALIGNED: return "misaligned pointer or row stride (x/delta need 16-byte alignment and D*sizeof(dtype) % 16 == 0)";
-    case CSSCAN_ERR_UNSUPPORTED: return "unsupported size (N must be 2, 4, 8, 16, 32 or 64)";
+    case CSSCAN_ERR_UNSUPPORTED:
+      return "unsupported size or mode for this entry point (N in {2, 4, 8, 16, 32, 64}; N <= 32 for the backward and "
+             "the zero-order-hold mode, which only csscan_forward / csscan_forward_ex take)";
     case CSSCAN_ERR_CUDA: return g_last_cuda_error[0] ? g_last_cuda_error : "CUDA error";
     case CSSCAN_ERR_LOOKBACK_TIMEOUT: return "a chunk's carry wait timed out on the device";
     case CSSCAN_ERR_PIPELINE_TIMEOUT: return "a tile copy did not arrive within its limit on the device";

@@ -31,10 +31,55 @@ template <> __device__ __forceinline__ float load_in<float>(const float* p, int6
 template <> __device__ __forceinline__ float load_in<uint16_t>(const uint16_t* p, int64_t i) {
   return bf16_bits_to_float(p[i]);
 }
+// The two values at p[2 i], p[2 i + 1] (a complex entry), with one load (needs 2 * sizeof(Tin)
+// alignment).
+template <typename Tin> __device__ __forceinline__ float2 load_pair(const Tin* p, int64_t i);
+template <> __device__ __forceinline__ float2 load_pair<float>(const float* p, int64_t i) {
+  return reinterpret_cast<const float2*>(p)[i];
+}
+template <> __device__ __forceinline__ float2 load_pair<uint16_t>(const uint16_t* p, int64_t i) {
+  const uint32_t v = reinterpret_cast<const uint32_t*>(p)[i];
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+}
 template <typename Tin> __device__ __forceinline__ float smem_in(const Tin* p, int i);
 template <> __device__ __forceinline__ float smem_in<float>(const float* p, int i) { return p[i]; }
 template <> __device__ __forceinline__ float smem_in<uint16_t>(const uint16_t* p, int i) {
   return bf16_bits_to_float(p[i]);
+}
+
+// ---------------------------------------------------------------------------- lane sums
+// Reduce-scatter of NARR arrays v[k][0 .. LEN-1] over the N lanes of a lane group (lane bits
+// below N; N and LEN powers of two): rounds with the high masks halve the arrays (each lane
+// keeps one half and adds its partner's copy of it), rounds with the remaining masks add whole
+// values. Afterwards a lane holds the group sums for entries base .. base + max(1, LEN/N) - 1 in
+// v[k][0 ..]; lanes that differ only in bits below max(1, N/LEN) hold the same entries.
+// Returns base. `lane` is the lane's index within its group.
+template <int N, int NARR, int LEN>
+__device__ __forceinline__ int butterfly(float (&v)[NARR][LEN], int lane) {
+  int base = 0;
+  int len = LEN;
+#pragma unroll
+  for (int m = N / 2; m >= 1; m >>= 1) {
+    const bool upper = (lane & m) != 0;
+    if (len > 1) {
+      const int half = len / 2;
+#pragma unroll
+      for (int k = 0; k < NARR; ++k)
+#pragma unroll
+        for (int i = 0; i < LEN / 2; ++i)
+          if (i < half) {
+            const float send = upper ? v[k][i] : v[k][i + half];
+            const float keep = upper ? v[k][i + half] : v[k][i];
+            v[k][i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+          }
+      if (upper) base += half;
+      len = half;
+    } else {
+#pragma unroll
+      for (int k = 0; k < NARR; ++k) v[k][0] += __shfl_xor_sync(0xffffffffu, v[k][0], m);
+    }
+  }
+  return base;
 }
 
 // ---------------------------------------------------------------------------- flags

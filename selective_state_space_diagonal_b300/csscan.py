@@ -27,6 +27,7 @@ CSSCAN_ERR_SCRATCH_LIMIT = 7
 
 CSSCAN_MODE_EXP_EULER = 0
 CSSCAN_MODE_EXP_TRAPEZOID = 1
+CSSCAN_MODE_ZOH = 2
 CSSCAN_F32 = 0
 CSSCAN_BF16 = 1
 

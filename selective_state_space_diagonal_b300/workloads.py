@@ -39,6 +39,7 @@ TID = {"x": 1, "delta": 2, "A": 3, "Bc": 4, "Cc": 5, "theta": 6, "lam": 7, "Dski
 
 MODE_EXP_EULER = 0
 MODE_EXP_TRAPEZOID = 1
+MODE_ZOH = 2
 
 
 @dataclasses.dataclass(frozen=True)
@@ -49,7 +50,7 @@ class Workload:
     L: int
     D: int
     N: int
-    mode: int            # 0 exp-Euler, 1 exp-trapezoid
+    mode: int            # 0 exp-Euler, 1 exp-trapezoid, 2 zero-order hold
     dtype: str           # "f32" or "bf16"
     dt_lo: float
     dt_hi: float
@@ -91,6 +92,9 @@ WORKLOADS: Dict[str, Workload] = {
                                 "neg_n1_over16", math.pi / 8, 0x5EED0003),
     "trap_bf16_batch": Workload("trap_bf16_batch", 16, 8192, 2560, 16, 1, "bf16", 1e-3, 1e-1,
                                 "neg_exp_u_ln16", math.pi, 0x5EED0004),
+    # the large-batch shape and distributions with the zero-order-hold injection
+    "zoh_bf16_batch": Workload("zoh_bf16_batch", 16, 8192, 2560, 16, 2, "bf16", 1e-3, 1e-1,
+                               "neg_exp_u_ln16", math.pi, 0x5EED0005),
 }
 
 

@@ -113,7 +113,7 @@ def test_backward_matches_oracle(mode, dtype, N):
     compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"m{mode}-{dtype}-N{N}")
 
 
-@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+@pytest.mark.parametrize("name", [k for k, v in wl.WORKLOADS.items() if v.mode != wl.MODE_ZOH])
 def test_backward_workload_shapes(name):
     """Each benchmark workload's distributions, modes and N at a reduced size."""
     w0 = wl.WORKLOADS[name]

@@ -167,7 +167,56 @@ def test_lookback_timeout_is_reported(carry):
     check(inp, y, f"after-timeout:carry{carry}")
 
 
-FULL = ["euler_f32_mamba1", "trap_bf16_mamba3", "euler_bf16_long", "trap_bf16_batch"]
+# ---------------------------------------------------------------------------- zero-order hold
+@pytest.mark.parametrize("N", [2, 4, 8, 16, 32])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zoh_shapes(N, dtype):
+    """Mode 2 (its own kernels: time chunks, then the recurrence with y) on ragged shapes."""
+    base = wl.WORKLOADS["zoh_bf16_batch"]
+    for (B, L, D) in [(1, 1, 8), (2, 13, 8), (1, 95, 24), (2, 300, 72)]:
+        w = base.with_shape(B=B, L=L, D=D, N=N, dtype=dtype, seed=base.seed + 13 * N + L)
+        inp = wl.generate(w)
+        y = gu.run_gpu(gu.to_device(inp), w.mode)
+        check(inp, y, f"zoh:N{N}:{dtype}:{B}x{L}x{D}")
+
+
+def test_zoh_one_chunk_and_small_exponents():
+    # enough rows that the scan runs as a single time chunk
+    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=16, L=24, D=2560, N=32, dtype="f32")
+    inp = wl.generate(w)
+    check(inp, gu.run_gpu(gu.to_device(inp), w.mode), "zoh:one-chunk", b_rows=[0, 15],
+          d_rows=np.array([0, 5, 1000, 2559]))
+    # |z| = |dt A + i theta| around 1e-6 and below: the series branch of (e^z - 1)/z. The
+    # state-space part is then ~1e-5 of the D-skip term, which float32 y could not resolve,
+    # so Dskip = 0 here
+    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=2, L=200, D=16, dtype="f32", dt_lo=1e-8, dt_hi=1e-6,
+                                                  theta_max=1e-6)
+    inp = wl.generate(w)
+    inp.Dskip[:] = 0.0
+    check(inp, gu.run_gpu(gu.to_device(inp), w.mode), "zoh:small-z")
+
+
+def test_zoh_rejected_where_unsupported():
+    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=1, L=16, D=16, N=16, dtype="f32")
+    dev = gu.to_device(wl.generate(w))
+    y = torch.empty((1, 16, 16), device="cuda")
+    args = (dev["x"], dev["delta"], dev["A"], dev["Bc"], dev["Cc"], dev["theta"], None, dev["Dskip"])
+    h = torch.zeros((1, 16, 16, 2), device="cuda")
+    with pytest.raises(csscan.CsscanError) as e:
+        csscan.csscan_forward_state(*args, y, 2, h0=h)
+    assert e.value.status == csscan.CSSCAN_ERR_UNSUPPORTED
+    with pytest.raises(csscan.CsscanError) as e:
+        csscan.csscan_backward(*args, torch.zeros_like(y), 2)
+    assert e.value.status == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert csscan.csscan_forward_noalloc(*args, y, 2) == csscan.CSSCAN_ERR_UNSUPPORTED
+    w64 = w.with_shape(N=64)
+    dev64 = gu.to_device(wl.generate(w64))
+    rc = csscan.csscan_forward_ex(dev64["x"], dev64["delta"], dev64["A"], dev64["Bc"], dev64["Cc"], dev64["theta"],
+                                  None, dev64["Dskip"], y, 2)
+    assert rc == csscan.CSSCAN_ERR_UNSUPPORTED
+
+
+FULL = ["euler_f32_mamba1", "trap_bf16_mamba3", "euler_bf16_long", "trap_bf16_batch", "zoh_bf16_batch"]
 
 
 @pytest.mark.parametrize("name", FULL)
