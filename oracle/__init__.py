@@ -66,6 +66,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.oracle_forward.restype = ctypes.c_int
     lib.oracle_backward.argtypes = [dp] * 17 + [i64] * 4 + [ctypes.c_int, ctypes.c_int]
     lib.oracle_backward.restype = ctypes.c_int
+    lib.oracle_forward_mimo.argtypes = [dp] * 9 + [i64] * 5 + [ctypes.c_int, ctypes.c_int]
+    lib.oracle_forward_mimo.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ctypes.c_int
     _lib_cache[path] = lib
@@ -161,6 +163,29 @@ def backward(x, delta, A, Bc, Cc, theta, lam, Dskip, dy, mode: int, *, nthreads:
     if rc <= 0:
         raise RuntimeError(f"oracle_backward failed with code {rc}")
     return out
+
+
+def forward_mimo(x, delta, A, Bm, Cm, theta, lam, Dskip, mode: int, *, nthreads: int = 0, lib=None) -> np.ndarray:
+    """MIMO scan (P channels of a head share one state): x (B,L,H,P), delta (B,L,H), A (H,N),
+    Bm, Cm (B,L,N,P) complex, theta (B,L,N), lam (B,L) or None, Dskip (H,P); returns y
+    (B,L,H,P) float64."""
+    lib = lib or load()
+    x = _f64(x)
+    Bsz, L, H, P = x.shape
+    N = np.asarray(A).shape[1]
+    delta = _f64(delta, (Bsz, L, H))
+    A = _f64(A, (H, N))
+    Bm = _f64(np.asarray(Bm, dtype=np.complex128), (Bsz, L, N, P))
+    Cm = _f64(np.asarray(Cm, dtype=np.complex128), (Bsz, L, N, P))
+    theta = _f64(theta, (Bsz, L, N))
+    lam = _f64(lam, (Bsz, L)) if lam is not None else None
+    Dskip = _f64(Dskip, (H, P))
+    y = np.zeros((Bsz, L, H, P))
+    rc = lib.oracle_forward_mimo(_ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(theta), _ptr(lam),
+                                 _ptr(Dskip), _ptr(y), Bsz, L, H, P, N, int(mode), int(nthreads))
+    if rc <= 0:
+        raise RuntimeError(f"oracle_forward_mimo failed with code {rc}")
+    return y
 
 
 def last_thread_count(nthreads: int = 0, rows: int = 1 << 30, lib=None) -> int:

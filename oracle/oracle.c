@@ -386,3 +386,94 @@ int oracle_backward(const double* x, const double* dt, const double* A, const do
   free(buf); free(th); free(jobs);
   return rc < 0 ? rc : nthreads;
 }
+
+/* ===================================================================================== *
+ * MIMO scan: P input/output channels of a head share one complex state per (b, head, n).
+ * "Mamba-3 paper story" (MIMO section and its SISO/MIMO table) widens B and C from vectors to
+ * N x P matrices so that one state serves P channels, raising the work per byte; its
+ * formulas were lost from the page. Reading taken (the SISO sharing carried over):
+ *   a_t = exp(dt[b,t,h] A[h,n] + i theta[b,t,n])
+ *   v_t[n] = sum_p Bm[b,t,n,p] x[b,t,h,p]                       (the rank-P injection)
+ *   exp-Euler:  h_t = a_t h_{t-1} + dt_t v_t
+ *   trapezoid:  h_t = a_t h_{t-1} + (1 - lam_t) dt_t a_t v_{t-1} + lam_t dt_t v_t,  v_{-1} = 0
+ *   y[b,t,h,p] = Re(sum_n Cm[b,t,n,p] h_t[n]) + Dskip[h,p] x[b,t,h,p]
+ * Layouts (float64; complex interleaved): x, y (B,L,H,P); dt (B,L,H); A (H,N);
+ * Bm, Cm (B,L,N,P) complex; theta (B,L,N); lam (B,L); Dskip (H,P).
+ * With P = 1 this is the scan above with one channel per head.
+ * ===================================================================================== */
+typedef struct {
+  const double *x, *dt, *A, *Bm, *Cm, *theta, *lam, *Dskip;
+  double* y;
+  int64_t B, L, H, P, N;
+  int mode;
+  int64_t row_begin, row_step;
+} mjob_t;
+
+static void mimo_row(const mjob_t* j, int64_t b, int64_t hd, cplx* h, cplx* v_prev) {
+  const int64_t L = j->L, H = j->H, P = j->P, N = j->N;
+  for (int64_t n = 0; n < N; ++n) { h[n] = 0.0; v_prev[n] = 0.0; }
+  for (int64_t t = 0; t < L; ++t) {
+    const double dtt = j->dt[(b * L + t) * H + hd];
+    const double lam = j->mode == 1 ? j->lam[b * L + t] : 0.0;
+    const double* xt = &j->x[((b * L + t) * H + hd) * P];
+    for (int64_t n = 0; n < N; ++n) {
+      const int64_t tn = (b * L + t) * N + n;
+      cplx v = 0.0;
+      for (int64_t p = 0; p < P; ++p) v += load_c(j->Bm, tn * P + p) * xt[p];
+      const cplx a = transition(dtt, j->A[hd * N + n], j->theta[tn]);
+      cplx u;
+      if (j->mode == 0) u = dtt * v;
+      else u = (1.0 - lam) * dtt * a * v_prev[n] + lam * dtt * v;
+      h[n] = a * h[n] + u;
+      v_prev[n] = v;
+    }
+    for (int64_t p = 0; p < P; ++p) {
+      double acc = 0.0;
+      for (int64_t n = 0; n < N; ++n) acc += creal(load_c(j->Cm, ((b * L + t) * N + n) * P + p) * h[n]);
+      j->y[((b * L + t) * H + hd) * P + p] = acc + j->Dskip[hd * P + p] * xt[p];
+    }
+  }
+}
+
+static void* mworker(void* arg) {
+  const mjob_t* j = (const mjob_t*)arg;
+  cplx* h = (cplx*)malloc(sizeof(cplx) * (size_t)(j->N > 0 ? 2 * j->N : 2));
+  if (!h) return (void*)1;
+  for (int64_t r = j->row_begin; r < j->B * j->H; r += j->row_step) mimo_row(j, r / j->H, r % j->H, h, h + j->N);
+  free(h);
+  return NULL;
+}
+
+/* MIMO forward over all (b, head) rows, split across `nthreads` POSIX threads (<= 0: all
+ * online cores). Returns the number of threads used (> 0) or a negative value on bad
+ * arguments. */
+int oracle_forward_mimo(const double* x, const double* dt, const double* A, const double* Bm, const double* Cm,
+                        const double* theta, const double* lam, const double* Dskip, double* y, int64_t B, int64_t L,
+                        int64_t H, int64_t P, int64_t N, int mode, int nthreads) {
+  if (B < 0 || L < 0 || H < 0 || P < 0 || N < 0) return -1;
+  if (mode != 0 && mode != 1) return -2;
+  if (mode == 1 && !lam && B * L > 0) return -3;
+  if (nthreads <= 0) nthreads = oracle_default_threads();
+  if ((int64_t)nthreads > B * H) nthreads = (int)(B * H > 0 ? B * H : 1);
+  mjob_t base = {x, dt, A, Bm, Cm, theta, lam, Dskip, y, B, L, H, P, N, mode, 0, 1};
+  if (nthreads == 1) return mworker(&base) ? -4 : 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  mjob_t* jobs = (mjob_t*)malloc(sizeof(mjob_t) * (size_t)nthreads);
+  if (!th || !jobs) { free(th); free(jobs); return -4; }
+  int rc = 0, started = 0;
+  for (int i = 0; i < nthreads; ++i) {
+    jobs[i] = base;
+    jobs[i].row_begin = i;
+    jobs[i].row_step = nthreads;
+    if (pthread_create(&th[i], NULL, mworker, &jobs[i]) != 0) { rc = -5; break; }
+    ++started;
+  }
+  for (int i = 0; i < started; ++i) {
+    void* ret = NULL;
+    pthread_join(th[i], &ret);
+    if (ret) rc = -4;
+  }
+  free(th);
+  free(jobs);
+  return rc < 0 ? rc : nthreads;
+}

@@ -363,6 +363,55 @@ def pin_zoh_small_step_limit(lib):
     assert 0 < e <= 1e-5, e
 
 
+# ---------------------------------------------------------------------------- MIMO
+def mimo_case(rng, B, L, H, P, N, mode):
+    return dict(
+        x=rng.standard_normal((B, L, H, P)),
+        delta=np.exp(rng.uniform(math.log(1e-2), math.log(0.5), (B, L, H))),
+        A=-np.exp(rng.uniform(0.0, math.log(8.0), (H, N))),
+        Bm=rng.standard_normal((B, L, N, P)) * 0.5 + 1j * rng.standard_normal((B, L, N, P)) * 0.5,
+        Cm=rng.standard_normal((B, L, N, P)) * 0.5 + 1j * rng.standard_normal((B, L, N, P)) * 0.5,
+        theta=rng.uniform(-1.0, 1.0, (B, L, N)),
+        lam=1.0 / (1.0 + np.exp(-rng.standard_normal((B, L)))) if mode == 1 else None,
+        Dskip=rng.standard_normal((H, P)),
+    )
+
+
+def run_mimo(lib, c, mode):
+    return oracle.forward_mimo(c["x"], c["delta"], c["A"], c["Bm"], c["Cm"], c["theta"], c["lam"], c["Dskip"], mode,
+                               lib=lib)
+
+
+def pin_mimo_one_channel_is_siso(lib):
+    """P = 1: the MIMO scan is the single-input scan with one channel per head (the SISO case
+    the MIMO section starts from), compared with the separately pinned forward oracle."""
+    rng = np.random.default_rng(43)
+    for mode in (0, 1):
+        c = mimo_case(rng, 2, 30, 3, 1, 4, mode)
+        y = run_mimo(lib, c, mode)
+        y_siso = oracle.forward(c["x"][..., 0], c["delta"], c["A"], c["Bm"][..., 0], c["Cm"][..., 0], c["theta"],
+                                c["lam"], c["Dskip"][:, 0], mode, lib=lib)
+        assert rel_err(y[..., 0], y_siso) <= 1e-13
+
+
+def pin_mimo_superposition(lib):
+    """The state is linear in the inputs, so the state shared by P channels is the sum of the P
+    states each channel drives alone: y_ssm[q] = sum_p siso(x[p], Bc = Bm[:, p], Cc = Cm[:, q]).
+    Pins the sum over p and which index of Bm and Cm is the channel."""
+    rng = np.random.default_rng(47)
+    for mode in (0, 1):
+        B, L, H, P, N = 2, 25, 2, 3, 4
+        c = mimo_case(rng, B, L, H, P, N, mode)
+        y = run_mimo(lib, c, mode)
+        for q in range(P):
+            ref = np.zeros((B, L, H))
+            for p in range(P):
+                ref += oracle.forward(c["x"][..., p], c["delta"], c["A"], c["Bm"][..., p], c["Cm"][..., q],
+                                      c["theta"], c["lam"], np.zeros(H), mode, lib=lib)
+            ssm = y[..., q] - c["Dskip"][None, None, :, q] * c["x"][..., q]
+            assert rel_err(ssm, ref) <= 1e-12, (mode, q)
+
+
 # ---------------------------------------------------------------------------- backward
 GRAD_OF = {"x": "dx", "delta": "ddelta", "A": "dA", "Bc": "dBc", "Cc": "dCc", "theta": "dtheta",
            "lam": "dlam", "Dskip": "dDskip"}
@@ -447,4 +496,5 @@ def pin_backward_identities(lib):
 ALL_PINS = [pin_combine_associative, pin_combine_is_composition, pin_bruteforce, pin_closed_form,
             pin_real_reduction, pin_rotation, pin_lambda_one, pin_linearity_and_causality,
             pin_split_invariance, pin_golden, pin_zoh_exact_hold, pin_zoh_real_reduction, pin_zoh_small_step_limit,
+            pin_mimo_one_channel_is_siso, pin_mimo_superposition,
             pin_backward_finite_differences, pin_backward_identities]

@@ -55,6 +55,14 @@ MUTANTS = [
     ("zoh gamma without the division", "(cexp(z) - 1.0) / z;", "(cexp(z) - 1.0);"),
     ("zoh gamma without dt", "cplx gamma = dt * phi;", "cplx gamma = phi;"),
     ("zoh gamma conjugated", "cplx gamma = dt * phi;", "cplx gamma = dt * conj(phi);"),
+    # MIMO
+    ("mimo injection from the first channel only", "for (int64_t p = 0; p < P; ++p) v += load_c(j->Bm, tn * P + p) * xt[p];",
+     "for (int64_t p = 0; p < 1; ++p) v += load_c(j->Bm, tn * P + p) * xt[p];"),
+    ("mimo output reads Cm's channel as the state", "load_c(j->Cm, ((b * L + t) * N + n) * P + p)",
+     "load_c(j->Cm, ((b * L + t) * P + p) * N + n)"),
+    ("mimo trapezoid without a_t", "u = (1.0 - lam) * dtt * a * v_prev[n] + lam * dtt * v;",
+     "u = (1.0 - lam) * dtt * v_prev[n] + lam * dtt * v;"),
+    ("mimo D-skip per head only", "acc + j->Dskip[hd * P + p] * xt[p];", "acc + j->Dskip[hd * P] * xt[p];"),
     # backward
     ("adjoint carried by a instead of conj(a)", "carry[n] = conj(a) * ghat;", "carry[n] = a * ghat;"),
     ("adjoint reads C unconjugated", "const cplx ghat = dyt * conj(load_c(j->Cc, tn)) + carry[n];",
