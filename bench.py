@@ -63,7 +63,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=400)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS))
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(wl.WORKLOADS) + list(wl.MIMO_WORKLOADS))
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -501,8 +501,174 @@ def traffic_from_profiles(workload: str):
         return None
 
 
+# ------------------------------------------------------------------------------ MIMO workloads
+def mimo_alu_ops_per_elem(P: int) -> float:
+    """FP32 lane-operations per (b,t,h,p,n) element of csscan_forward_mimo, counted from its
+    source: the rank-P injection and the output each cost 2 per element; the decay exponent (1),
+    the transition (2), the trapezoid injection (~8) and the update (4) are per (b,t,h,n),
+    shared by the P channels."""
+    return 4.0 + 15.0 / P
+
+
+def mimo_cpu_sample(inp, target_s: float):
+    """Times the float64 MIMO oracle on batch 0 and a prefix of the heads (all steps, channels
+    and states), sized to about target_s seconds. Returns (Gelem/s, threads, description, s)."""
+    import oracle
+    w = inp.workload
+    lib = oracle.load()
+
+    def run(nh):
+        f = wl.widen_mimo(inp, b=slice(0, 1), h=np.arange(nh))
+        t0 = time.perf_counter()
+        oracle.forward_mimo(f["x"], f["delta"], f["A"], f["Bm"], f["Cm"], f["theta"], f["lam"], f["Dskip"], w.mode,
+                            lib=lib)
+        return time.perf_counter() - t0
+
+    nh = min(w.H, oracle.last_thread_count())
+    dt = run(nh)
+    while dt < 0.5 and nh < w.H:
+        nh = min(w.H, nh * 4)
+        dt = run(nh)
+    nh_final = max(1, min(w.H, int(nh * target_s / max(dt, 1e-6))))
+    if nh_final != nh:
+        nh = nh_final
+        dt = run(nh)
+    elems = w.L * nh * w.P * w.N
+    desc = f"batch 0, heads 0..{nh - 1} of {w.H}, all {w.L} steps, {w.P} channels, {w.N} states ({elems:.3e} elements)"
+    return elems / dt / 1e9, oracle.last_thread_count(rows=nh), desc, dt
+
+
+def mimo_config(w) -> dict:
+    return {"workload": w.name, "B": w.B, "L": w.L, "H": w.H, "P": w.P, "N": w.N,
+            "mode": {0: "exp-Euler", 1: "exp-trapezoidal"}[w.mode], "input_dtype": w.dtype,
+            "elements": w.elements, "elements_note": "B*L*H*P*N channel-state pairs", "min_bytes": w.min_bytes()}
+
+
+def run_mimo(args):
+    """The bench contract for a MIMO workload (csscan_forward_mimo): one step = one call."""
+    import torch
+    import torch.distributed as dist
+    from selective_state_space_diagonal_b300 import csscan
+
+    rank, world, local = rank_info()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        w = wl.MIMO_WORKLOADS[args.workload]
+        inp = wl.generate_mimo(w)
+        v, cores, desc, secs = mimo_cpu_sample(inp, max(1.0, min(5.0, 150.0 / max(1, args.steps + args.warmup))))
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": mimo_config(w),
+                "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+                "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    csscan.load_library()
+    w = rank_workload(wl.MIMO_WORKLOADS[args.workload], rank)
+    inp = wl.generate_mimo(w)
+
+    def pinned(a):
+        if a is None:
+            return None
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).pin_memory()
+        return t.view(torch.bfloat16) if a.dtype == np.uint16 else t
+
+    keys = ("x", "delta", "A", "Bm", "Cm", "theta", "lam", "Dskip")
+    host = {k: pinned(getattr(inp, k)) for k in keys}
+    dev = {k: (None if v is None else v.to("cuda", non_blocking=True)) for k, v in host.items()}
+    y = torch.empty((w.B, w.L, w.H, w.P), dtype=torch.float32, device="cuda")
+    y_host = torch.empty(y.shape, dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        csscan.csscan_forward_mimo(dev["x"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], dev["theta"], dev["lam"],
+                                   dev["Dskip"], y, w.mode, stream=stream)
+
+    flush = w.min_bytes() < 4 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") if flush else None
+    l2_note = ("L2 flushed (a 252 MB write) before every step; steps timed individually" if flush else
+               f"inputs larger than L2 ({w.min_bytes() / 1e9:.2f} GB minimum traffic per step), no flush")
+    for _ in range(args.warmup):
+        if flush:
+            scratch.zero_()
+        step()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local).start()
+    with clocks:
+        for i in range(K):
+            if flush:
+                scratch.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    clocks.stop()
+    barrier()
+    call_ms = [a.elapsed_time(b) for a, b in ev]
+    elapsed_ms = sum(call_ms)
+    max_s = reduce_max(elapsed_ms / 1e3)
+    value = aggregate_value(w.elements, K, world, max_s)
+    e2e_steps = max(1, args.e2e_steps)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for k in keys:
+            if host[k] is not None:
+                dev[k].copy_(host[k], non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        stream.synchronize()
+    e2e_s = reduce_max(time.perf_counter() - t0)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    hbm_peak, sm_max_mhz, peak_kind = measured_peaks()
+    mean_s = statistics.mean(call_ms) / 1e3
+    alu_peak = FP32_LANES_PER_SM * N_SM * sm_max_mhz * 1e6 / 1e12
+    ops = mimo_alu_ops_per_elem(w.P)
+    alu = ops * w.elements / mean_s / 1e12
+    gbs = w.min_bytes() / mean_s / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        v, cores, desc, secs = mimo_cpu_sample(inp, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "seconds": secs}
+    import torch as _t
+    nsm = _t.cuda.get_device_properties(local).multi_processor_count
+    launches = 2 if w.B * w.H * w.N >= nsm * 8192 else 4
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": dict(mimo_config(w), l2=l2_note),
+            "roofline": {"bound": "alu", "achieved": alu, "peak": alu_peak, "unit": "Tops/s", "frac": alu / alu_peak,
+                         "traffic": None, "kernel": "mimo_out_kernel (+ table and chunk passes)",
+                         "ms_per_launch": 1e3 * mean_s,
+                         "peak_note": f"FP32 pipe: {FP32_LANES_PER_SM} lanes/SM x {N_SM} SMs x {sm_max_mhz:.0f} MHz; "
+                                      f"{ops:.2f} lane-ops per element"},
+            "hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak, "peak_kind": peak_kind},
+            "cpu_baseline": cpu,
+            "e2e": {"value": aggregate_value(w.elements, e2e_steps, world, e2e_s), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": y.numel() * 4, "steps": e2e_steps},
+            "gpu_launches": launches * K, "clocks": clocks.summary()}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.workload in wl.MIMO_WORKLOADS:
+        return run_mimo(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

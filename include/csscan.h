@@ -177,6 +177,31 @@ int csscan_decode_step(const void* x, const void* delta, const float* A, const v
                        cudaStream_t stream);
 
 /*
+ * MIMO scan: each of H heads holds one complex state of N values shared by its P channels.
+ * "Mamba-3 paper story" (MIMO section) widens B and C from N-vectors to N x P matrices so that
+ * a state serves P input and output channels; its formulas were lost from the page, and the
+ * reading here carries the single-input sharing over:
+ *   a_t     = exp(dt[b,t,h] A[h,n] + i theta[b,t,n])
+ *   v_t[n]  = sum_p Bm[b,t,n,p] x[b,t,h,p]
+ *   exp-Euler   h_t = a_t h_{t-1} + dt_t v_t
+ *   trapezoid   h_t = a_t h_{t-1} + (1 - lam_t) dt_t a_t v_{t-1} + lam_t dt_t v_t   (v_{-1} = 0)
+ *   y[b,t,h,p] = Re(sum_n Cm[b,t,n,p] h_t[n]) + Dskip[h,p] x[b,t,h,p]
+ * With P = 1 it is csscan_forward with D = H.
+ *   x       : (B, L, H, P) in `dtype`          delta : (B, L, H) in `dtype`
+ *   Bm, Cm  : (B, L, N, P, 2) in `dtype`, complex entries (re, im), shared by all heads
+ *   theta   : (B, L, N) in `dtype`             lambda : (B, L) in `dtype` (trapezoid mode only)
+ *   A       : device float32 (H, N)            Dskip : device float32 (H, P)
+ *   y       : device float32 (B, L, H, P), written in full
+ *   mode    : CSSCAN_MODE_EXP_EULER or CSSCAN_MODE_EXP_TRAPEZOID (ZOH: CSSCAN_ERR_UNSUPPORTED)
+ * N must be 2, 4, 8, 16 or 32 and P 1, 2, 4 or 8 (CSSCAN_ERR_UNSUPPORTED otherwise). Pointers
+ * need their element alignment, Bm and Cm that of one complex entry. Starts from the zero
+ * state. Uses the per-stream workspace like csscan_forward.
+ */
+int csscan_forward_mimo(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
+                        const void* theta, const void* lambda, const float* Dskip, float* y, int64_t B, int64_t L,
+                        int64_t H, int64_t P, int64_t N, int mode, int dtype, cudaStream_t stream);
+
+/*
  * Backward pass of csscan_forward (sequence from the zero state, no step -1 halo): the
  * gradients of l = sum_{b,t,d} dy[b,t,d] y[b,t,d] with respect to every input. The pages call
  * for this pass and for regenerating the states during it instead of storing them ("Complex

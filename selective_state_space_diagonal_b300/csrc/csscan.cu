@@ -1,8 +1,9 @@
 // csscan.cu -- host side of the C ABI declared in include/csscan.h: argument checks,
 // launch planning (block width, sequence chunks, shared-memory ring), the per-(device,
 // stream) workspace, tile-copy descriptors, and the launches of the rotation-table kernel
-// and the scan kernel (scan_kernels.cuh), the zero-order-hold scan (zoh_kernels.cuh), the
-// decode step (decode_kernel.cuh) and the backward pass (backward_kernels.cuh).
+// and the scan kernel (scan_kernels.cuh), the zero-order-hold scan (zoh_kernels.cuh), the MIMO
+// scan (mimo_kernels.cuh), the decode step (decode_kernel.cuh) and the backward pass
+// (backward_kernels.cuh).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -16,6 +17,7 @@
 #include "csscan.h"
 #include "backward_kernels.cuh"
 #include "decode_kernel.cuh"
+#include "mimo_kernels.cuh"
 #include "scan_kernels.cuh"
 #include "zoh_kernels.cuh"
 
@@ -549,6 +551,118 @@ int decode_impl(const void* x, const void* delta, const float* A, const void* Bc
   return mode == 0 ? dispatch_decode<uint16_t, 0>(dp, stream) : dispatch_decode<uint16_t, 1>(dp, stream);
 }
 
+// ----------------------------------------------------------------------------- MIMO
+struct MimoArgs {
+  const void *x, *delta, *Bm, *Cm, *theta, *lam;
+  const float *A, *Dskip;
+  float* y;
+  int64_t B, L, H, P, N;
+  int mode, dtype;
+};
+
+template <typename Tin, int MODE, int N, int P>
+int launch_mimo(const MimoArgs& a, cudaStream_t st) {
+  int dev = 0, nsm = 0;
+  CSSCAN_CUDA(cudaGetDevice(&dev));
+  CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
+  // time chunks until there are about 8192 threads per SM (the recurrence is sequential per thread)
+  const int64_t G = mimo::GROUP;
+  const int64_t S = (a.L + G - 1) / G;
+  const int64_t rows = a.B * a.H * N;
+  const int64_t target = int64_t(nsm) * 8192;
+  int64_t C = std::min<int64_t>(S, std::max<int64_t>(1, (target + rows - 1) / rows));
+  const int64_t TC = (S + C - 1) / C * G;
+  C = (a.L + TC - 1) / TC;
+  const size_t rot_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float2), 256);
+  const size_t chunk_bytes = C > 1 ? size_t(a.B * C * a.H * N) * 2 * sizeof(float2) : 0;
+  WsEntry ws;
+  int rc = get_workspace(dev, st, 1, rot_bytes + chunk_bytes, &ws);
+  if (rc != CSSCAN_OK) return rc;
+  char* rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
+  mimo::Params p;
+  p.x = a.x;
+  p.dt = a.delta;
+  p.Bm = a.Bm;
+  p.Cm = a.Cm;
+  p.lam = MODE == 1 ? a.lam : nullptr;
+  p.A = a.A;
+  p.Dskip = a.Dskip;
+  p.y = a.y;
+  p.rot = reinterpret_cast<const float2*>(rest);
+  p.chunk = C > 1 ? reinterpret_cast<float2*>(rest + rot_bytes) : nullptr;
+  p.B = int(a.B);
+  p.L = int(a.L);
+  p.H = int(a.H);
+  p.N = N;
+  p.P = P;
+  p.TC = int(TC);
+  p.C = int(C);
+  const long long n_rot = (long long)a.B * a.L * N;
+  mimo::mimo_rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest),
+                                                                           n_rot);
+  CSSCAN_CUDA(cudaGetLastError());
+  const long long n_thr = (long long)a.B * C * a.H * N;
+  if (C > 1) {
+    mimo::mimo_chunk_kernel<Tin, MODE, P><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+    mimo::mimo_combine_kernel<<<unsigned((rows + 255) / 256), 256, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+  }
+  mimo::mimo_out_kernel<Tin, MODE, N, P><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
+  CSSCAN_CUDA(cudaGetLastError());
+  return CSSCAN_OK;
+}
+
+template <typename Tin, int MODE, int P>
+int dispatch_mimo_n(const MimoArgs& a, cudaStream_t st) {
+  switch (a.N) {
+    case 2: return launch_mimo<Tin, MODE, 2, P>(a, st);
+    case 4: return launch_mimo<Tin, MODE, 4, P>(a, st);
+    case 8: return launch_mimo<Tin, MODE, 8, P>(a, st);
+    case 16: return launch_mimo<Tin, MODE, 16, P>(a, st);
+    case 32: return launch_mimo<Tin, MODE, 32, P>(a, st);
+    default: return CSSCAN_ERR_UNSUPPORTED;
+  }
+}
+
+template <typename Tin, int MODE>
+int dispatch_mimo(const MimoArgs& a, cudaStream_t st) {
+  switch (a.P) {
+    case 1: return dispatch_mimo_n<Tin, MODE, 1>(a, st);
+    case 2: return dispatch_mimo_n<Tin, MODE, 2>(a, st);
+    case 4: return dispatch_mimo_n<Tin, MODE, 4>(a, st);
+    case 8: return dispatch_mimo_n<Tin, MODE, 8>(a, st);
+    default: return CSSCAN_ERR_UNSUPPORTED;
+  }
+}
+
+int mimo_impl(const MimoArgs& a, cudaStream_t st) {
+  if (a.mode != CSSCAN_MODE_EXP_EULER && a.mode != CSSCAN_MODE_EXP_TRAPEZOID) {
+    return a.mode == CSSCAN_MODE_ZOH ? CSSCAN_ERR_UNSUPPORTED : CSSCAN_ERR_INVALID_ARG;
+  }
+  if (a.dtype != CSSCAN_F32 && a.dtype != CSSCAN_BF16) return CSSCAN_ERR_INVALID_ARG;
+  if (a.B < 0 || a.L < 0 || a.H < 0 || a.P <= 0 || a.N <= 0) return CSSCAN_ERR_INVALID_ARG;
+  const bool rows = a.B > 0 && a.L > 0, heads = a.H > 0;
+  if (heads && (!a.A || !a.Dskip)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && (!a.Bm || !a.Cm || !a.theta)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && heads && (!a.x || !a.delta || !a.y)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && a.mode == CSSCAN_MODE_EXP_TRAPEZOID && !a.lam) return CSSCAN_ERR_INVALID_ARG;
+  if (a.N != 2 && a.N != 4 && a.N != 8 && a.N != 16 && a.N != 32) return CSSCAN_ERR_UNSUPPORTED;
+  if (a.P != 1 && a.P != 2 && a.P != 4 && a.P != 8) return CSSCAN_ERR_UNSUPPORTED;
+  if (a.B > (int64_t(1) << 31) - 1 || a.L > (int64_t(1) << 30) || a.H > (int64_t(1) << 30) ||
+      a.B * a.L * a.H * a.P > (int64_t(1) << 40))
+    return CSSCAN_ERR_UNSUPPORTED;
+  const size_t s = a.dtype == CSSCAN_F32 ? 4 : 2;
+  if (!aligned(a.x, s) || !aligned(a.delta, s) || !aligned(a.Bm, 2 * s) || !aligned(a.Cm, 2 * s) ||
+      !aligned(a.theta, s) || (a.lam && !aligned(a.lam, s)) || !aligned(a.A, 4) || !aligned(a.Dskip, 4) ||
+      !aligned(a.y, 4))
+    return CSSCAN_ERR_MISALIGNED;
+  if (!rows || !heads) return CSSCAN_OK;
+  if (a.dtype == CSSCAN_F32)
+    return a.mode == 0 ? dispatch_mimo<float, 0>(a, st) : dispatch_mimo<float, 1>(a, st);
+  return a.mode == 0 ? dispatch_mimo<uint16_t, 0>(a, st) : dispatch_mimo<uint16_t, 1>(a, st);
+}
+
 // ----------------------------------------------------------------------------- backward
 struct BwdArgs {
   const void *x, *delta, *Bc, *Cc, *theta, *lam;
@@ -828,6 +942,13 @@ int csscan_forward_noalloc(const void* x, const void* delta, const float* A, con
                        : dispatch_noalloc<float, 1>(a, device_status, stream);
   return a.mode == 0 ? dispatch_noalloc<uint16_t, 0>(a, device_status, stream)
                      : dispatch_noalloc<uint16_t, 1>(a, device_status, stream);
+}
+
+int csscan_forward_mimo(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
+                        const void* theta, const void* lambda, const float* Dskip, float* y, int64_t B, int64_t L,
+                        int64_t H, int64_t P, int64_t N, int mode, int dtype, cudaStream_t stream) {
+  MimoArgs a{x, delta, Bm, Cm, theta, lambda, A, Dskip, y, B, L, H, P, N, mode, dtype};
+  return mimo_impl(a, stream);
 }
 
 int csscan_backward(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,

@@ -71,6 +71,8 @@ def load_library(path: str = LIBRARY) -> ctypes.CDLL:
     lib.csscan_forward_state.restype = i32
     lib.csscan_decode_step.argtypes = [vp] * 12 + [i64] * 3 + [i32, i32, vp]
     lib.csscan_decode_step.restype = i32
+    lib.csscan_forward_mimo.argtypes = [vp] * 9 + [i64] * 5 + [i32, i32, vp]
+    lib.csscan_forward_mimo.restype = i32
     lib.csscan_backward.argtypes = [vp] * 17 + [i64] * 4 + [i32, i32, vp]
     lib.csscan_backward.restype = i32
     _lib = lib
@@ -154,6 +156,19 @@ def csscan_decode_step(x, delta, A, Bc, Cc, theta, lam, Dskip, y, h, mode: int, 
         _ptr(x_prev), _ptr(Bc_prev), B, D, N, int(mode), _dtype_code(x), _stream_handle(stream))
     if rc != CSSCAN_OK:
         raise CsscanError(rc, "csscan_decode_step")
+
+
+def csscan_forward_mimo(x, delta, A, Bm, Cm, theta, lam, Dskip, y, mode: int, stream=None) -> None:
+    """MIMO scan (P channels of a head share one state): x (B,L,H,P), delta (B,L,H),
+    Bm, Cm (B,L,N,P,2), theta (B,L,N), lam (B,L) or None, A (H,N), Dskip (H,P) float32,
+    y (B,L,H,P) float32 out."""
+    B, L, H, P = x.shape
+    N = A.shape[1]
+    rc = load_library().csscan_forward_mimo(_ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(theta),
+                                            _ptr(lam), _ptr(Dskip), _ptr(y), B, L, H, P, N, int(mode),
+                                            _dtype_code(x), _stream_handle(stream))
+    if rc != CSSCAN_OK:
+        raise CsscanError(rc, "csscan_forward_mimo")
 
 
 def csscan_backward(x, delta, A, Bc, Cc, theta, lam, Dskip, dy, mode: int, stream=None, out=None) -> dict:

@@ -254,3 +254,118 @@ def widen(inp: Inputs, b: Optional[slice] = None, d: Optional[np.ndarray] = None
         "Dskip": inp.Dskip[dsel].astype(np.float64),
     }
     return out
+
+
+# ----------------------------------------------------------------------------- MIMO workloads
+@dataclasses.dataclass(frozen=True)
+class MimoWorkload:
+    """A MIMO scan: H heads of P channels, each head one state of N complex values shared by
+    its P channels. Same distributions as Workload (dt per (b,t,h), A per (h,n), Dskip per
+    (h,p), Bm and Cm per (b,t,n,p))."""
+    name: str
+    B: int
+    L: int
+    H: int
+    P: int
+    N: int
+    mode: int
+    dtype: str
+    dt_lo: float
+    dt_hi: float
+    A_kind: str
+    theta_max: float
+    seed: int
+
+    @property
+    def elements(self) -> int:
+        """B*L*H*P*N: channel-state pairs per step, as B*L*D*N with D = H*P channels."""
+        return self.B * self.L * self.H * self.P * self.N
+
+    @property
+    def in_bytes(self) -> int:
+        return 4 if self.dtype == "f32" else 2
+
+    def min_bytes(self) -> int:
+        """Minimum HBM bytes of one pass: per (b,t) x (H*P*s), y (H*P*4), dt (H*s), Bm and Cm
+        (4*N*P*s), theta (N*s), lam (s, trapezoid); A and Dskip once."""
+        s = self.in_bytes
+        per_bt = self.H * self.P * (s + 4) + self.H * s + 4 * self.N * self.P * s + self.N * s + \
+            (s if self.mode == 1 else 0)
+        return self.B * self.L * per_bt + (self.H * self.N + self.H * self.P) * 4
+
+    def with_shape(self, **kw) -> "MimoWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+MIMO_WORKLOADS: Dict[str, MimoWorkload] = {
+    # the large-batch shape's 2560 channels as 640 heads of 4, trapezoid, bf16
+    "mimo_trap_bf16_batch": MimoWorkload("mimo_trap_bf16_batch", 16, 8192, 640, 4, 16, 1, "bf16", 1e-3, 1e-1,
+                                         "neg_exp_u_ln16", math.pi, 0x5EED0006),
+}
+
+
+@dataclasses.dataclass
+class MimoInputs:
+    workload: MimoWorkload
+    x: np.ndarray        # (B,L,H,P)
+    delta: np.ndarray    # (B,L,H)
+    A: np.ndarray        # (H,N) float32
+    Bm: np.ndarray       # (B,L,N,P,2)
+    Cm: np.ndarray       # (B,L,N,P,2)
+    theta: np.ndarray    # (B,L,N)
+    lam: Optional[np.ndarray]  # (B,L) or None
+    Dskip: np.ndarray    # (H,P) float32
+
+
+def generate_mimo(w: MimoWorkload, threads: Optional[int] = None) -> MimoInputs:
+    threads = threads or min(32, os.cpu_count() or 1)
+    st = w.dtype
+    sdt = np.float32 if st == "f32" else np.uint16
+    B, L, H, P, N = w.B, w.L, w.H, w.P, w.N
+    keys = {k: stream_key(w.seed, t) for k, t in TID.items()}
+    x = np.empty((B, L, H, P), dtype=sdt)
+    _fill(x, lambda i: normals(keys["x"], i), st, threads)
+    lo, hi = math.log(w.dt_lo), math.log(w.dt_hi)
+    delta = np.empty((B, L, H), dtype=sdt)
+    _fill(delta, lambda i: np.exp(lo + (hi - lo) * uniforms(keys["delta"], i)), st, threads)
+    n_idx = np.arange(H * N, dtype=np.uint64)
+    n_of = (np.arange(H * N) % N).astype(np.float64)
+    if w.A_kind == "neg_n1":
+        A64 = -(n_of + 1.0)
+    elif w.A_kind == "neg_n1_over16":
+        A64 = -(n_of + 1.0) / 16.0
+    elif w.A_kind == "neg_exp_u_ln16":
+        A64 = -np.exp(math.log(16.0) * uniforms(keys["A"], n_idx))
+    else:
+        raise ValueError(w.A_kind)
+    A = round_to_f32(A64).reshape(H, N)
+    Bm = np.empty((B, L, N, P, 2), dtype=sdt)
+    _fill(Bm, lambda i: 0.5 * normals(keys["Bc"], i), st, threads)
+    Cm = np.empty((B, L, N, P, 2), dtype=sdt)
+    _fill(Cm, lambda i: 0.5 * normals(keys["Cc"], i), st, threads)
+    m = w.theta_max
+    theta = np.empty((B, L, N), dtype=sdt)
+    _fill(theta, lambda i: -m + 2.0 * m * uniforms(keys["theta"], i), st, threads)
+    lam = None
+    if w.mode == 1:
+        lam = np.empty((B, L), dtype=sdt)
+        _fill(lam, lambda i: 1.0 / (1.0 + np.exp(-normals(keys["lam"], i))), st, threads)
+    Dskip = round_to_f32(normals(keys["Dskip"], np.arange(H * P, dtype=np.uint64))).reshape(H, P)
+    return MimoInputs(w, x, delta, A, Bm, Cm, theta, lam, Dskip)
+
+
+def widen_mimo(inp: MimoInputs, b: Optional[slice] = None, h: Optional[np.ndarray] = None) -> dict:
+    """Float64/complex128 copies (optionally a batch slice and a subset of heads)."""
+    st = inp.workload.dtype
+    bs = b if b is not None else slice(None)
+    hs = h if h is not None else slice(None)
+    return {
+        "x": to_f64(inp.x[bs][:, :, hs], st),
+        "delta": to_f64(inp.delta[bs][:, :, hs], st),
+        "A": inp.A[hs].astype(np.float64),
+        "Bm": to_complex(to_f64(inp.Bm[bs], st)),
+        "Cm": to_complex(to_f64(inp.Cm[bs], st)),
+        "theta": to_f64(inp.theta[bs], st),
+        "lam": to_f64(inp.lam[bs], st) if inp.lam is not None else None,
+        "Dskip": inp.Dskip[hs].astype(np.float64),
+    }

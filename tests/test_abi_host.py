@@ -111,3 +111,17 @@ def test_backward_rejects_bad_arguments_on_host(lib):
     assert bw(*args(mode=3)) == csscan.CSSCAN_ERR_INVALID_ARG
     assert bw(*args(dx=A16 + 2)) == csscan.CSSCAN_ERR_MISALIGNED
     assert bw(*args(x=A16 + 1, dtype=1)) == csscan.CSSCAN_ERR_MISALIGNED
+
+
+def test_mimo_rejects_bad_arguments_on_host(lib):
+    mf = lib.csscan_forward_mimo
+    def args(**k):
+        return [A16, A16, A16, k.get("bm", A16), A16, A16, k.get("lam", A16), A16, A16,
+                2, 64, 4, k.get("P", 4), k.get("N", 16), k.get("mode", 0), 0, None]
+    assert mf(*args(P=3)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert mf(*args(P=16)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert mf(*args(N=64)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert mf(*args(mode=2)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert mf(*args(mode=5)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert mf(*args(mode=1, lam=None)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert mf(*args(bm=A16 + 4)) == csscan.CSSCAN_ERR_MISALIGNED    # one float32 complex entry is 8 bytes
