@@ -264,13 +264,13 @@ def run_reference(args):
 
 def launches_per_step(w: wl.Workload) -> int:
     """Kernels one forward call enqueues: the rotation table and the scan; in the zero-order-hold
-    mode the table, the output pass and, when the rows alone leave under 8192 threads per SM
+    mode the table, the output pass and, when the rows alone leave under 4096 threads per SM
     (the library's rule), the time-chunk pass and the chunk sweep."""
     if w.mode != wl.MODE_ZOH:
         return 2
     import torch
     nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return 2 if w.B * w.D * w.N >= nsm * 8192 else 4
+    return 2 if w.B * w.D * w.N >= nsm * 4096 else 4
 
 
 def workload_config(w: wl.Workload, l2_note: str = ""):
@@ -645,7 +645,7 @@ def run_mimo(args):
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "seconds": secs}
     import torch as _t
     nsm = _t.cuda.get_device_properties(local).multi_processor_count
-    launches = 2 if w.B * w.H * w.N >= nsm * 8192 else 4
+    launches = 2 if w.B * w.H * w.N * w.P >= nsm * 4096 else 4
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic", "config": dict(mimo_config(w), l2=l2_note),

@@ -28,7 +28,7 @@
 //                     entry state and backwards for each chunk's true first-step adjoint;
 //   ckpt_kernel       per (b, c, d, n): the forward recurrence over the chunk from its entry
 //                     state, storing the state before every segment of SEG steps;
-//   grad_kernel   a thread owns one state n of K channels of one batch row. For each segment,
+//   grad_kernel   a thread owns one state n of K = 4 channels of one batch row. For each segment,
 //                 last to first, and each of its channels it recomputes the segment's SEG states
 //                 from the checkpoint into registers, then walks the segment backwards. Sums over
 //                 n (dx, ddt, dlam) use a butterfly over the N lanes of a channel; sums over d
@@ -74,7 +74,7 @@ struct Params {
 template <int N> struct GradTile {
   static_assert(N >= 2 && N <= 32 && (N & (N - 1)) == 0, "grad_kernel handles N = 2 .. 32");
   static constexpr int CPW = 32 / N;
-  static constexpr int K = N < 16 ? N : 16;
+  static constexpr int K = N < 4 ? N : 4;
   static constexpr int CB = K * CPW * WARPS;
 };
 

@@ -92,6 +92,9 @@ struct Plan {
 };
 
 constexpr int MAX_DYN_SMEM = 160 * 1024;         // opt-in dynamic shared memory per block
+// The zero-order-hold and MIMO paths run one thread per (row, state) sequentially over time;
+// below this many such threads per SM they also split the sequence into time chunks.
+constexpr int64_t SEQ_THREADS_PER_SM = 4096;
 constexpr int RESIDENT_WARPS_PER_SM = 8;         // target of the automatic chunking
 
 // Blocks of `threads` threads and `smem` dynamic bytes resident per SM (cached per device).
@@ -406,11 +409,11 @@ int launch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
   int dev = 0, nsm = 0;
   CSSCAN_CUDA(cudaGetDevice(&dev));
   CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-  // time chunks until there are about 8192 threads per SM (the recurrence is sequential per thread)
+  // time chunks until there are SEQ_THREADS_PER_SM threads per SM (the recurrence is sequential per thread)
   const int64_t G = zoh::GROUP;
   const int64_t S = (a.L + G - 1) / G;
   const int64_t rows = a.B * a.D * N;
-  const int64_t target = int64_t(nsm) * 8192;
+  const int64_t target = int64_t(nsm) * SEQ_THREADS_PER_SM;
   int64_t C = std::min<int64_t>(S, std::max<int64_t>(1, (target + rows - 1) / rows));
   const int64_t TC = (S + C - 1) / C * G;
   C = (a.L + TC - 1) / TC;
@@ -565,11 +568,12 @@ int launch_mimo(const MimoArgs& a, cudaStream_t st) {
   int dev = 0, nsm = 0;
   CSSCAN_CUDA(cudaGetDevice(&dev));
   CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-  // time chunks until there are about 8192 threads per SM (the recurrence is sequential per thread)
+  // time chunks until there are SEQ_THREADS_PER_SM / P threads per SM (the recurrence is sequential
+  // per thread, and a thread carries P channels' work)
   const int64_t G = mimo::GROUP;
   const int64_t S = (a.L + G - 1) / G;
   const int64_t rows = a.B * a.H * N;
-  const int64_t target = int64_t(nsm) * 8192;
+  const int64_t target = int64_t(nsm) * SEQ_THREADS_PER_SM / P;
   int64_t C = std::min<int64_t>(S, std::max<int64_t>(1, (target + rows - 1) / rows));
   const int64_t TC = (S + C - 1) / C * G;
   C = (a.L + TC - 1) / TC;
@@ -680,11 +684,16 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
   CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
   const int64_t S = (a.L + bwd::SEG - 1) / bwd::SEG;
   // time chunks, only where the rows leave the GPU short of about two gradient blocks per SM;
-  // then enough chunks for about four per SM (the two chunk passes cost about one forward each)
+  // then enough chunks for about four gradient blocks per SM and SEQ_THREADS_PER_SM threads of
+  // the sequential per-(b, d, n) passes per SM (the two chunk passes cost about one forward each)
   const int64_t row_blocks = a.B * ((a.D + bwd::GradTile<N>::CB - 1) / bwd::GradTile<N>::CB);
-  int64_t C = row_blocks >= 2 * int64_t(nsm)
-                  ? 1
-                  : std::min<int64_t>(S, std::max<int64_t>(1, (4 * int64_t(nsm) + row_blocks - 1) / row_blocks));
+  const int64_t seq_rows = a.B * a.D * N;
+  int64_t C = 1;
+  if (row_blocks < 2 * int64_t(nsm)) {
+    const int64_t c_blocks = (4 * int64_t(nsm) + row_blocks - 1) / row_blocks;
+    const int64_t c_threads = (int64_t(nsm) * SEQ_THREADS_PER_SM + seq_rows - 1) / seq_rows;
+    C = std::min<int64_t>(S, std::max<int64_t>(1, std::max(c_blocks, c_threads)));
+  }
   if (C > 65535) C = 65535;
   const int64_t TC = (S + C - 1) / C * bwd::SEG;
   C = (a.L + TC - 1) / TC;

@@ -9,7 +9,7 @@
 // rotating-frame scan kernel does not apply; these kernels run the recurrence directly:
 //   zoh_table_kernel   per (b, t, n): cos theta, sin theta, theta, cos theta - 1
 //   zoh_chunk_kernel   per (b, c, d, n): state at the chunk's end from a zero entry state and
-//                      the product of a over the chunk                       (chunks > 1 only)
+//                      the product of a over the chunk  (only when the rows leave few threads)
 //   zoh_combine_kernel per (b, d, n): walks the chunks for each chunk's entry state
 //   zoh_out_kernel     per (b, c, d, n): the recurrence over the chunk from its entry state;
 //                      the N lanes of a channel sum Re(Cc h) with shuffles and one stores y
@@ -62,7 +62,7 @@ __device__ __forceinline__ void zoh_step(float dtt, float xt, float Adn, float4 
   const float zz = fmaf(zr, zr, zi * zi);
   float pr, pi;   // phi = (e^z - 1) / z
   if (zz > 1e-12f) {
-    const float inv = 1.f / zz;
+    const float inv = __frcp_rn(zz);
     pr = (er * zr + ei * zi) * inv;
     pi = (ei * zr - er * zi) * inv;
   } else {        // |z| < 1e-6: 1 + z/2 + z^2/6
