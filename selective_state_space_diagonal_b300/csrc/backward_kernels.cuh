@@ -102,17 +102,23 @@ struct FwdStep {
                                         float* Pr = nullptr, float* Pi = nullptr) const {
     float xs[SEG], ds[SEG], brs[SEG], bis[SEG], ls[SEG];
     float2 ros[SEG];
+    // one 64-bit base per array for the group; steps past te - 1 repeat the last one
+    const long long bt = b * L + t0;
+    const Tin* xg = X + bt * D + d;
+    const Tin* dg = DT + bt * D + d;
+    const float2* rg = rot + bt * N + n;
+    const Tin* bg = BC + 2 * (bt * N + n);
+    const int last = te - 1 - t0;
 #pragma unroll
     for (int i = 0; i < SEG; ++i) {
-      const int t = min(t0 + i, te - 1);
-      const long long td = (b * L + t) * D + d;
-      const long long tn = (b * L + t) * N + n;
-      xs[i] = load_in<Tin>(X, td);
-      ds[i] = load_in<Tin>(DT, td);
-      ros[i] = rot[tn];
-      brs[i] = load_in<Tin>(BC, 2 * tn);
-      bis[i] = load_in<Tin>(BC, 2 * tn + 1);
-      ls[i] = MODE == 1 ? load_in<Tin>(LAM, b * L + t) : 0.f;
+      const int ii = min(i, last);
+      xs[i] = load_in<Tin>(xg, ii * D);
+      ds[i] = load_in<Tin>(dg, ii * D);
+      ros[i] = rg[ii * N];
+      const float2 bb = load_pair<Tin>(bg, ii * N);
+      brs[i] = bb.x;
+      bis[i] = bb.y;
+      ls[i] = MODE == 1 ? load_in<Tin>(LAM, bt + ii) : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < SEG; ++i) {
@@ -198,7 +204,7 @@ __device__ __forceinline__ float2* chunk_rec(const Params& p, long long b, int c
 
 // U_c (state at the chunk's end from a zero entry state) and P_c (product of a over the chunk).
 template <typename Tin, int MODE>
-__global__ void __launch_bounds__(256) chunk_fwd_kernel(const Params p) {
+__global__ void __launch_bounds__(256, 3) chunk_fwd_kernel(const Params p) {
   const ChunkThread th = chunk_thread(p);
   if (!th.ok) return;
   const auto f = fwd_step<Tin, MODE>(p, th.b, th.d, th.n);
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(256) chunk_combine_kernel(const Params p) {
 // Forward recurrence per (b, c, d, n) over chunk c from its entry state, storing h_{s SEG - 1}
 // before every segment s that starts inside the chunk.
 template <typename Tin, int MODE>
-__global__ void __launch_bounds__(256) ckpt_kernel(const Params p) {
+__global__ void __launch_bounds__(256, 3) ckpt_kernel(const Params p) {
   const ChunkThread th = chunk_thread(p);
   if (!th.ok) return;
   const auto f = fwd_step<Tin, MODE>(p, th.b, th.d, th.n);
