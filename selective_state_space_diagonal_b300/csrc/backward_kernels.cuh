@@ -27,7 +27,10 @@
 //   chunk_combine_kernel  per (b, d, n): walks the C chunks forwards for each chunk's true
 //                     entry state and backwards for each chunk's true first-step adjoint;
 //   ckpt_kernel       per (b, c, d, n): the forward recurrence over the chunk from its entry
-//                     state, storing the state before every segment of SEG steps;
+//                     state, storing the state before every segment of SEG steps (used when the
+//                     inputs do not meet the tile-copy rules of the scan kernel, whose
+//                     checkpoint variant otherwise writes every segment's entry state and makes
+//                     chunk_fwd_kernel and this pass unnecessary);
 //   grad_kernel   a thread owns one state n of K = 4 channels of one batch row. For each segment,
 //                 last to first, and each of its channels it recomputes the segment's SEG states
 //                 from the checkpoint into registers, then walks the segment backwards. Sums over
@@ -68,6 +71,7 @@ struct Params {
   float2* chunk;       // (B, C, D, N, 5) per chunk: U | h_in, P, W | ghat_first, Q, conj(a_tc)
   int B, L, D, N, S;
   int TC, C;           // chunk length (a multiple of SEG) and chunk count
+  int fwd_ckpt;        // 1: ckpt holds every segment's entry state (chunk starts included)
 };
 
 // Channels per block of grad_kernel: K slots per thread x (32 / N) channels per warp x WARPS.
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(256) chunk_combine_kernel(const Params p) {
   const int d = int(bd % p.D);
   const long long b = bd / p.D;
   float hr = 0.f, hi = 0.f;
-  for (int c = 0; c < p.C; ++c) {
+  for (int c = 0; c < p.C && !p.fwd_ckpt; ++c) {   // entry states (not needed with forward checkpoints)
     float2* rec = chunk_rec(p, b, c, d, n);
     const float2 U = rec[0], P = rec[1];
     rec[0] = make_float2(hr, hi);
@@ -451,6 +455,10 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
       // ---- forward: the segment's states from the checkpoint (or the chunk's entry state)
       float h0r = 0.f, h0i = 0.f;
       if (valid && s > s_first) {
+        const float2 c = p.ckpt[((b * p.S + s) * D + dd) * N + n];
+        h0r = c.x;
+        h0i = c.y;
+      } else if (valid && s == s_first && chunk > 0 && p.fwd_ckpt) {
         const float2 c = p.ckpt[((b * p.S + s) * D + dd) * N + n];
         h0r = c.x;
         h0i = c.y;

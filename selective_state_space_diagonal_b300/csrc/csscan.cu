@@ -213,7 +213,7 @@ int make_plan(const Args& a, const csscan_options_t& o, int dev, Plan* pl) {
   pl->o_crot = carry == CARRY_DECOUPLED ? take(size_t(n_units) * N * 8) : 0;
   pl->o_tab = take(size_t(a.B) * a.L * 4 * N * 4);
   pl->o_aux = MODE == 1 ? take(size_t(a.B) * a.L * SG::AUX_W * 4) : 0;
-  pl->o_rot = take(size_t(a.B) * S * 2 * N * 4);
+  pl->o_rot = take(size_t(a.B) * S * 4 * 2 * N * 4);
   pl->rest_bytes = off;
   return CSSCAN_OK;
 }
@@ -221,9 +221,11 @@ int make_plan(const Args& a, const csscan_options_t& o, int dev, Plan* pl) {
 // Fill the descriptors and pointers and enqueue both kernels. `hdr` is the workspace header
 // (epoch, ticket, done, status words), `flags` the per-unit flag words, `rest` the region laid
 // out by the plan.
-template <int N, typename Tin, int MODE>
+// CKPT: the checkpoint variant of the scan kernel (no y; the state before every 8-step segment
+// into `ckpt`, (B, S8, D, N) complex), which the backward pass launches.
+template <int N, typename Tin, int MODE, bool CKPT = false>
 int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* hdr, uint32_t* flags, char* rest,
-            cudaStream_t st) {
+            cudaStream_t st, float2* ckpt = nullptr, int64_t S8 = 0) {
   TableParams tp;
   tp.Bc = a.Bc;
   tp.Cc = a.Cc;
@@ -247,7 +249,8 @@ int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* 
             make_map(&sp.tm_dt, tin, a.delta, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, pl.DT, SG::DT_ROWS, 1) &&
             make_map(&sp.tm_tab, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.tab, 4 * N, a.L, a.B, 16 * N, a.L * 16 * N, 4 * N,
                      SG::TAB_ROWS, 1) &&
-            make_map(&sp.tm_rot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.rot, 2 * N, S, a.B, 8 * N, S * 8 * N, 2 * N, 1, 1);
+            make_map(&sp.tm_rot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.rot, 2 * N, 4 * S, a.B, 8 * N, 4 * S * 8 * N, 2 * N, 4,
+                     1);
   if (ok && MODE == 1)
     ok = make_map(&sp.tm_aux, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.aux, SG::AUX_W, a.L, a.B, SG::AUX_W * 4,
                   a.L * SG::AUX_W * 4, SG::AUX_W, SG::AUX_ROWS, 1);
@@ -286,6 +289,8 @@ int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* 
   sp.y_vec2 = (reinterpret_cast<uintptr_t>(a.y) % 8) == 0;
   sp.silent_chunk = o.silent_chunk;
   sp.poll_limit = o.poll_limit > 0 ? o.poll_limit : (int64_t(1) << 22);
+  sp.ckpt = reinterpret_cast<float4*>(ckpt);
+  sp.S8 = int(S8);
 
   const int64_t table_threads = a.B * S * N;
   table_kernel<Tin, MODE><<<unsigned((table_threads + 255) / 256), 256, 0, st>>>(tp);
@@ -293,11 +298,11 @@ int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* 
   if (o.scan_begin) CSSCAN_CUDA(cudaEventRecord(o.scan_begin, st));
   const dim3 grid{unsigned(pl.n_units)}, block{unsigned(THREADS)};
   if (pl.carry == CARRY_NONE)
-    scan_kernel<N, Tin, MODE, CARRY_NONE><<<grid, block, unsigned(pl.smem), st>>>(sp);
+    scan_kernel<N, Tin, MODE, CARRY_NONE, CKPT><<<grid, block, unsigned(pl.smem), st>>>(sp);
   else if (pl.carry == CARRY_SERIAL)
-    scan_kernel<N, Tin, MODE, CARRY_SERIAL><<<grid, block, unsigned(pl.smem), st>>>(sp);
+    scan_kernel<N, Tin, MODE, CARRY_SERIAL, CKPT><<<grid, block, unsigned(pl.smem), st>>>(sp);
   else
-    scan_kernel<N, Tin, MODE, CARRY_DECOUPLED><<<grid, block, unsigned(pl.smem), st>>>(sp);
+    scan_kernel<N, Tin, MODE, CARRY_DECOUPLED, CKPT><<<grid, block, unsigned(pl.smem), st>>>(sp);
   CSSCAN_CUDA(cudaGetLastError());
   if (o.scan_end) CSSCAN_CUDA(cudaEventRecord(o.scan_end, st));
   return CSSCAN_OK;
@@ -554,6 +559,23 @@ int decode_impl(const void* x, const void* delta, const float* A, const void* Bc
   return mode == 0 ? dispatch_decode<uint16_t, 0>(dp, stream) : dispatch_decode<uint16_t, 1>(dp, stream);
 }
 
+// The checkpoint variants of the scan kernel need the same opt-in shared memory as the others.
+template <int N, typename Tin, int MODE>
+int set_ckpt_attributes(int dev) {
+  static std::mutex mu;
+  static std::map<int, bool> done;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done[dev]) return CSSCAN_OK;
+  CSSCAN_CUDA(cudaFuncSetAttribute(scan_kernel<N, Tin, MODE, CARRY_NONE, true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_DYN_SMEM));
+  CSSCAN_CUDA(cudaFuncSetAttribute(scan_kernel<N, Tin, MODE, CARRY_SERIAL, true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_DYN_SMEM));
+  CSSCAN_CUDA(cudaFuncSetAttribute(scan_kernel<N, Tin, MODE, CARRY_DECOUPLED, true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, MAX_DYN_SMEM));
+  done[dev] = true;
+  return CSSCAN_OK;
+}
+
 // ----------------------------------------------------------------------------- MIMO
 struct MimoArgs {
   const void *x, *delta, *Bm, *Cm, *theta, *lam;
@@ -700,10 +722,26 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
   const size_t rot_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float2), 256);
   const size_t ckpt_bytes = align_up(size_t(a.B * S * a.D * N) * sizeof(float2), 256);
   const size_t chunk_bytes = C > 1 ? size_t(a.B * C * a.D * N) * 5 * sizeof(float2) : 0;
+  // The checkpoints come from the scan kernel's checkpoint variant where its tile copies can
+  // read x and delta (16-byte rows and base addresses); otherwise from ckpt_kernel.
+  const size_t s_in = sizeof(Tin);
+  const bool fwd_ckpt = aligned(a.x, 16) && aligned(a.delta, 16) && (a.D * int64_t(s_in)) % 16 == 0;
+  Args fa{a.x, a.delta, a.Bc, a.Cc, a.theta, a.lam, a.A, a.Dskip, nullptr, nullptr, nullptr, nullptr, nullptr,
+          a.B, a.L, a.D, N, a.mode, a.dtype};
+  Plan fpl;
+  if (fwd_ckpt) {
+    int rc = make_plan<N, Tin, MODE>(fa, default_options(), dev, &fpl);
+    if (rc != CSSCAN_OK) return rc;
+    rc = set_ckpt_attributes<N, Tin, MODE>(dev);
+    if (rc != CSSCAN_OK) return rc;
+  }
+  const size_t fwd_bytes = fwd_ckpt ? align_up(fpl.rest_bytes, 256) : 0;
   WsEntry ws;
-  int rc = get_workspace(dev, st, 1, rot_bytes + ckpt_bytes + chunk_bytes, &ws);
+  int rc = get_workspace(dev, st, fwd_ckpt ? size_t(fpl.n_units) : 1, fwd_bytes + rot_bytes + ckpt_bytes + chunk_bytes,
+                         &ws);
   if (rc != CSSCAN_OK) return rc;
-  char* rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
+  char* fwd_rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
+  char* rest = fwd_rest + fwd_bytes;
 
   // gradients that are sums over several rows are accumulated and start at zero
   CSSCAN_CUDA(cudaMemsetAsync(a.dA, 0, size_t(a.D * N) * 4, st));
@@ -740,22 +778,32 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
   p.S = int(S);
   p.TC = int(TC);
   p.C = int(C);
+  p.fwd_ckpt = fwd_ckpt ? 1 : 0;
 
+  if (fwd_ckpt) {   // every checkpoint, chunk entries included, from the scan kernel
+    uint32_t* hdr = static_cast<uint32_t*>(ws.base);
+    rc = enqueue<N, Tin, MODE, true>(fa, default_options(), fpl, hdr,
+                                     reinterpret_cast<uint32_t*>(static_cast<char*>(ws.base) + HDR_BYTES), fwd_rest,
+                                     st, p.ckpt, S);
+    if (rc != CSSCAN_OK) return rc;
+  }
   const long long n_rot = (long long)a.B * a.L * N;
   bwd::rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest), n_rot);
   CSSCAN_CUDA(cudaGetLastError());
   const long long n_ck = (long long)a.B * C * a.D * N;   // threads of the per-chunk passes
   const unsigned ck_blocks = unsigned((n_ck + 255) / 256);
   if (C > 1) {
-    bwd::chunk_fwd_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
-    CSSCAN_CUDA(cudaGetLastError());
+    if (!fwd_ckpt) {
+      bwd::chunk_fwd_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
+      CSSCAN_CUDA(cudaGetLastError());
+    }
     bwd::chunk_adj_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
     const long long n_cb = (long long)a.B * a.D * N;
     bwd::chunk_combine_kernel<<<unsigned((n_cb + 255) / 256), 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
   }
-  if (TC > bwd::SEG) {   // some segments start inside a chunk: their checkpoints
+  if (!fwd_ckpt && TC > bwd::SEG) {   // some segments start inside a chunk: their checkpoints
     bwd::ckpt_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
   }

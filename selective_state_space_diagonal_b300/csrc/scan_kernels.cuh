@@ -69,7 +69,7 @@ struct Stage {
   static constexpr int DT_BYTES = DT_ROWS * DT * SIN;
   static constexpr int TAB_BYTES = TAB_ROWS * 4 * N * 4;
   static constexpr int AUX_BYTES = MODE == 1 ? AUX_ROWS * AUX_W * 4 : 0;
-  static constexpr int ROT_BYTES = 2 * N * 4;
+  static constexpr int ROT_BYTES = 4 * 2 * N * 4;       // e^{i Phi} after local steps 7, 15, 23, last
   static constexpr int OFF_X = 0;
   static constexpr int OFF_DT = align128(OFF_X + X_BYTES);
   static constexpr int OFF_TAB = align128(OFF_DT + DT_BYTES);
@@ -107,7 +107,8 @@ struct TableParams {
   float* tab;  // (B, L, N/2, 8): per state pair (Btr, Btr', Bti, Bti', Ctr, Ctr', -Cti, -Cti')
   float* aux;  // (B, L, 8): lam_t, lam_t, mu, mu, E_t, E_t, 0, 0 with mu = 1 - lam_{t+1}
                // (0 at t = L-1) (trapezoid only)
-  float* rot;  // (B, S, N, 2): e^{i Phi} at the last step of sub-chunk s
+  float* rot;  // (B, S, 4, N, 2): e^{i Phi} of sub-chunk s after its local steps 7, 15, 23 and
+               // after its last step (row r: local step min(8 r + 7, last))
   int B, L, N, S;
 };
 
@@ -126,10 +127,15 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
   const int t0 = s * T_SUB, t1 = min(t0 + T_SUB, p.L);
   const int q = n >> 1, odd = n & 1;
   float phi = 0.f, cs = 1.f, sn = 0.f;
+  float* rr = p.rot + ((int64_t(b) * p.S + s) * 4 * p.N + n) * 2;   // row r at rr + r * 2N
   for (int t = t0; t < t1; ++t) {
     const int64_t tn = (int64_t(b) * p.L + t) * p.N + n;
     phi += load_in<Tin>(th, tn);
     sincosf(phi, &sn, &cs);
+    if (((t - t0) & 7) == 7) {
+      rr[((t - t0) >> 3) * 2 * p.N] = cs;
+      rr[((t - t0) >> 3) * 2 * p.N + 1] = sn;
+    }
     const float br = load_in<Tin>(Bc, 2 * tn), bi = load_in<Tin>(Bc, 2 * tn + 1);
     const float cr = load_in<Tin>(Cc, 2 * tn), ci = load_in<Tin>(Cc, 2 * tn + 1);
     float* row = p.tab + (int64_t(b) * p.L + t) * (4 * p.N) + q * 8;
@@ -138,9 +144,12 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
     row[4 + odd] = cs * cr - sn * ci;    // Re(e^{+i Phi} Cc)
     row[6 + odd] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
   }
-  float* rr = p.rot + ((int64_t(b) * p.S + s) * p.N + n) * 2;
-  rr[0] = cs;
-  rr[1] = sn;
+  for (int r = 0; r < 4; ++r) {   // rows past the sub-chunk's last step hold the last step's value
+    if (8 * r + 7 > t1 - 1 - t0) {
+      rr[r * 2 * p.N] = cs;
+      rr[r * 2 * p.N + 1] = sn;
+    }
+  }
   if (MODE == 1 && n == 0) {
     const Tin* lam = static_cast<const Tin*>(p.lam);
     for (int t = t0; t < t1; ++t) {
@@ -165,7 +174,7 @@ struct ScanParams {
   CUtensorMap tm_dt;   // (D, L, B) input dtype, box (DT, T_SUB + 2, 1)
   CUtensorMap tm_tab;  // (4N, L, B) f32, box (4N, T_SUB + 1, 1)
   CUtensorMap tm_aux;  // (8, L, B) f32, box (8, T_SUB + 1, 1)
-  CUtensorMap tm_rot;  // (2N, S, B) f32, box (2N, 1, 1)
+  CUtensorMap tm_rot;  // (2N, 4S, B) f32, box (2N, 4, 1)
   const float* A;
   const float* Dskip;
   float* y;
@@ -184,6 +193,8 @@ struct ScanParams {
   int y_vec2;           // y is 8-byte aligned: store channel pairs as float2
   int silent_chunk;
   long long poll_limit;
+  float4* ckpt;         // checkpoint variant: (B, S8, D, N/2) state pairs before every 8-step segment
+  int S8;               // ceil(L / 8)
 };
 
 __device__ __forceinline__ bool flag_ready(uint32_t f, uint32_t epoch, uint32_t need) {
@@ -243,7 +254,9 @@ template <> struct PairLoad<uint16_t> {
 // CARRY (== p.carry) selects what is compiled in: CARRY_NONE (one chunk per row), CARRY_SERIAL
 // (each chunk waits for its predecessor's final state) or CARRY_DECOUPLED (aggregate pass,
 // then look-back); the lighter variants keep no registers for the heavier ones.
-template <int N, typename Tin, int MODE, int CARRY>
+// CKPT = true is the checkpoint variant for the backward pass: no y, and the true state
+// h_t = e^{i Phi_t} (k_{t+1} - p_{t+1} Bt_t) after every 8th step stored to p.ckpt.
+template <int N, typename Tin, int MODE, int CARRY, bool CKPT = false>
 __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant__ ScanParams p) {
   using TL = Tile<N>;
   using SG = Stage<N, Tin, MODE>;
@@ -334,7 +347,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
     tma_load_3d(base + SG::OFF_DT, &p.tm_dt, d0, sub * T_SUB, b, &full_bar[slot]);
     tma_load_3d(base + SG::OFF_TAB, &p.tm_tab, 0, sub * T_SUB, b, &full_bar[slot]);
     if (MODE == 1) tma_load_3d(base + SG::OFF_AUX, &p.tm_aux, 0, sub * T_SUB, b, &full_bar[slot]);
-    tma_load_3d(base + SG::OFF_ROT, &p.tm_rot, 0, sub, b, &full_bar[slot]);
+    tma_load_3d(base + SG::OFF_ROT, &p.tm_rot, 0, 4 * sub, b, &full_bar[slot]);
   };
   if (tid == 0) {
     for (int gs = 0; gs < min(NST, total_stages); ++gs) issue(gs);
@@ -403,6 +416,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   // trapezoid correction and the D-skip added, and the lanes with g < 2 store the result.
   const bool store_one = NG > 1 && g < 2 && dvalid;
   auto finish_y = [&](float2 yp, const StepIn& sc, float* yrow, bool ok) {
+    if (CKPT) return;
     if (NG == 1) {
       const float o0 = fmaf(Ds.x, sc.x.x, fmaf(-sc.pc.x, sc.E, yp.x));
       const float o1 = fmaf(Ds.y, sc.x.y, fmaf(-sc.pc.y, sc.E, yp.y));
@@ -503,14 +517,14 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
           ki[0][q] = fma2(rc[0][q], ki[0][q], mul2(cur.w0, bti));
           kr[1][q] = fma2(rc[1][q], kr[1][q], mul2(cur.w1, btr));
           ki[1][q] = fma2(rc[1][q], ki[1][q], mul2(cur.w1, bti));
-          if (WITH_Y) {
+          if (WITH_Y && !CKPT) {
             const float4 ct = cur.tb[2 * q + 1];
             const float2 ctr = f2(ct.x, ct.y), cti = f2(ct.z, ct.w);
             acc0 = fma2(cti, ki[0][q], fma2(ctr, kr[0][q], acc0));
             acc1 = fma2(cti, ki[1][q], fma2(ctr, kr[1][q], acc1));
           }
         }
-        if (WITH_Y) ypend = f2(acc0.x + acc0.y, acc1.x + acc1.y);
+        if (WITH_Y && !CKPT) ypend = f2(acc0.x + acc0.y, acc1.x + acc1.y);
       };
 
       StepIn sa, sb;
@@ -525,6 +539,30 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
         }
         sb = sa;
       }
+      // Checkpoint variant: after local step j = 8 r + 7 the state is k_{t+1} = g_t + p_{t+1} Bt_t
+      // in the frame of row r of the rotation table; h_t = e^{i Phi_t} (k - p Bt) is stored as
+      // the state before the segment that starts at t + 1.
+      auto store_ckpt = [&](int j, const StepIn& sc) {
+        const int t1 = t_sub0 + j + 1;
+        if (t1 >= p.L || !dvalid) return;
+        const float4* rrow = srot + (j >> 3) * (N / 2);
+#pragma unroll
+        for (int q = 0; q < NPAIR; ++q) {
+          const float4 rr = rrow[n0 / 2 + q];
+          const float2 cc = f2(rr.x, rr.z), ss = f2(rr.y, rr.w), nss = f2(-rr.y, -rr.w);
+          const float4 bt = sc.tb[2 * q];
+          const float2 btr = f2(bt.x, bt.y), bti = f2(bt.z, bt.w);
+#pragma unroll
+          for (int ch = 0; ch < CH; ++ch) {
+            const float pcv = ch ? sc.pc.y : sc.pc.x;
+            const float2 npc = f2(-pcv, -pcv);
+            const float2 ur = fma2(npc, btr, kr[ch][q]), ui = fma2(npc, bti, ki[ch][q]);
+            const float2 hr = fma2(cc, ur, mul2(nss, ui)), hi = fma2(cc, ui, mul2(ss, ur));
+            p.ckpt[((b * int64_t(p.S8) + t1 / 8) * D + chan(ch)) * (N / 2) + n0 / 2 + q] =
+                make_float4(hr.x, hi.x, hr.y, hi.y);
+          }
+        }
+      };
       int tt = 0;
       // 8 steps per trip: the shared-memory offsets of a trip are immediates and the loop
       // bookkeeping is paid once per 8 steps (measured 6 % faster than 2 steps per trip)
@@ -532,10 +570,12 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
       for (; tt + 1 < nt; tt += 2) {
         step(tt, sa, ra, sb, rb);
         step(tt + 1, sb, rb, sa, ra);
+        if (CKPT && WITH_Y && ((tt + 2) & 7) == 0) store_ckpt(tt + 1, sb);
       }
       // yrow now points at the row of the last step taken, whose output is still pending
       if (tt < nt) {
         step(tt, sa, ra, sb, rb);
+        if (CKPT && WITH_Y && ((tt + 1) & 7) == 0) store_ckpt(tt, sa);
         if (WITH_Y) finish_y(ypend, sa, yrow, true);
       } else if (WITH_Y) {
         finish_y(ypend, sb, yrow, true);
@@ -543,7 +583,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
       // frame reset: rotate the state by e^{i Phi_last} of this sub-chunk
 #pragma unroll
       for (int q = 0; q < NPAIR; ++q) {
-        const float4 rr = srot[n0 / 2 + q];
+        const float4 rr = srot[3 * (N / 2) + n0 / 2 + q];
         const float2 cc = f2(rr.x, rr.z), ss = f2(rr.y, rr.w), nss = f2(-rr.y, -rr.w);
 #pragma unroll
         for (int ch = 0; ch < CH; ++ch) {

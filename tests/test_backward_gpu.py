@@ -209,3 +209,21 @@ def test_backward_unchunked_row_rich():
         inp = wl.generate(w)
         dy = make_dy(w, seed=19 + mode)
         compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"unchunked m{mode}")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_backward_rows_the_tile_copies_cannot_take(mode):
+    """Rows of D * sizeof(dtype) bytes that are not a multiple of 16 (float32 D = 6, bf16 D = 12):
+    the checkpoints then come from the backward's own sequential pass instead of the scan
+    kernel's checkpoint variant; with few rows the sequence is also cut into time chunks."""
+    for dtype, D in (("f32", 6), ("bf16", 12)):
+        w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=2, L=77, D=D, N=8, mode=mode, dtype=dtype,
+                                                       seed=0x5EED2000 + D + mode)
+        inp = wl.generate(w)
+        dy = make_dy(w, seed=23 + D)
+        compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"rows{D}:{dtype}:m{mode}")
+    # many rows (one time chunk) with unaligned rows too
+    w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=64, L=19, D=1002, N=16, mode=mode, dtype="f32")
+    inp = wl.generate(w)
+    dy = make_dy(w, seed=29)
+    compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"rows1002:m{mode}")
