@@ -322,15 +322,18 @@ __global__ void __launch_bounds__(256, 3) ckpt_kernel(const Params p) {
   }
 }
 
-// Dynamic shared memory of grad_kernel: one segment's inputs, staged once per block.
+// Dynamic shared memory of grad_kernel: one segment's inputs (and, in the trapezoid mode, the
+// per-step products of them every lane of a channel needs), staged once per block.
 // Rows r = 0 .. SEG + 1 stand for steps t = ts - 1 + r (zeros outside 0 .. L-1 and past D).
 template <int N> struct GradStage {
   static constexpr int CB = GradTile<N>::CB;
   static constexpr int OFF_TD = 0;                                        // float4 [SEG+2][CB]: x, dt, dy
-  static constexpr int OFF_TN = OFF_TD + (SEG + 2) * CB * 16;             // float4 [SEG+1][N]: rot c, s, Bc re, im
+  // trapezoid only: per (t, d) products every lane of the channel needs, formed once
+  static constexpr int OFF_TQ = OFF_TD + (SEG + 2) * CB * 16;             // float4 [SEG+2][CB]: see below
+  static constexpr int OFF_TR = OFF_TQ + (SEG + 2) * CB * 16;             // float4 [SEG+2][CB]
+  static constexpr int OFF_TN = OFF_TR + (SEG + 2) * CB * 16;             // float4 [SEG+1][N]: rot c, s, Bc re, im
   static constexpr int OFF_CC = OFF_TN + (SEG + 1) * N * 16;              // float2 [SEG+1][N]: Cc re, im
-  static constexpr int OFF_LAM = OFF_CC + (SEG + 1) * N * 8;              // float [SEG+2]
-  static constexpr int BYTES = OFF_LAM + (SEG + 2) * 4;
+  static constexpr int BYTES = OFF_CC + (SEG + 1) * N * 8;
 };
 
 template <typename Tin, int MODE, int N>
@@ -346,11 +349,15 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
   __shared__ float s_dD[K][THREADS];
   __shared__ float s_acc[SEG][N][5];   // per (t, n): dBc re, im, dCc re, im, dtheta
   __shared__ float s_lam[SEG];
+  __shared__ float2 s_const[K][THREADS];   // per (slot, thread): A[d, n], Dskip[d]
   extern __shared__ __align__(16) unsigned char g_stage[];
   float4 (*s_td)[CB] = reinterpret_cast<float4 (*)[CB]>(g_stage + GS::OFF_TD);
+  // trapezoid: s_tq = (lam dt x, (1 - lam) dt, (1 - lam) dt x_{t-1}, lam dt),
+  //            s_tr = (lam x, (1 - lam) x_{t-1}, dt x, dt x_{t-1})
+  float4 (*s_tq)[CB] = reinterpret_cast<float4 (*)[CB]>(g_stage + GS::OFF_TQ);
+  float4 (*s_tr)[CB] = reinterpret_cast<float4 (*)[CB]>(g_stage + GS::OFF_TR);
   float4 (*s_tn)[N] = reinterpret_cast<float4 (*)[N]>(g_stage + GS::OFF_TN);
   float2 (*s_cc)[N] = reinterpret_cast<float2 (*)[N]>(g_stage + GS::OFF_CC);
-  float* s_lv = reinterpret_cast<float*>(g_stage + GS::OFF_LAM);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = lane % N, cl = lane / N;
@@ -389,6 +396,8 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
     }
     s_state[j][tid] = st;
     s_dD[j][tid] = 0.f;
+    const long long dc = d < p.D ? d : 0;
+    s_const[j][tid] = make_float2(p.A[dc * N + n], p.Dskip[dc]);
   }
   for (int k = tid; k < SEG * N * 5; k += THREADS) (&s_acc[0][0][0])[k] = 0.f;
   if (tid < SEG) s_lam[tid] = 0.f;
@@ -405,6 +414,16 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
       if (t >= 0 && t < L && d < D) {
         const long long td = (b * L + t) * D + d;
         v = make_float4(load_in<Tin>(X, td), load_in<Tin>(DT, td), p.dy[td], 0.f);
+        if (MODE == 1) {
+          const float lm = load_in<Tin>(LAM, b * L + t);
+          const float xp = t > 0 ? load_in<Tin>(X, td - D) : 0.f;
+          const float m = (1.f - lm) * v.y;
+          s_tq[r][c] = make_float4(lm * v.y * v.x, m, m * xp, lm * v.y);
+          s_tr[r][c] = make_float4(lm * v.x, (1.f - lm) * xp, v.y * v.x, v.y * xp);
+        }
+      } else if (MODE == 1) {
+        s_tq[r][c] = v;
+        s_tr[r][c] = v;
       }
       s_td[r][c] = v;
     }
@@ -421,10 +440,6 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
       }
       s_tn[r][nn] = v;
       s_cc[r][nn] = c;
-    }
-    if (tid < SEG + 2) {
-      const long long t = ts - 1 + tid;
-      s_lv[tid] = (MODE == 1 && t >= 0 && t < L) ? load_in<Tin>(LAM, b * L + t) : 0.f;
     }
     __syncthreads();
 
@@ -445,9 +460,10 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
       const bool valid = d < p.D;
       const long long dd = valid ? d : 0;
       // an absent channel was staged with x = dt = dy = 0: every contribution is exactly zero
-      const float Ad = p.A[dd * N + n];
+      const float2 cst = s_const[j][tid];
+      const float Ad = cst.x;
       const float a2 = Ad * LOG2E;
-      const float Ds = p.Dskip[dd];
+      const float Ds = cst.y;
       float4 st = s_state[j][tid];
       float cgr = st.x, cgi = st.y, Rn = st.z, dA_acc = st.w;
       float dD_acc = s_dD[j][tid];
@@ -484,9 +500,9 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
               ur = w * q.z;
               ui = w * q.w;
             } else {
-              const float lm = s_lv[i + 1];
               const float4 qp = s_tn[i][n];
-              const float w = lm * dtt * xt, c2 = (1.f - lm) * dtt * s_td[i][cb].x;
+              const float4 q2 = s_tq[i + 1][cb];
+              const float w = q2.x, c2 = q2.z;   // lam dt x, (1 - lam) dt x_{t-1}
               ur = w * q.z + c2 * (ar * qp.z - ai * qp.w);
               ui = w * q.w + c2 * (ar * qp.w + ai * qp.z);
             }
@@ -503,7 +519,7 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
       // ---- backward through the segment
       float g3[3][SEG];   // per t: dx, ddt, dlam partial sums over this lane's state
       // (1 - lam_{t+1}) dt_{t+1}: the next step's beta weight (zero past the end)
-      float mnext = MODE == 1 ? (1.f - s_lv[nt + 1]) * s_td[nt + 1][cb].y : 0.f;
+      float mnext = MODE == 1 ? s_tq[nt + 1][cb].y : 0.f;
 #pragma unroll
       for (int i = SEG - 1; i >= 0; --i) {
         g3[0][i] = 0.f;
@@ -538,24 +554,23 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
             gx = dtt * P;
             gdt = xt * P;
           } else {
-            const float lm = s_lv[i + 1];
-            const float coef = lm * dtt * xt;
+            const float4 q2 = s_tq[i + 1][cb];   // lam dt x, (1 - lam) dt, (1 - lam) dt x_{t-1}, lam dt
+            const float4 q3 = s_tr[i + 1][cb];   // lam x, (1 - lam) x_{t-1}, dt x, dt x_{t-1}
             const float cn = mnext * xt;   // beta_{t+1} reaches Bc_t through conj(a_{t+1}) ghat_{t+1}
-            acc[i][0] += coef * gr + cn * cgr;
-            acc[i][1] += coef * gi + cn * cgi;
+            acc[i][0] += q2.x * gr + cn * cgr;
+            acc[i][1] += q2.x * gi + cn * cgi;
             // step t-1 (zeros before the sequence)
-            const float xp = s_td[i][cb].x;
             const float4 qp = s_tn[i][n];
             const float bpr = qp.z, bpi = qp.w;
-            const float c2 = (1.f - lm) * dtt * xp;
+            const float c2 = q2.z;
             const float vr = ar * bpr - ai * bpi, vi = ar * bpi + ai * bpr;   // a_t Bc_{t-1}
             R = vr * gr + vi * gi;
             Gar += c2 * (gr * bpr + gi * bpi);
             Gai += c2 * (gi * bpr - gr * bpi);
-            gx = lm * dtt * P + mnext * Rn;
-            gdt = lm * xt * P + (1.f - lm) * xp * R;
-            glam = dtt * (xt * P - xp * R);
-            mnext = (1.f - lm) * dtt;
+            gx = fmaf(q2.w, P, mnext * Rn);
+            gdt = fmaf(q3.x, P, q3.y * R);
+            glam = fmaf(q3.z, P, -q3.w * R);
+            mnext = q2.y;
           }
           // exponential: G(z) = conj(a) G(a)
           const float Gzr = ar * Gar + ai * Gai;
