@@ -214,7 +214,9 @@ int csscan_forward_mimo(const void* x, const void* delta, const float* A, const 
  *   dx, ddelta : (B, L, D)          dA : (D, N)          dDskip : (D)
  *   dBc, dCc   : (B, L, N, 2), (d/dRe, d/dIm) of each complex entry
  *   dtheta     : (B, L, N)          dlambda : (B, L), trapezoid mode only (may be NULL in exp-Euler mode)
- * Inputs need only their element alignment (no 16-byte rule). N must be 2, 4, 8, 16 or 32
+ * Inputs need their element alignment, Bc and Cc that of one complex entry (no 16-byte rule;
+ * inputs that also meet csscan_forward's 16-byte rule let the library take the checkpoints from
+ * the scan kernel, otherwise from a slower pass of its own). N must be 2, 4, 8, 16 or 32
  * (CSSCAN_ERR_UNSUPPORTED otherwise) and B <= 65535. The library grows its per-stream
  * workspace to B*L*N*8 + B*ceil(L/8)*D*N*8 bytes (rotation table and checkpoints). Sums over
  * rows use float32 atomic adds, so the summed gradients (dA, dBc, dCc, dtheta, dlambda,

@@ -236,16 +236,22 @@ __global__ void __launch_bounds__(256) chunk_adj_kernel(const Params p) {
   for (int t1 = te - 1; t1 >= tc; t1 -= SEG) {   // groups of SEG steps, last to first
     float dys[SEG], ccr[SEG], cci[SEG], ds[SEG];
     float2 ros[SEG];
+    // one 64-bit base per array for the group (step t1); steps before tc repeat tc
+    const long long bt = b * p.L + t1;
+    const float* dyg = p.dy + bt * p.D + th.d;
+    const Tin* dg = DT + bt * p.D + th.d;
+    const Tin* cg = CC + 2 * (bt * p.N + th.n);
+    const float2* rg = p.rot + bt * p.N + th.n;
+    const int first = t1 - tc;
 #pragma unroll
     for (int i = 0; i < SEG; ++i) {
-      const int t = max(t1 - i, tc);
-      const long long td = (b * p.L + t) * p.D + th.d;
-      const long long tn = (b * p.L + t) * p.N + th.n;
-      dys[i] = p.dy[td];
-      ccr[i] = load_in<Tin>(CC, 2 * tn);
-      cci[i] = load_in<Tin>(CC, 2 * tn + 1);
-      ds[i] = load_in<Tin>(DT, td);
-      ros[i] = p.rot[tn];
+      const int ii = min(i, first);   // t = t1 - ii
+      dys[i] = dyg[-ii * p.D];
+      const float2 cc = load_pair<Tin>(cg, -ii * p.N);
+      ccr[i] = cc.x;
+      cci[i] = cc.y;
+      ds[i] = load_in<Tin>(dg, -ii * p.D);
+      ros[i] = rg[-ii * p.N];
     }
 #pragma unroll
     for (int i = 0; i < SEG; ++i) {

@@ -851,7 +851,8 @@ int backward_impl(const BwdArgs& a, cudaStream_t st) {
       a.B * a.L * a.D > (int64_t(1) << 40) || (a.D + 63) / 64 > 65535)
     return CSSCAN_ERR_UNSUPPORTED;
   const size_t s = a.dtype == CSSCAN_F32 ? 4 : 2;
-  if (!aligned(a.x, s) || !aligned(a.delta, s) || !aligned(a.Bc, s) || !aligned(a.Cc, s) || !aligned(a.theta, s) ||
+  // Bc and Cc are read one complex entry (2 values) at a time
+  if (!aligned(a.x, s) || !aligned(a.delta, s) || !aligned(a.Bc, 2 * s) || !aligned(a.Cc, 2 * s) || !aligned(a.theta, s) ||
       (a.lam && !aligned(a.lam, s)) || !aligned(a.A, 4) || !aligned(a.Dskip, 4) || !aligned(a.dy, 4) ||
       !aligned(a.dx, 4) || !aligned(a.ddelta, 4) || !aligned(a.dA, 4) || !aligned(a.dBc, 4) || !aligned(a.dCc, 4) ||
       !aligned(a.dtheta, 4) || (a.dlam && !aligned(a.dlam, 4)) || !aligned(a.dDskip, 4))

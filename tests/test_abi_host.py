@@ -111,6 +111,9 @@ def test_backward_rejects_bad_arguments_on_host(lib):
     assert bw(*args(mode=3)) == csscan.CSSCAN_ERR_INVALID_ARG
     assert bw(*args(dx=A16 + 2)) == csscan.CSSCAN_ERR_MISALIGNED
     assert bw(*args(x=A16 + 1, dtype=1)) == csscan.CSSCAN_ERR_MISALIGNED
+    cargs = args(dtype=1)
+    cargs[3] = A16 + 2    # Bc: one bf16 element off a complex entry
+    assert bw(*cargs) == csscan.CSSCAN_ERR_MISALIGNED
 
 
 def test_mimo_rejects_bad_arguments_on_host(lib):
