@@ -369,14 +369,14 @@ def run_ours(args):
 
     # end to end through the public API: pinned host inputs -> device, scan, y -> host, every
     # byte of every step inside the timed region. The batch is cut into pieces of whole rows on
-    # two streams, as a streaming caller would, so that one piece's upload, another's scan and
+    # three streams, as a streaming caller would, so that one piece's upload, another's scan and
     # a third's download overlap (each piece is one csscan_forward call).
     e2e_steps = max(1, args.e2e_steps)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = y.numel() * 4
-    n_pieces = max(1, min(w.B, 4))
+    n_pieces = max(1, min(w.B, 8))
     bounds = [(w.B * i // n_pieces, w.B * (i + 1) // n_pieces) for i in range(n_pieces)]
-    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    streams = [torch.cuda.Stream() for _ in range(3)]
     shared_done = torch.cuda.Event()
     per_row = ("x", "delta", "Bc", "Cc", "theta", "lam")
 
@@ -387,7 +387,7 @@ def run_ours(args):
             dev["Dskip"].copy_(host["Dskip"], non_blocking=True)
             shared_done.record(s0)
         for i, (b0, b1) in enumerate(bounds):
-            s = streams[i % 2]
+            s = streams[i % len(streams)]
             with torch.cuda.stream(s):
                 s.wait_event(shared_done)
                 for k in per_row:
@@ -445,7 +445,7 @@ def run_ours(args):
             "dtype": "f32", "data": "synthetic", "config": workload_config(w, l2_note),
             "roofline": roofline, "hbm": hbm, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps, "pieces": n_pieces, "streams": 2},
+                    "steps": e2e_steps, "pieces": n_pieces, "streams": len(streams)},
             "gpu_launches": launches_per_step(w) * K, "clocks": clk}
     if bwd is not None:
         ms = bwd.pop("ms")

@@ -193,7 +193,7 @@ int csscan_decode_step(const void* x, const void* delta, const float* A, const v
  *   A       : device float32 (H, N)            Dskip : device float32 (H, P)
  *   y       : device float32 (B, L, H, P), written in full
  *   mode    : CSSCAN_MODE_EXP_EULER or CSSCAN_MODE_EXP_TRAPEZOID (ZOH: CSSCAN_ERR_UNSUPPORTED)
- * N must be 2, 4, 8, 16 or 32 and P 1, 2, 4 or 8 (CSSCAN_ERR_UNSUPPORTED otherwise). Pointers
+ * N must be 2, 4, 8, 16 or 32, P 1, 2, 4 or 8 and B <= 65535 (CSSCAN_ERR_UNSUPPORTED otherwise). Pointers
  * need their element alignment, Bm and Cm that of one complex entry. Starts from the zero
  * state. Uses the per-stream workspace like csscan_forward.
  */

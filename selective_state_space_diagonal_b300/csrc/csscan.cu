@@ -597,6 +597,7 @@ int launch_mimo(const MimoArgs& a, cudaStream_t st) {
   const int64_t rows = a.B * a.H * N;
   const int64_t target = int64_t(nsm) * SEQ_THREADS_PER_SM / P;
   int64_t C = std::min<int64_t>(S, std::max<int64_t>(1, (target + rows - 1) / rows));
+  if (C > 65535) C = 65535;   // the output pass has one grid row per chunk
   const int64_t TC = (S + C - 1) / C * G;
   C = (a.L + TC - 1) / TC;
   const size_t rot_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float2), 256);
@@ -634,7 +635,9 @@ int launch_mimo(const MimoArgs& a, cudaStream_t st) {
     mimo::mimo_combine_kernel<<<unsigned((rows + 255) / 256), 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
   }
-  mimo::mimo_out_kernel<Tin, MODE, N, P><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
+  constexpr int HB = mimo::MimoStage<N, P>::HB;
+  const dim3 ogrid{unsigned((a.H + HB - 1) / HB), unsigned(C), unsigned(a.B)};
+  mimo::mimo_out_kernel<Tin, MODE, N, P><<<ogrid, 256, 0, st>>>(p);
   CSSCAN_CUDA(cudaGetLastError());
   return CSSCAN_OK;
 }
@@ -675,7 +678,7 @@ int mimo_impl(const MimoArgs& a, cudaStream_t st) {
   if (rows && a.mode == CSSCAN_MODE_EXP_TRAPEZOID && !a.lam) return CSSCAN_ERR_INVALID_ARG;
   if (a.N != 2 && a.N != 4 && a.N != 8 && a.N != 16 && a.N != 32) return CSSCAN_ERR_UNSUPPORTED;
   if (a.P != 1 && a.P != 2 && a.P != 4 && a.P != 8) return CSSCAN_ERR_UNSUPPORTED;
-  if (a.B > (int64_t(1) << 31) - 1 || a.L > (int64_t(1) << 30) || a.H > (int64_t(1) << 30) ||
+  if (a.B > 65535 || a.L > (int64_t(1) << 30) || a.H > (int64_t(1) << 30) ||
       a.B * a.L * a.H * a.P > (int64_t(1) << 40))
     return CSSCAN_ERR_UNSUPPORTED;
   const size_t s = a.dtype == CSSCAN_F32 ? 4 : 2;

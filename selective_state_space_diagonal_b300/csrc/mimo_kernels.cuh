@@ -13,9 +13,11 @@
 //   mimo_chunk_kernel   per (b, c, h, n): the chunk's end state from a zero entry state and
 //                       the product of a over the chunk                     (chunks > 1 only)
 //   mimo_combine_kernel per (b, h, n): each chunk's entry state
-//   mimo_out_kernel     per (b, c, h, n): the recurrence over the chunk with y; each lane keeps
-//                       its P partial outputs for 8 steps and a reduce-scatter over the
-//                       head's N lanes leaves every (step, channel) sum in one lane
+//   mimo_out_kernel     blocks of 256 / N heads of one (b, c), a thread per (head, n): the
+//                       recurrence over the chunk with y, each 8-step group's shared inputs
+//                       staged in shared memory first; each lane keeps its P partial outputs
+//                       for the group and a reduce-scatter over the head's N lanes leaves
+//                       every (step, channel) sum in one lane
 #pragma once
 
 #include "device_util.cuh"
@@ -164,63 +166,144 @@ __global__ void __launch_bounds__(256) mimo_combine_kernel(const Params p) {
   }
 }
 
-// The recurrence over chunk c with y. Lanes n = 0 .. N-1 of one (b, c, h) are neighbours in a
-// warp (N <= 32); every lane of a warp runs the same number of groups (the shuffles span the
-// warp) and a lane past its chunk's end (or past the problem) adds zeros and stores nothing.
+// The recurrence over chunk c with y. A block owns HB = 256 / N heads of one (b, c): thread
+// (head hl, state n), the N lanes of a head neighbours in a warp (N <= 32). For each group of
+// GROUP steps the block first stages, coalesced, what its lanes share -- e^{i theta}, Bm and Cm
+// per (t, n), x and dt per (t, head), lam per t -- in shared memory. Each lane then keeps its P
+// partial outputs for the group and a reduce-scatter over the head's N lanes leaves every
+// (step, channel) sum in one lane. Grid: (ceil(H / HB), C, B).
+template <int N, int P> struct MimoStage {
+  static constexpr int HB = 256 / N;                       // heads per block
+  static constexpr int TN = GROUP * N;                     // (t, n) entries of a group
+  static constexpr int TH = GROUP * HB;                    // (t, head) entries of a group
+  static constexpr int OFF_ROT = 0;                        // float2 [GROUP][N]
+  static constexpr int OFF_BM = OFF_ROT + TN * 8;          // float2 [GROUP][N][P]
+  static constexpr int OFF_CM = OFF_BM + TN * P * 8;       // float2 [GROUP][N][P]
+  static constexpr int OFF_X = OFF_CM + TN * P * 8;        // float [GROUP][HB][P]
+  static constexpr int OFF_DT = OFF_X + TH * P * 4;        // float [GROUP][HB]
+  static constexpr int OFF_LAM = OFF_DT + TH * 4;          // float [GROUP]
+  static constexpr int BYTES = OFF_LAM + GROUP * 4;
+};
+
 template <typename Tin, int MODE, int N, int P>
 __global__ void __launch_bounds__(256) mimo_out_kernel(const Params p) {
+  using MS = MimoStage<N, P>;
+  constexpr int HB = MS::HB;
   constexpr int E = GROUP * P;                   // (step, channel) entries of one group
   constexpr int HOLD = E >= N ? E / N : 1;
   constexpr int DUP = N > E ? N / E : 1;
-  const Thread th = thread_of(p);
-  const long long b = th.b;
-  const int h = th.h, n = th.n;
-  const float a2 = p.A[(long long)h * N + n] * LOG2E;
+  __shared__ __align__(16) unsigned char sm[MS::BYTES];
+  float2 (*s_rot)[N] = reinterpret_cast<float2 (*)[N]>(sm + MS::OFF_ROT);
+  float2 (*s_bm)[N][P] = reinterpret_cast<float2 (*)[N][P]>(sm + MS::OFF_BM);
+  float2 (*s_cm)[N][P] = reinterpret_cast<float2 (*)[N][P]>(sm + MS::OFF_CM);
+  float (*s_x)[HB][P] = reinterpret_cast<float (*)[HB][P]>(sm + MS::OFF_X);
+  float (*s_dt)[HB] = reinterpret_cast<float (*)[HB]>(sm + MS::OFF_DT);
+  float* s_lam = reinterpret_cast<float*>(sm + MS::OFF_LAM);
+
+  const int tid = threadIdx.x;
+  const int n = tid % N, hl = tid / N;
+  const int h0 = blockIdx.x * HB;
+  const int h = h0 + hl;
+  const bool valid = h < p.H;
+  const int hc = valid ? h : 0;
+  const int c = blockIdx.y;
+  const long long b = blockIdx.z;
+  const Tin* X = static_cast<const Tin*>(p.x);
+  const Tin* DT = static_cast<const Tin*>(p.dt);
+  const Tin* BM = static_cast<const Tin*>(p.Bm);
+  const Tin* CM = static_cast<const Tin*>(p.Cm);
+  const Tin* LAM = static_cast<const Tin*>(p.lam);
+  const float a2 = p.A[(long long)hc * N + n] * LOG2E;
   float Ds[P];
 #pragma unroll
-  for (int q = 0; q < P; ++q) Ds[q] = p.Dskip[(long long)h * P + q];
-  const Tin* CM = static_cast<const Tin*>(p.Cm);
-  const int tc = th.c * p.TC;
-  const int te = th.ok ? min(p.L, tc + p.TC) : tc;
-  const int ngroups = (p.TC + GROUP - 1) / GROUP;
+  for (int q = 0; q < P; ++q) Ds[q] = p.Dskip[(long long)hc * P + q];
+  const int tc = c * p.TC, te = min(p.L, tc + p.TC);
   float hr = 0.f, hi = 0.f;
-  if (p.C > 1 && th.ok) {
-    const float2 h0 = rec_of(p, b, th.c, h, n)[0];
-    hr = h0.x;
-    hi = h0.y;
+  if (p.C > 1 && valid) {
+    const float2 hin = rec_of(p, b, c, h, n)[0];
+    hr = hin.x;
+    hi = hin.y;
   }
-  float2 vp = th.ok ? v_before<Tin, MODE, P>(p, b, tc, h, n) : make_float2(0.f, 0.f);
-  for (int gi = 0; gi < ngroups; ++gi) {
-    const int t0 = tc + gi * GROUP;
+  float2 vp = valid ? v_before<Tin, MODE, P>(p, b, tc, hc, n) : make_float2(0.f, 0.f);
+  for (int t0 = tc; t0 < te; t0 += GROUP) {
+    const int ng = min(GROUP, te - t0);
+    // ---- stage the group (steps past te or heads past H as zeros)
+    for (int k = tid; k < GROUP * N * P; k += 256) {
+      const int i = k / (N * P), r = k % (N * P);
+      float2 bb = make_float2(0.f, 0.f), cc = make_float2(0.f, 0.f);
+      if (i < ng) {
+        const long long e = ((b * p.L + t0 + i) * N) * P + r;   // entry (t, n, q), n * P + q = r
+        bb = load_pair<Tin>(BM, e);
+        cc = load_pair<Tin>(CM, e);
+      }
+      (&s_bm[0][0][0])[k] = bb;
+      (&s_cm[0][0][0])[k] = cc;
+    }
+    for (int k = tid; k < GROUP * N; k += 256) {
+      const int i = k / N, nn = k % N;
+      s_rot[i][nn] = i < ng ? p.rot[(b * p.L + t0 + i) * N + nn] : make_float2(0.f, 0.f);
+    }
+    for (int k = tid; k < GROUP * HB * P; k += 256) {
+      const int i = k / (HB * P), r = k % (HB * P), hh = h0 + r / P;
+      (&s_x[0][0][0])[k] = (i < ng && hh < p.H) ? load_in<Tin>(X, ((b * p.L + t0 + i) * p.H + h0) * P + r) : 0.f;
+    }
+    for (int k = tid; k < GROUP * HB; k += 256) {
+      const int i = k / HB, r = k % HB;
+      s_dt[i][r] = (i < ng && h0 + r < p.H) ? load_in<Tin>(DT, (b * p.L + t0 + i) * p.H + h0 + r) : 0.f;
+    }
+    if (MODE == 1 && tid < GROUP) s_lam[tid] = tid < ng ? load_in<Tin>(LAM, b * p.L + t0 + tid) : 0.f;
+    __syncthreads();
+
     float part[1][E];
 #pragma unroll
     for (int i = 0; i < GROUP; ++i) {
-      const int t = t0 + i;
 #pragma unroll
       for (int q = 0; q < P; ++q) part[0][i * P + q] = 0.f;
-      if (t < te) {
-        float xs[P];
-        const float2 v = inject<Tin, P>(p, b, t, h, n, xs);
-        float ar, ai;
-        mimo_step<Tin, MODE>(p, b, t, h, n, a2, v, vp, hr, hi, ar, ai);
-        const long long tn = ((b * p.L + t) * p.N + n) * P;
+      if (i < ng) {
+        float vr = 0.f, vi = 0.f;
 #pragma unroll
         for (int q = 0; q < P; ++q) {
-          const float2 cc = load_pair<Tin>(CM, tn + q);
+          const float2 bb = s_bm[i][n][q];
+          vr = fmaf(bb.x, s_x[i][hl][q], vr);
+          vi = fmaf(bb.y, s_x[i][hl][q], vi);
+        }
+        const float dtt = s_dt[i][hl];
+        const float2 ro = s_rot[i][n];
+        const float r = ex2_approx(dtt * a2);
+        const float ar = r * ro.x, ai = r * ro.y;
+        float ur, ui;
+        if (MODE == 0) {
+          ur = dtt * vr;
+          ui = dtt * vi;
+        } else {
+          const float lm = s_lam[i];
+          const float c1 = lm * dtt, c2 = (1.f - lm) * dtt;
+          ur = c1 * vr + c2 * (ar * vp.x - ai * vp.y);
+          ui = c1 * vi + c2 * (ar * vp.y + ai * vp.x);
+          vp = make_float2(vr, vi);
+        }
+        const float nr = fmaf(ar, hr, fmaf(-ai, hi, ur));
+        const float ni = fmaf(ar, hi, fmaf(ai, hr, ui));
+        hr = nr;
+        hi = ni;
+#pragma unroll
+        for (int q = 0; q < P; ++q) {
+          const float2 cc = s_cm[i][n][q];
           float o = cc.x * hr - cc.y * hi;
-          if (n == 0) o = fmaf(Ds[q], xs[q], o);
+          if (n == 0) o = fmaf(Ds[q], s_x[i][hl][q], o);
           part[0][i * P + q] = o;
         }
       }
     }
     const int base = butterfly<N, 1, E>(part, n);
-    if ((n % DUP) == 0) {
+    if ((n % DUP) == 0 && valid) {
 #pragma unroll
       for (int k = 0; k < HOLD; ++k) {
-        const int e = base + k, t = t0 + e / P, q = e % P;
-        if (t < te) p.y[((b * p.L + t) * p.H + h) * P + q] = part[0][k];
+        const int e = base + k, i = e / P, q = e % P;
+        if (i < ng) p.y[((b * p.L + t0 + i) * p.H + h) * P + q] = part[0][k];
       }
     }
+    __syncthreads();
   }
 }
 
