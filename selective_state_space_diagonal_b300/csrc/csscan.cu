@@ -66,6 +66,8 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType type, const void* base, uint64
 }
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+// A 1-D launch of `threads` threads in blocks of 256 stays within the grid's x limit.
+bool grid_fits(long long threads) { return (threads + 255) / 256 <= 0x7fffffffLL; }
 constexpr size_t HDR_BYTES = 256;
 
 // ----------------------------------------------------------------------------- arguments
@@ -293,6 +295,7 @@ int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* 
   sp.S8 = int(S8);
 
   const int64_t table_threads = a.B * S * N;
+  if (!grid_fits(table_threads)) return CSSCAN_ERR_UNSUPPORTED;
   table_kernel<Tin, MODE><<<unsigned((table_threads + 255) / 256), 256, 0, st>>>(tp);
   CSSCAN_CUDA(cudaGetLastError());
   if (o.scan_begin) CSSCAN_CUDA(cudaEventRecord(o.scan_begin, st));
@@ -445,11 +448,12 @@ int launch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
   p.TC = int(TC);
   p.C = int(C);
   const long long n_tab = (long long)a.B * a.L * N;
+  const long long n_thr = (long long)a.B * C * a.D * N;
+  if (!grid_fits(n_tab) || !grid_fits(n_thr)) return CSSCAN_ERR_UNSUPPORTED;
   zoh::zoh_table_kernel<Tin><<<unsigned((n_tab + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float4*>(rest),
                                                                             n_tab);
   CSSCAN_CUDA(cudaGetLastError());
   if (o.scan_begin) CSSCAN_CUDA(cudaEventRecord(o.scan_begin, st));
-  const long long n_thr = (long long)a.B * C * a.D * N;
   if (C > 1) {
     zoh::zoh_chunk_kernel<Tin><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
@@ -625,10 +629,11 @@ int launch_mimo(const MimoArgs& a, cudaStream_t st) {
   p.TC = int(TC);
   p.C = int(C);
   const long long n_rot = (long long)a.B * a.L * N;
+  const long long n_thr = (long long)a.B * C * a.H * N;
+  if (!grid_fits(n_rot) || !grid_fits(n_thr)) return CSSCAN_ERR_UNSUPPORTED;
   mimo::mimo_rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest),
                                                                            n_rot);
   CSSCAN_CUDA(cudaGetLastError());
-  const long long n_thr = (long long)a.B * C * a.H * N;
   if (C > 1) {
     mimo::mimo_chunk_kernel<Tin, MODE, P><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
@@ -783,6 +788,7 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
   p.C = int(C);
   p.fwd_ckpt = fwd_ckpt ? 1 : 0;
 
+  if (!grid_fits((long long)a.B * a.L * N) || !grid_fits((long long)a.B * C * a.D * N)) return CSSCAN_ERR_UNSUPPORTED;
   if (fwd_ckpt) {   // every checkpoint, chunk entries included, from the scan kernel
     uint32_t* hdr = static_cast<uint32_t*>(ws.base);
     rc = enqueue<N, Tin, MODE, true>(fa, default_options(), fpl, hdr,
