@@ -423,6 +423,7 @@ int launch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
   const int64_t rows = a.B * a.D * N;
   const int64_t target = int64_t(nsm) * SEQ_THREADS_PER_SM;
   int64_t C = std::min<int64_t>(S, std::max<int64_t>(1, (target + rows - 1) / rows));
+  if (C > 65535) C = 65535;   // the output pass has one grid row per chunk
   const int64_t TC = (S + C - 1) / C * G;
   C = (a.L + TC - 1) / TC;
   const size_t tab_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float4), 256);
@@ -460,7 +461,9 @@ int launch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
     zoh::zoh_combine_kernel<<<unsigned((rows + 255) / 256), 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
   }
-  zoh::zoh_out_kernel<Tin, N><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
+  constexpr int CBZ = 256 / N;
+  const dim3 ogrid{unsigned((a.D + CBZ - 1) / CBZ), unsigned(C), unsigned(a.B)};
+  zoh::zoh_out_kernel<Tin, N><<<ogrid, 256, 0, st>>>(p);
   CSSCAN_CUDA(cudaGetLastError());
   if (o.scan_end) CSSCAN_CUDA(cudaEventRecord(o.scan_end, st));
   return CSSCAN_OK;
@@ -487,7 +490,7 @@ int forward_impl(const Args& a, const csscan_options_t* opts, cudaStream_t st) {
     a0.mode = CSSCAN_MODE_EXP_EULER;   // same pointer, size and alignment rules
     int rc = validate(a0, o);
     if (rc != CSSCAN_OK) return rc;
-    if (a.N > 32) return CSSCAN_ERR_UNSUPPORTED;
+    if (a.N > 32 || a.B > 65535) return CSSCAN_ERR_UNSUPPORTED;
     const size_t pair = a.dtype == CSSCAN_F32 ? 8 : 4;   // Bc, Cc are read one complex entry at a time
     if (!aligned(a.Bc, pair) || !aligned(a.Cc, pair)) return CSSCAN_ERR_MISALIGNED;
     if (a.B == 0 || a.L == 0 || a.D == 0) return CSSCAN_OK;

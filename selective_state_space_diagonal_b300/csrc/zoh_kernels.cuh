@@ -11,8 +11,10 @@
 //   zoh_chunk_kernel   per (b, c, d, n): state at the chunk's end from a zero entry state and
 //                      the product of a over the chunk  (only when the rows leave few threads)
 //   zoh_combine_kernel per (b, d, n): walks the chunks for each chunk's entry state
-//   zoh_out_kernel     per (b, c, d, n): the recurrence over the chunk from its entry state;
-//                      the N lanes of a channel sum Re(Cc h) with shuffles and one stores y
+//   zoh_out_kernel     blocks of 256 / N channels of one (b, c), a thread per (channel, n): the
+//                      recurrence over the chunk from its entry state, each 8-step group's
+//                      shared inputs staged in shared memory first; the N lanes of a channel
+//                      sum Re(Cc h) with a reduce-scatter and one stores y
 // gamma is evaluated without cancellation: e^z - 1 = expm1(dt A) e^{i theta} + (e^{i theta} - 1)
 // with cos theta - 1 = -2 sin^2(theta / 2), then divided by z.
 #pragma once
@@ -174,59 +176,89 @@ __global__ void __launch_bounds__(256) zoh_combine_kernel(const Params p) {
   }
 }
 
-// The recurrence over chunk c from its entry state, with y. Lanes n = 0 .. N-1 of one (b, c, d)
-// are neighbours in a warp (N <= 32). Each lane keeps its Re(Cc h) for a group of GROUP steps
-// (lane 0 adds Dskip x); a reduce-scatter over the N lanes then leaves each step's sum in
-// one lane, which stores it.
+// The recurrence over chunk c from its entry state, with y. A block owns CBZ = 256 / N channels
+// of one (b, c): thread (channel dl, state n), the N lanes of a channel neighbours in a warp
+// (N <= 32). For each group of GROUP steps the block first stages, coalesced, what its lanes
+// share -- the (cos, sin, theta, cos - 1) row, Bc and Cc per (t, n), x and dt per (t, channel)
+// -- in shared memory. Each lane keeps its Re(Cc h) for the group (lane 0 adds Dskip x); a
+// reduce-scatter over the N lanes then leaves each step's sum in one lane, which stores it.
+// Grid: (ceil(D / CBZ), C, B).
 template <typename Tin, int N>
 __global__ void __launch_bounds__(256) zoh_out_kernel(const Params p) {
+  constexpr int CBZ = 256 / N;
   constexpr int HOLD = GROUP >= N ? GROUP / N : 1;
   constexpr int DUP = N > GROUP ? N / GROUP : 1;
-  const Thread th = thread_of(p);
-  const long long b = th.b;
-  const int d = th.d, n = th.n;
-  const float Adn = p.A[(long long)d * N + n];
-  const float Ds = p.Dskip[d];
-  const int tc = th.c * p.TC;
-  // every lane of a warp runs the same number of groups (the shuffles span the warp); the
-  // chunks of one warp's lanes can differ, so a lane past its chunk's end (or past the
-  // problem) computes on clamped steps and stores nothing
-  const int te = th.ok ? min(p.L, tc + p.TC) : tc;
-  const int ngroups = (p.TC + GROUP - 1) / GROUP;
+  __shared__ float4 s_tab[GROUP][N];
+  __shared__ float4 s_bc[GROUP][N];      // Bc re, im, Cc re, im
+  __shared__ float2 s_xd[GROUP][CBZ];    // x, dt
+  const int tid = threadIdx.x;
+  const int n = tid % N, dl = tid / N;
+  const int d0 = blockIdx.x * CBZ;
+  const int d = d0 + dl;
+  const bool valid = d < p.D;
+  const int dc = valid ? d : 0;
+  const int c = blockIdx.y;
+  const long long b = blockIdx.z;
+  const Tin* X = static_cast<const Tin*>(p.x);
+  const Tin* DT = static_cast<const Tin*>(p.dt);
+  const Tin* BC = static_cast<const Tin*>(p.Bc);
+  const Tin* CC = static_cast<const Tin*>(p.Cc);
+  const float Adn = p.A[(long long)dc * N + n];
+  const float Ds = p.Dskip[dc];
+  const int tc = c * p.TC, te = min(p.L, tc + p.TC);
   float hr = 0.f, hi = 0.f;
-  if (p.C > 1 && th.ok) {
-    const float2 h0 = rec_of(p, b, th.c, d, n)[0];
+  if (p.C > 1 && valid) {
+    const float2 h0 = rec_of(p, b, c, d, n)[0];
     hr = h0.x;
     hi = h0.y;
   }
-  for (int gi = 0; gi < ngroups; ++gi) {
-    const int t0 = tc + gi * GROUP;
-    float part[1][GROUP];
-    if (t0 < te) {
-      Group<Tin> g;
-      g.load(p, b, d, n, t0, te, true);
-#pragma unroll
-      for (int i = 0; i < GROUP; ++i) {
-        part[0][i] = 0.f;
-        if (t0 + i < te) {
-          float ar, ai;
-          zoh_step(g.ds[i], g.xs[i], Adn, g.tbs[i], g.brs[i], g.bis[i], hr, hi, ar, ai);
-          part[0][i] = g.crs[i] * hr - g.cis[i] * hi;
-          if (n == 0) part[0][i] = fmaf(Ds, g.xs[i], part[0][i]);
-        }
+  for (int t0 = tc; t0 < te; t0 += GROUP) {
+    const int ng = min(GROUP, te - t0);
+    // ---- stage the group (steps past te and channels past D as zeros)
+    for (int k = tid; k < GROUP * N; k += 256) {
+      const int i = k / N, nn = k % N;
+      float4 tb = make_float4(0.f, 0.f, 0.f, 0.f), bc = tb;
+      if (i < ng) {
+        const long long tn = (b * p.L + t0 + i) * N + nn;
+        tb = p.tab[tn];
+        const float2 bb = load_pair<Tin>(BC, tn), cc = load_pair<Tin>(CC, tn);
+        bc = make_float4(bb.x, bb.y, cc.x, cc.y);
       }
-    } else {
+      s_tab[i][nn] = tb;
+      s_bc[i][nn] = bc;
+    }
+    for (int k = tid; k < GROUP * CBZ; k += 256) {
+      const int i = k / CBZ, cd = k % CBZ;
+      float2 v = make_float2(0.f, 0.f);
+      if (i < ng && d0 + cd < p.D) {
+        const long long td = (b * p.L + t0 + i) * p.D + d0 + cd;
+        v = make_float2(load_in<Tin>(X, td), load_in<Tin>(DT, td));
+      }
+      s_xd[i][cd] = v;
+    }
+    __syncthreads();
+    float part[1][GROUP];
 #pragma unroll
-      for (int i = 0; i < GROUP; ++i) part[0][i] = 0.f;
+    for (int i = 0; i < GROUP; ++i) {
+      part[0][i] = 0.f;
+      if (i < ng) {
+        const float2 xd = s_xd[i][dl];
+        const float4 bc = s_bc[i][n];
+        float ar, ai;
+        zoh_step(xd.y, xd.x, Adn, s_tab[i][n], bc.x, bc.y, hr, hi, ar, ai);
+        part[0][i] = bc.z * hr - bc.w * hi;
+        if (n == 0) part[0][i] = fmaf(Ds, xd.x, part[0][i]);
+      }
     }
     const int base = butterfly<N, 1, GROUP>(part, n);
-    if ((n % DUP) == 0) {
+    if ((n % DUP) == 0 && valid) {
 #pragma unroll
       for (int h = 0; h < HOLD; ++h) {
-        const int t = t0 + base + h;
-        if (t < te) p.y[(b * p.L + t) * p.D + d] = part[0][h];
+        const int i = base + h;
+        if (i < ng) p.y[(b * p.L + t0 + i) * p.D + d] = part[0][h];
       }
     }
+    __syncthreads();
   }
 }
 
