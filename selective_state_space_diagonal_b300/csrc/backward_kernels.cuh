@@ -23,7 +23,8 @@
 // Kernels:
 //   rot_kernel        e^{i theta} per (b, t, n), shared by every channel;
 //   chunk_fwd_kernel  per (b, c, d, n): U_c and P_c from a zero state       (only when C > 1)
-//   chunk_adj_kernel  per (b, c, d, n): W_c, Q_c and conj(a_tc) from a zero carry  (C > 1)
+//   chunk_adj_kernel  per (b, c, d, n): W_c, Q_c and conj(a_tc) from a zero carry, each 8-step
+//                     group staged once per block of channels                  (C > 1)
 //   chunk_combine_kernel  per (b, d, n): walks the C chunks forwards for each chunk's true
 //                     entry state and backwards for each chunk's true first-step adjoint;
 //   ckpt_kernel       per (b, c, d, n): the forward recurrence over the chunk from its entry
@@ -222,46 +223,60 @@ __global__ void __launch_bounds__(256, 3) chunk_fwd_kernel(const Params p) {
 }
 
 // W_c (adjoint at the chunk's first step with nothing flowing in from later chunks),
-// Q_c = conj(prod of a over the chunk's steps after the first) and conj(a_tc).
-template <typename Tin, int MODE>
+// Q_c = conj(prod of a over the chunk's steps after the first) and conj(a_tc). A block owns
+// 256 / N channels of one (b, c), a thread per (channel, n); each group of SEG steps (last to
+// first) is staged once per block -- e^{i theta} and Cc per (t, n), dy and dt per (t, d) --
+// before the lanes walk it. Grid: (ceil(D / (256 / N)), C, B).
+template <typename Tin, int MODE, int N>
 __global__ void __launch_bounds__(256) chunk_adj_kernel(const Params p) {
-  const ChunkThread th = chunk_thread(p);
-  if (!th.ok) return;
+  constexpr int CBZ = 256 / N;
+  __shared__ float4 s_tn[SEG][N];     // rot c, s, Cc re, im
+  __shared__ float2 s_td[SEG][CBZ];   // dy, dt
+  const int tid = threadIdx.x;
+  const int n = tid % N, dl = tid / N;
+  const int d0 = blockIdx.x * CBZ;
+  const int d = d0 + dl;
+  const bool valid = d < p.D;
+  const int c = blockIdx.y;
+  const long long b = blockIdx.z;
   const Tin* DT = static_cast<const Tin*>(p.dt);
   const Tin* CC = static_cast<const Tin*>(p.Cc);
-  const float a2 = p.A[(long long)th.d * p.N + th.n] * LOG2E;
-  const long long b = th.b;
-  const int tc = th.c * p.TC, te = min(p.L, tc + p.TC);
+  const float a2 = p.A[(long long)(valid ? d : 0) * N + n] * LOG2E;
+  const int tc = c * p.TC, te = min(p.L, tc + p.TC);
   float cr = 0.f, ci = 0.f, gr = 0.f, gi = 0.f, Qr = 1.f, Qi = 0.f, ar = 1.f, ai = 0.f;
   for (int t1 = te - 1; t1 >= tc; t1 -= SEG) {   // groups of SEG steps, last to first
-    float dys[SEG], ccr[SEG], cci[SEG], ds[SEG];
-    float2 ros[SEG];
-    // one 64-bit base per array for the group (step t1); steps before tc repeat tc
-    const long long bt = b * p.L + t1;
-    const float* dyg = p.dy + bt * p.D + th.d;
-    const Tin* dg = DT + bt * p.D + th.d;
-    const Tin* cg = CC + 2 * (bt * p.N + th.n);
-    const float2* rg = p.rot + bt * p.N + th.n;
-    const int first = t1 - tc;
-#pragma unroll
-    for (int i = 0; i < SEG; ++i) {
-      const int ii = min(i, first);   // t = t1 - ii
-      dys[i] = dyg[-ii * p.D];
-      const float2 cc = load_pair<Tin>(cg, -ii * p.N);
-      ccr[i] = cc.x;
-      cci[i] = cc.y;
-      ds[i] = load_in<Tin>(dg, -ii * p.D);
-      ros[i] = rg[-ii * p.N];
+    const int ng = min(SEG, t1 - tc + 1);        // row i is step t1 - i
+    for (int k = tid; k < SEG * N; k += 256) {
+      const int i = k / N, nn = k % N;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < ng) {
+        const long long tn = (b * p.L + t1 - i) * N + nn;
+        const float2 ro = p.rot[tn], cc = load_pair<Tin>(CC, tn);
+        v = make_float4(ro.x, ro.y, cc.x, cc.y);
+      }
+      s_tn[i][nn] = v;
     }
+    for (int k = tid; k < SEG * CBZ; k += 256) {
+      const int i = k / CBZ, cd = k % CBZ;
+      float2 v = make_float2(0.f, 0.f);
+      if (i < ng && d0 + cd < p.D) {
+        const long long td = (b * p.L + t1 - i) * p.D + d0 + cd;
+        v = make_float2(p.dy[td], load_in<Tin>(DT, td));
+      }
+      s_td[i][cd] = v;
+    }
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < SEG; ++i) {
       const int t = t1 - i;
-      if (t >= tc) {
-        gr = fmaf(dys[i], ccr[i], cr);
-        gi = fmaf(-dys[i], cci[i], ci);
-        const float r = ex2_approx(ds[i] * a2);
-        ar = r * ros[i].x;
-        ai = r * ros[i].y;
+      if (i < ng) {
+        const float4 q = s_tn[i][n];
+        const float2 v = s_td[i][dl];
+        gr = fmaf(v.x, q.z, cr);
+        gi = fmaf(-v.x, q.w, ci);
+        const float r = ex2_approx(v.y * a2);
+        ar = r * q.x;
+        ai = r * q.y;
         if (t > tc) {
           cr = ar * gr + ai * gi;   // conj(a_t) ghat_t
           ci = ar * gi - ai * gr;
@@ -271,11 +286,14 @@ __global__ void __launch_bounds__(256) chunk_adj_kernel(const Params p) {
         }
       }
     }
+    __syncthreads();
   }
-  float2* rec = chunk_rec(p, b, th.c, th.d, th.n);
-  rec[2] = make_float2(gr, gi);
-  rec[3] = make_float2(Qr, Qi);
-  rec[4] = make_float2(ar, -ai);
+  if (valid) {
+    float2* rec = chunk_rec(p, b, c, d, n);
+    rec[2] = make_float2(gr, gi);
+    rec[3] = make_float2(Qr, Qi);
+    rec[4] = make_float2(ar, -ai);
+  }
 }
 
 // Walk the chunks of (b, d, n): rec[0] <- entry state h_in, rec[2] <- true adjoint at the

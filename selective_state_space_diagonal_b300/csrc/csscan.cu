@@ -809,7 +809,8 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
       bwd::chunk_fwd_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
       CSSCAN_CUDA(cudaGetLastError());
     }
-    bwd::chunk_adj_kernel<Tin, MODE><<<ck_blocks, 256, 0, st>>>(p);
+    const dim3 agrid{unsigned((a.D + 256 / N - 1) / (256 / N)), unsigned(C), unsigned(a.B)};
+    bwd::chunk_adj_kernel<Tin, MODE, N><<<agrid, 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
     const long long n_cb = (long long)a.B * a.D * N;
     bwd::chunk_combine_kernel<<<unsigned((n_cb + 255) / 256), 256, 0, st>>>(p);
