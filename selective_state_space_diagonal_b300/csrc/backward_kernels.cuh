@@ -619,7 +619,9 @@ __global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
       s_dD[j][tid] = dD_acc;
 
       // ---- sums over n: dx and ddt of (t, d) are final; dlam goes on to the sum over d
-      hold_base = butterfly<N, 3, SEG>(g3, n);
+      // dlam exists only in the trapezoid mode: exp-Euler reduces dx and ddt alone
+      hold_base = MODE == 1 ? butterfly<N, 3, SEG>(g3, n)
+                            : butterfly<N, 2, SEG>(*reinterpret_cast<float(*)[2][SEG]>(&g3), n);
       const bool owner = (n % DUP) == 0;
 #pragma unroll
       for (int h = 0; h < HOLD; ++h) {
