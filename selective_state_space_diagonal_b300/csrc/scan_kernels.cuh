@@ -128,6 +128,11 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
   const int q = n >> 1, odd = n & 1;
   float phi = 0.f, cs = 1.f, sn = 0.f;
   float* rr = p.rot + ((int64_t(b) * p.S + s) * 4 * p.N + n) * 2;   // row r at rr + r * 2N
+  // trapezoid: E_t = sum_n Re(Cc_t Bc_t) by a shuffle sum over the N lanes of (b, s), which are
+  // neighbours in a warp when N <= 32 (whole groups: the thread count is a multiple of N)
+  const bool lane_sum = MODE == 1 && p.N <= 32;
+  const unsigned gmask = p.N >= 32 ? 0xffffffffu : (((1u << p.N) - 1u) << ((threadIdx.x & 31) & ~(p.N - 1)));
+  const Tin* lam = static_cast<const Tin*>(p.lam);
   for (int t = t0; t < t1; ++t) {
     const int64_t tn = (int64_t(b) * p.L + t) * p.N + n;
     phi += load_in<Tin>(th, tn);
@@ -143,6 +148,18 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
     row[2 + odd] = cs * bi - sn * br;    // Im(e^{-i Phi} Bc)
     row[4 + odd] = cs * cr - sn * ci;    // Re(e^{+i Phi} Cc)
     row[6 + odd] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
+    if (lane_sum) {
+      float E = cr * br - ci * bi;
+      for (int o = p.N / 2; o >= 1; o >>= 1) E += __shfl_xor_sync(gmask, E, o);
+      if (n == 0) {
+        const int64_t tb = int64_t(b) * p.L + t;
+        const float lt = load_in<Tin>(lam, tb);
+        const float mu = (t + 1 < p.L) ? 1.f - load_in<Tin>(lam, tb + 1) : 0.f;
+        float4* a = reinterpret_cast<float4*>(p.aux) + 2 * tb;
+        a[0] = make_float4(lt, lt, mu, mu);
+        a[1] = make_float4(E, E, 0.f, 0.f);
+      }
+    }
   }
   for (int r = 0; r < 4; ++r) {   // rows past the sub-chunk's last step hold the last step's value
     if (8 * r + 7 > t1 - 1 - t0) {
@@ -150,8 +167,7 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
       rr[r * 2 * p.N + 1] = sn;
     }
   }
-  if (MODE == 1 && n == 0) {
-    const Tin* lam = static_cast<const Tin*>(p.lam);
+  if (MODE == 1 && n == 0 && !lane_sum) {   // N = 64: one lane sums the row
     for (int t = t0; t < t1; ++t) {
       const int64_t tb = int64_t(b) * p.L + t;
       float E = 0.f;
