@@ -360,8 +360,15 @@ template <int N> struct GradStage {
   static constexpr int BYTES = OFF_CC + (SEG + 1) * N * 8;
 };
 
+// Resident blocks per SM that grad_kernel is compiled for. Five (96 registers) hides more
+// latency than four for every shape but the N = 32 trapezoid, where the 96-register cap
+// spills inside the butterfly and four (128 registers) is faster.
+template <int MODE, int N> struct GradOcc {
+  static constexpr int MIN_BLOCKS = MODE == 1 && N == 32 ? 4 : 5;
+};
+
 template <typename Tin, int MODE, int N>
-__global__ void __launch_bounds__(THREADS) grad_kernel(const Params p) {
+__global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_kernel(const Params p) {
   using GT = GradTile<N>;
   using GS = GradStage<N>;
   constexpr int CPW = GT::CPW, K = GT::K, CB = GT::CB;
