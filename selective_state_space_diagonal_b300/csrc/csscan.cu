@@ -461,9 +461,9 @@ int launch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
     zoh::zoh_combine_kernel<<<unsigned((rows + 255) / 256), 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
   }
-  constexpr int CBZ = 256 / N;
+  constexpr int CBZ = zoh::OUT_THREADS / N;
   const dim3 ogrid{unsigned((a.D + CBZ - 1) / CBZ), unsigned(C), unsigned(a.B)};
-  zoh::zoh_out_kernel<Tin, N><<<ogrid, 256, 0, st>>>(p);
+  zoh::zoh_out_kernel<Tin, N><<<ogrid, zoh::OUT_THREADS, 0, st>>>(p);
   CSSCAN_CUDA(cudaGetLastError());
   if (o.scan_end) CSSCAN_CUDA(cudaEventRecord(o.scan_end, st));
   return CSSCAN_OK;
@@ -645,7 +645,7 @@ int launch_mimo(const MimoArgs& a, cudaStream_t st) {
   }
   constexpr int HB = mimo::MimoStage<N, P>::HB;
   const dim3 ogrid{unsigned((a.H + HB - 1) / HB), unsigned(C), unsigned(a.B)};
-  mimo::mimo_out_kernel<Tin, MODE, N, P><<<ogrid, 256, 0, st>>>(p);
+  mimo::mimo_out_kernel<Tin, MODE, N, P><<<ogrid, mimo::OUT_THREADS, 0, st>>>(p);
   CSSCAN_CUDA(cudaGetLastError());
   return CSSCAN_OK;
 }

@@ -13,7 +13,7 @@
 //   mimo_chunk_kernel   per (b, c, h, n): the chunk's end state from a zero entry state and
 //                       the product of a over the chunk                     (chunks > 1 only)
 //   mimo_combine_kernel per (b, h, n): each chunk's entry state
-//   mimo_out_kernel     blocks of 256 / N heads of one (b, c), a thread per (head, n): the
+//   mimo_out_kernel     blocks of OUT_THREADS / N heads of one (b, c), a thread per (head, n): the
 //                       recurrence over the chunk with y, each 8-step group's shared inputs
 //                       staged in shared memory first; each lane keeps its P partial outputs
 //                       for the group and a reduce-scatter over the head's N lanes leaves
@@ -26,6 +26,15 @@ namespace csscan {
 namespace mimo {
 
 constexpr int GROUP = 8;
+// Threads per block of mimo_out_kernel. Blocks of 128 threads compiled for 9 resident
+// blocks per SM (56 registers) hold 1152 threads per SM, so 16 x 640 x 16 (b, head, n) rows
+// run in one wave; 256-thread blocks at 64 registers held 1024 and needed a second, 8 %
+// full wave (11.5 -> 8.4 ms). With P = 8 the 56-register cap spills the 64 partial outputs,
+// so those kernels keep 128 registers (4 blocks).
+constexpr int OUT_THREADS = 128;
+template <int P> struct OutOcc {
+  static constexpr int MIN_BLOCKS = P <= 4 ? 9 : 4;
+};
 constexpr float LOG2E = 1.4426950408889634f;
 
 struct Params {
@@ -166,14 +175,14 @@ __global__ void __launch_bounds__(256) mimo_combine_kernel(const Params p) {
   }
 }
 
-// The recurrence over chunk c with y. A block owns HB = 256 / N heads of one (b, c): thread
+// The recurrence over chunk c with y. A block owns HB = OUT_THREADS / N heads of one (b, c): thread
 // (head hl, state n), the N lanes of a head neighbours in a warp (N <= 32). For each group of
 // GROUP steps the block first stages, coalesced, what its lanes share -- e^{i theta}, Bm and Cm
 // per (t, n), x and dt per (t, head), lam per t -- in shared memory. Each lane then keeps its P
 // partial outputs for the group and a reduce-scatter over the head's N lanes leaves every
 // (step, channel) sum in one lane. Grid: (ceil(H / HB), C, B).
 template <int N, int P> struct MimoStage {
-  static constexpr int HB = 256 / N;                       // heads per block
+  static constexpr int HB = OUT_THREADS / N;               // heads per block
   static constexpr int TN = GROUP * N;                     // (t, n) entries of a group
   static constexpr int TH = GROUP * HB;                    // (t, head) entries of a group
   static constexpr int OFF_ROT = 0;                        // float2 [GROUP][N]
@@ -186,7 +195,7 @@ template <int N, int P> struct MimoStage {
 };
 
 template <typename Tin, int MODE, int N, int P>
-__global__ void __launch_bounds__(256) mimo_out_kernel(const Params p) {
+__global__ void __launch_bounds__(OUT_THREADS, OutOcc<P>::MIN_BLOCKS) mimo_out_kernel(const Params p) {
   using MS = MimoStage<N, P>;
   constexpr int HB = MS::HB;
   constexpr int E = GROUP * P;                   // (step, channel) entries of one group
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(256) mimo_out_kernel(const Params p) {
   for (int t0 = tc; t0 < te; t0 += GROUP) {
     const int ng = min(GROUP, te - t0);
     // ---- stage the group (steps past te or heads past H as zeros)
-    for (int k = tid; k < GROUP * N * P; k += 256) {
+    for (int k = tid; k < GROUP * N * P; k += OUT_THREADS) {
       const int i = k / (N * P), r = k % (N * P);
       float2 bb = make_float2(0.f, 0.f), cc = make_float2(0.f, 0.f);
       if (i < ng) {
@@ -239,15 +248,15 @@ __global__ void __launch_bounds__(256) mimo_out_kernel(const Params p) {
       (&s_bm[0][0][0])[k] = bb;
       (&s_cm[0][0][0])[k] = cc;
     }
-    for (int k = tid; k < GROUP * N; k += 256) {
+    for (int k = tid; k < GROUP * N; k += OUT_THREADS) {
       const int i = k / N, nn = k % N;
       s_rot[i][nn] = i < ng ? p.rot[(b * p.L + t0 + i) * N + nn] : make_float2(0.f, 0.f);
     }
-    for (int k = tid; k < GROUP * HB * P; k += 256) {
+    for (int k = tid; k < GROUP * HB * P; k += OUT_THREADS) {
       const int i = k / (HB * P), r = k % (HB * P), hh = h0 + r / P;
       (&s_x[0][0][0])[k] = (i < ng && hh < p.H) ? load_in<Tin>(X, ((b * p.L + t0 + i) * p.H + h0) * P + r) : 0.f;
     }
-    for (int k = tid; k < GROUP * HB; k += 256) {
+    for (int k = tid; k < GROUP * HB; k += OUT_THREADS) {
       const int i = k / HB, r = k % HB;
       s_dt[i][r] = (i < ng && h0 + r < p.H) ? load_in<Tin>(DT, (b * p.L + t0 + i) * p.H + h0 + r) : 0.f;
     }

@@ -11,7 +11,7 @@
 //   zoh_chunk_kernel   per (b, c, d, n): state at the chunk's end from a zero entry state and
 //                      the product of a over the chunk  (only when the rows leave few threads)
 //   zoh_combine_kernel per (b, d, n): walks the chunks for each chunk's entry state
-//   zoh_out_kernel     blocks of 256 / N channels of one (b, c), a thread per (channel, n): the
+//   zoh_out_kernel     blocks of OUT_THREADS / N channels of one (b, c), a thread per (channel, n): the
 //                      recurrence over the chunk from its entry state, each 8-step group's
 //                      shared inputs staged in shared memory first; the N lanes of a channel
 //                      sum Re(Cc h) with a reduce-scatter and one stores y
@@ -25,6 +25,7 @@ namespace csscan {
 namespace zoh {
 
 constexpr int GROUP = 8;   // steps whose loads are issued together
+constexpr int OUT_THREADS = 256;   // threads per block of zoh_out_kernel
 
 struct Params {
   const void* x;       // (B, L, D)
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(256) zoh_combine_kernel(const Params p) {
   }
 }
 
-// The recurrence over chunk c from its entry state, with y. A block owns CBZ = 256 / N channels
+// The recurrence over chunk c from its entry state, with y. A block owns CBZ = OUT_THREADS / N channels
 // of one (b, c): thread (channel dl, state n), the N lanes of a channel neighbours in a warp
 // (N <= 32). For each group of GROUP steps the block first stages, coalesced, what its lanes
 // share -- the (cos, sin, theta, cos - 1) row, Bc and Cc per (t, n), x and dt per (t, channel)
@@ -184,8 +185,8 @@ __global__ void __launch_bounds__(256) zoh_combine_kernel(const Params p) {
 // reduce-scatter over the N lanes then leaves each step's sum in one lane, which stores it.
 // Grid: (ceil(D / CBZ), C, B).
 template <typename Tin, int N>
-__global__ void __launch_bounds__(256) zoh_out_kernel(const Params p) {
-  constexpr int CBZ = 256 / N;
+__global__ void __launch_bounds__(OUT_THREADS) zoh_out_kernel(const Params p) {
+  constexpr int CBZ = OUT_THREADS / N;
   constexpr int HOLD = GROUP >= N ? GROUP / N : 1;
   constexpr int DUP = N > GROUP ? N / GROUP : 1;
   __shared__ float4 s_tab[GROUP][N];
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(256) zoh_out_kernel(const Params p) {
   for (int t0 = tc; t0 < te; t0 += GROUP) {
     const int ng = min(GROUP, te - t0);
     // ---- stage the group (steps past te and channels past D as zeros)
-    for (int k = tid; k < GROUP * N; k += 256) {
+    for (int k = tid; k < GROUP * N; k += OUT_THREADS) {
       const int i = k / N, nn = k % N;
       float4 tb = make_float4(0.f, 0.f, 0.f, 0.f), bc = tb;
       if (i < ng) {
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(256) zoh_out_kernel(const Params p) {
       s_tab[i][nn] = tb;
       s_bc[i][nn] = bc;
     }
-    for (int k = tid; k < GROUP * CBZ; k += 256) {
+    for (int k = tid; k < GROUP * CBZ; k += OUT_THREADS) {
       const int i = k / CBZ, cd = k % CBZ;
       float2 v = make_float2(0.f, 0.f);
       if (i < ng && d0 + cd < p.D) {
