@@ -43,12 +43,11 @@ L2_BYTES = 126 * 1024 * 1024
 # injection, update), the segment recompute (the same again) and the reverse step (~28 /
 # ~45: adjoint, transition gradient, injection gradients, exponential chain rule, carry).
 BWD_ALU_OPS_PER_ELEM = {0: 48, 1: 79}
-# FP32 lane-operations per element of the zero-order-hold scan (zoh_kernels.cuh), counted
-# from its source: decay exponent 1, expm1 about 8, transition 3, e^z - 1 and |z|^2 4,
-# (e^z - 1)/z 6, gamma x 3, complex injection 4, update 4, Re(Cc h) 2, plus one MUFU
-# reciprocal; the time-chunk pass adds the update and the chunk product again when the
-# rows alone do not fill the GPU.
-ZOH_ALU_OPS_PER_ELEM = 35
+# FP32 lane-operations per element of the zero-order-hold mode of the scan kernel, counted
+# from its source: decay exponent 2 (formed again as Re z), expm1 5 (polynomial and r - 1),
+# E beta + delta 2, |z|^2 1, times conj(z) 4, the tau term 1, weight 1, update 4, Re(Ct k) 2;
+# plus one MUFU ex2 and one MUFU reciprocal on their own pipe.
+ZOH_ALU_OPS_PER_ELEM = 22
 # FP32 pipe lane-operations per scanned element in this implementation's formulation: one
 # multiply for the decay exponent, four for the complex decay-and-inject update, two for the
 # real part of C h (plus one MUFU ex2 on its own pipe).
@@ -263,14 +262,8 @@ def run_reference(args):
 
 
 def launches_per_step(w: wl.Workload) -> int:
-    """Kernels one forward call enqueues: the rotation table and the scan; in the zero-order-hold
-    mode the table, the output pass and, when the rows alone leave under 4096 threads per SM
-    (the library's rule), the time-chunk pass and the chunk sweep."""
-    if w.mode != wl.MODE_ZOH:
-        return 2
-    import torch
-    nsm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    return 2 if w.B * w.D * w.N >= nsm * 4096 else 4
+    """Kernels one forward call enqueues, in every mode: the table kernel and the scan kernel."""
+    return 2
 
 
 def workload_config(w: wl.Workload, l2_note: str = ""):
@@ -428,7 +421,7 @@ def run_ours(args):
     traffic = traffic_from_profiles(w.name)
     roofline = {"bound": "alu", "achieved": alu_achieved, "peak": alu_peak, "unit": "Tops/s",
                 "frac": alu_achieved / alu_peak, "traffic": traffic,
-                "kernel": "zoh_out_kernel (+ chunk passes)" if w.mode == wl.MODE_ZOH else "scan_kernel",
+                "kernel": "scan_kernel",
                 "ms_per_launch": 1e3 * scan_mean_s,
                 "peak_note": f"FP32 pipe: {FP32_LANES_PER_SM} lanes/SM x {N_SM} SMs x {sm_max_mhz:.0f} MHz; "
                              f"{ops_per_elem} lane-ops per element"}

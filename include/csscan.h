@@ -84,7 +84,7 @@ enum {
  *   ZOH           gamma_t = dt_t (e^{z_t} - 1) / z_t with z_t = dt_t A + i theta_t (the table's
  *                 A^{-1}(exp(dt A) - I) with the complex exponent of a_t in place of dt A);
  *                 csscan_forward and csscan_forward_ex only (without initial state or halo),
- *                 N <= 32, B <= 65535; the other entry points return CSSCAN_ERR_UNSUPPORTED for it */
+ *                 N <= 32; the other entry points return CSSCAN_ERR_UNSUPPORTED for it */
 typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1, CSSCAN_MODE_ZOH = 2 } csscan_mode_t;
 typedef enum { CSSCAN_F32 = 0, CSSCAN_BF16 = 1 } csscan_dtype_t;
 

@@ -7,7 +7,7 @@ import subprocess
 HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 SOURCES = [os.path.join(HERE, "csrc", "csscan.cu")]
-HEADERS = [os.path.join(HERE, "csrc", f) for f in ("scan_kernels.cuh", "device_util.cuh", "decode_kernel.cuh", "backward_kernels.cuh", "zoh_kernels.cuh", "mimo_kernels.cuh")] + \
+HEADERS = [os.path.join(HERE, "csrc", f) for f in ("scan_kernels.cuh", "device_util.cuh", "decode_kernel.cuh", "backward_kernels.cuh", "mimo_kernels.cuh")] + \
           [os.path.join(ROOT, "include", "csscan.h")]
 OUTPUT = os.path.join(HERE, "libcsscan.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")

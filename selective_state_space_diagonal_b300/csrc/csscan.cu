@@ -1,8 +1,8 @@
 // csscan.cu -- host side of the C ABI declared in include/csscan.h: argument checks,
 // launch planning (block width, sequence chunks, shared-memory ring), the per-(device,
 // stream) workspace, tile-copy descriptors, and the launches of the rotation-table kernel
-// and the scan kernel (scan_kernels.cuh), the zero-order-hold scan (zoh_kernels.cuh), the MIMO
-// scan (mimo_kernels.cuh), the decode step (decode_kernel.cuh) and the backward pass
+// and the scan kernel (scan_kernels.cuh; every forward mode, the zero-order hold included),
+// the MIMO scan (mimo_kernels.cuh), the decode step (decode_kernel.cuh) and the backward pass
 // (backward_kernels.cuh).
 #include <cudaTypedefs.h>
 
@@ -19,7 +19,6 @@
 #include "decode_kernel.cuh"
 #include "mimo_kernels.cuh"
 #include "scan_kernels.cuh"
-#include "zoh_kernels.cuh"
 
 using namespace csscan;
 
@@ -94,8 +93,8 @@ struct Plan {
 };
 
 constexpr int MAX_DYN_SMEM = 160 * 1024;         // opt-in dynamic shared memory per block
-// The zero-order-hold and MIMO paths run one thread per (row, state) sequentially over time;
-// below this many such threads per SM they also split the sequence into time chunks.
+// The MIMO path and the backward's gradient pass run one thread per (row, state) sequentially
+// over time; below this many such threads per SM they also split the sequence into time chunks.
 constexpr int64_t SEQ_THREADS_PER_SM = 4096;
 constexpr int RESIDENT_WARPS_PER_SM = 8;         // target of the automatic chunking
 
@@ -213,7 +212,7 @@ int make_plan(const Args& a, const csscan_options_t& o, int dev, Plan* pl) {
   pl->o_agg = carry == CARRY_DECOUPLED ? take(size_t(n_units) * DT * N * 8) : 0;
   pl->o_sdt = carry == CARRY_DECOUPLED ? take(size_t(n_units) * DT * 4) : 0;
   pl->o_crot = carry == CARRY_DECOUPLED ? take(size_t(n_units) * N * 8) : 0;
-  pl->o_tab = take(size_t(a.B) * a.L * 4 * N * 4);
+  pl->o_tab = take(size_t(a.B) * a.L * SG::TABW * N * 4);
   pl->o_aux = MODE == 1 ? take(size_t(a.B) * a.L * SG::AUX_W * 4) : 0;
   pl->o_rot = take(size_t(a.B) * S * 4 * 2 * N * 4);
   pl->rest_bytes = off;
@@ -249,8 +248,8 @@ int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* 
   using SG = Stage<N, Tin, MODE>;
   bool ok = make_map(&sp.tm_x, tin, a.x, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, pl.DT, SG::X_ROWS, 1) &&
             make_map(&sp.tm_dt, tin, a.delta, a.D, a.L, a.B, a.D * s_in, a.L * a.D * s_in, pl.DT, SG::DT_ROWS, 1) &&
-            make_map(&sp.tm_tab, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.tab, 4 * N, a.L, a.B, 16 * N, a.L * 16 * N, 4 * N,
-                     SG::TAB_ROWS, 1) &&
+            make_map(&sp.tm_tab, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.tab, SG::TABW * N, a.L, a.B, SG::TABW * N * 4,
+                     a.L * SG::TABW * N * 4, SG::TABW * N, SG::TAB_ROWS, 1) &&
             make_map(&sp.tm_rot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.rot, 2 * N, 4 * S, a.B, 8 * N, 4 * S * 8 * N, 2 * N, 4,
                      1);
   if (ok && MODE == 1)
@@ -375,7 +374,10 @@ int dispatch_n(const Args& a, const csscan_options_t& o, cudaStream_t st) {
     case 8: return launch<8, Tin, MODE>(a, o, st);
     case 16: return launch<16, Tin, MODE>(a, o, st);
     case 32: return launch<32, Tin, MODE>(a, o, st);
-    case 64: return launch<64, Tin, MODE>(a, o, st);
+    case 64:
+      // the zero-order-hold table row (8 N floats) exceeds one TMA box at N = 64
+      if constexpr (MODE == 2) return CSSCAN_ERR_UNSUPPORTED;
+      else return launch<64, Tin, MODE>(a, o, st);
     default: return CSSCAN_ERR_UNSUPPORTED;
   }
 }
@@ -411,90 +413,20 @@ csscan_options_t default_options() {
   return o;
 }
 
-// ----------------------------------------------------------------------------- zero-order hold
-template <typename Tin, int N>
-int launch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
-  int dev = 0, nsm = 0;
-  CSSCAN_CUDA(cudaGetDevice(&dev));
-  CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-  // time chunks until there are SEQ_THREADS_PER_SM threads per SM (the recurrence is sequential per thread)
-  const int64_t G = zoh::GROUP;
-  const int64_t S = (a.L + G - 1) / G;
-  const int64_t rows = a.B * a.D * N;
-  const int64_t target = int64_t(nsm) * SEQ_THREADS_PER_SM;
-  int64_t C = std::min<int64_t>(S, std::max<int64_t>(1, (target + rows - 1) / rows));
-  if (C > 65535) C = 65535;   // the output pass has one grid row per chunk
-  const int64_t TC = (S + C - 1) / C * G;
-  C = (a.L + TC - 1) / TC;
-  const size_t tab_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float4), 256);
-  const size_t chunk_bytes = C > 1 ? size_t(a.B * C * a.D * N) * 2 * sizeof(float2) : 0;
-  WsEntry ws;
-  int rc = get_workspace(dev, st, 1, tab_bytes + chunk_bytes, &ws);
-  if (rc != CSSCAN_OK) return rc;
-  char* rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
-  zoh::Params p;
-  p.x = a.x;
-  p.dt = a.delta;
-  p.Bc = a.Bc;
-  p.Cc = a.Cc;
-  p.A = a.A;
-  p.Dskip = a.Dskip;
-  p.y = a.y;
-  p.tab = reinterpret_cast<const float4*>(rest);
-  p.chunk = C > 1 ? reinterpret_cast<float2*>(rest + tab_bytes) : nullptr;
-  p.B = int(a.B);
-  p.L = int(a.L);
-  p.D = int(a.D);
-  p.N = N;
-  p.TC = int(TC);
-  p.C = int(C);
-  const long long n_tab = (long long)a.B * a.L * N;
-  const long long n_thr = (long long)a.B * C * a.D * N;
-  if (!grid_fits(n_tab) || !grid_fits(n_thr)) return CSSCAN_ERR_UNSUPPORTED;
-  zoh::zoh_table_kernel<Tin><<<unsigned((n_tab + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float4*>(rest),
-                                                                            n_tab);
-  CSSCAN_CUDA(cudaGetLastError());
-  if (o.scan_begin) CSSCAN_CUDA(cudaEventRecord(o.scan_begin, st));
-  if (C > 1) {
-    zoh::zoh_chunk_kernel<Tin><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
-    CSSCAN_CUDA(cudaGetLastError());
-    zoh::zoh_combine_kernel<<<unsigned((rows + 255) / 256), 256, 0, st>>>(p);
-    CSSCAN_CUDA(cudaGetLastError());
-  }
-  constexpr int CBZ = zoh::OUT_THREADS / N;
-  const dim3 ogrid{unsigned((a.D + CBZ - 1) / CBZ), unsigned(C), unsigned(a.B)};
-  zoh::zoh_out_kernel<Tin, N><<<ogrid, zoh::OUT_THREADS, 0, st>>>(p);
-  CSSCAN_CUDA(cudaGetLastError());
-  if (o.scan_end) CSSCAN_CUDA(cudaEventRecord(o.scan_end, st));
-  return CSSCAN_OK;
-}
-
-template <typename Tin>
-int dispatch_zoh(const Args& a, const csscan_options_t& o, cudaStream_t st) {
-  switch (a.N) {
-    case 2: return launch_zoh<Tin, 2>(a, o, st);
-    case 4: return launch_zoh<Tin, 4>(a, o, st);
-    case 8: return launch_zoh<Tin, 8>(a, o, st);
-    case 16: return launch_zoh<Tin, 16>(a, o, st);
-    case 32: return launch_zoh<Tin, 32>(a, o, st);
-    default: return CSSCAN_ERR_UNSUPPORTED;
-  }
-}
-
 int forward_impl(const Args& a, const csscan_options_t* opts, cudaStream_t st) {
   csscan_options_t o = opts ? *opts : default_options();
   if (a.mode == CSSCAN_MODE_ZOH) {
-    // the zero-order-hold scan starts from the zero state and has no chunk options
+    // the zero-order-hold scan starts from the zero state (no h0, final state or halo)
     if (a.h0 || a.h_last || a.x_prev || a.Bc_prev) return CSSCAN_ERR_UNSUPPORTED;
     Args a0 = a;
     a0.mode = CSSCAN_MODE_EXP_EULER;   // same pointer, size and alignment rules
     int rc = validate(a0, o);
     if (rc != CSSCAN_OK) return rc;
-    if (a.N > 32 || a.B > 65535) return CSSCAN_ERR_UNSUPPORTED;
+    if (a.N > 32) return CSSCAN_ERR_UNSUPPORTED;
     const size_t pair = a.dtype == CSSCAN_F32 ? 8 : 4;   // Bc, Cc are read one complex entry at a time
     if (!aligned(a.Bc, pair) || !aligned(a.Cc, pair)) return CSSCAN_ERR_MISALIGNED;
     if (a.B == 0 || a.L == 0 || a.D == 0) return CSSCAN_OK;
-    return a.dtype == CSSCAN_F32 ? dispatch_zoh<float>(a, o, st) : dispatch_zoh<uint16_t>(a, o, st);
+    return a.dtype == CSSCAN_F32 ? dispatch_n<float, 2>(a, o, st) : dispatch_n<uint16_t, 2>(a, o, st);
   }
   int rc = validate(a, o);
   if (rc != CSSCAN_OK) return rc;

@@ -28,6 +28,16 @@
 //    (decoupled look-back) or wait for the predecessor's final state (serial carry).
 //    Chunk order comes from an atomic ticket, so a block only ever waits on blocks that
 //    started earlier; every wait is bounded and reports a status instead of hanging.
+// 5. Zero-order hold (MODE 2). The injection is dt x Bc (e^z - 1) / z with z = dt A + i theta,
+//    a complex weight per (t, d, n) (ZOH row of the discretisation table of "Mamba-3 paper
+//    story", complex exponent as for alpha_t). With e^z - 1 = E e^{i theta} + (e^{i theta} - 1),
+//    E = e^{dt A} - 1, the frame injection is dt x (E beta_t + delta_t) / z, where
+//    beta_t = Bt_t e^{i theta_t} and delta_t = Bt_t (e^{i theta_t} - 1) are per-(b, t, n) table
+//    entries. A thread forms per element only E (a Taylor polynomial where |dt A| is small,
+//    else r - 1), one complex product with conj(z) and a hardware reciprocal of |z|^2. The
+//    table holds beta, delta and theta in base-2 units (times log2 e), so that the decay's
+//    own argument v = dt A log2 e is Re z; |z|^2 carries a floor tau whose numerator partner
+//    tau beta makes the weight tend to Bt as z -> 0.
 #pragma once
 
 #include <type_traits>
@@ -43,6 +53,13 @@ constexpr int THREADS = WARPS * 32;
 constexpr int MAX_STAGES = 4;   // depth of the shared-memory ring
 constexpr int RING_BYTES = 56 * 1024;   // shared memory for the ring of one block
 constexpr float LOG2E_F = 1.4426950408889634f;
+// Zero-order hold: Taylor coefficients (ln 2)^k / k! of 2^v - 1, the |v| below which that
+// polynomial (truncation below 3e-8 relative) replaces r - 1, and the floor tau of |z|^2.
+constexpr float ZOH_C1 = 0.6931471805599453f, ZOH_C2 = 0.2402265069591007f;
+constexpr float ZOH_C3 = 0.05550410866482158f, ZOH_C4 = 0.009618129107628477f;
+constexpr float ZOH_V_POLY = 0.0625f;
+constexpr float ZOH_TAU = 1e-30f;
+constexpr float ZOH_TAU_LN2 = ZOH_TAU * 0.6931471805599453f;   // tau times beta / beta'
 
 // Thread tile for N states: NS states per thread, NG lanes per channel pair, CPW channels
 // per warp, DT channels per block.
@@ -67,7 +84,8 @@ struct Stage {
   static constexpr int AUX_W = 8;                       // floats per aux row
   static constexpr int X_BYTES = X_ROWS * DT * SIN;
   static constexpr int DT_BYTES = DT_ROWS * DT * SIN;
-  static constexpr int TAB_BYTES = TAB_ROWS * 4 * N * 4;
+  static constexpr int TABW = MODE == 2 ? 8 : 4;         // table floats per state and step
+  static constexpr int TAB_BYTES = TAB_ROWS * TABW * N * 4;
   static constexpr int AUX_BYTES = MODE == 1 ? AUX_ROWS * AUX_W * 4 : 0;
   static constexpr int ROT_BYTES = 4 * 2 * N * 4;       // e^{i Phi} after local steps 7, 15, 23, last
   static constexpr int OFF_X = 0;
@@ -104,7 +122,10 @@ struct TableParams {
   const void* Cc;
   const void* theta;
   const void* lam;
-  float* tab;  // (B, L, N/2, 8): per state pair (Btr, Btr', Bti, Bti', Ctr, Ctr', -Cti, -Cti')
+  float* tab;  // (B, L, N/2, 8): per state pair (Btr, Btr', Bti, Bti', Ctr, Ctr', -Cti, -Cti');
+               // zero-order hold (B, L, N/2, 16): (beta re x2, beta im x2, Ct as above,
+               // delta re x2, delta im x2, theta x2, theta^2 + tau x2), beta, delta and theta
+               // times log2 e
   float* aux;  // (B, L, 8): lam_t, lam_t, mu, mu, E_t, E_t, 0, 0 with mu = 1 - lam_{t+1}
                // (0 at t = L-1) (trapezoid only)
   float* rot;  // (B, S, 4, N, 2): e^{i Phi} of sub-chunk s after its local steps 7, 15, 23 and
@@ -143,9 +164,27 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
     }
     const float br = load_in<Tin>(Bc, 2 * tn), bi = load_in<Tin>(Bc, 2 * tn + 1);
     const float cr = load_in<Tin>(Cc, 2 * tn), ci = load_in<Tin>(Cc, 2 * tn + 1);
-    float* row = p.tab + (int64_t(b) * p.L + t) * (4 * p.N) + q * 8;
-    row[odd] = cs * br + sn * bi;        // Re(e^{-i Phi} Bc)
-    row[2 + odd] = cs * bi - sn * br;    // Im(e^{-i Phi} Bc)
+    constexpr int TW = MODE == 2 ? 8 : 4;
+    float* row = p.tab + (int64_t(b) * p.L + t) * (TW * p.N) + q * 2 * TW;
+    const float btr = cs * br + sn * bi;   // Re(e^{-i Phi} Bc)
+    const float bti = cs * bi - sn * br;   // Im(e^{-i Phi} Bc)
+    if (MODE == 2) {
+      // e^{i theta} - 1 without cancellation: cos theta - 1 = -2 sin^2(theta / 2)
+      const float th_t = load_in<Tin>(th, tn);
+      float sh, chh;
+      sincosf(0.5f * th_t, &sh, &chh);
+      const float cm1 = -2.f * sh * sh, s1 = 2.f * sh * chh, c1 = 1.f + cm1;
+      row[odd] = LOG2E_F * (btr * c1 - bti * s1);        // beta = Bt e^{i theta}
+      row[2 + odd] = LOG2E_F * (btr * s1 + bti * c1);
+      row[8 + odd] = LOG2E_F * (btr * cm1 - bti * s1);   // delta = Bt (e^{i theta} - 1)
+      row[10 + odd] = LOG2E_F * (btr * s1 + bti * cm1);
+      const float tq = LOG2E_F * th_t;
+      row[12 + odd] = tq;
+      row[14 + odd] = fmaf(tq, tq, ZOH_TAU);
+    } else {
+      row[odd] = btr;
+      row[2 + odd] = bti;
+    }
     row[4 + odd] = cs * cr - sn * ci;    // Re(e^{+i Phi} Cc)
     row[6 + odd] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
     if (lane_sum) {
@@ -272,6 +311,28 @@ template <> struct PairLoad<uint16_t> {
 // then look-back); the lighter variants keep no registers for the heavier ones.
 // CKPT = true is the checkpoint variant for the backward pass: no y, and the true state
 // h_t = e^{i Phi_t} (k_{t+1} - p_{t+1} Bt_t) after every 8th step stored to p.ckpt.
+// Zero-order-hold update of one state pair of one channel in the rotating frame:
+// k <- r k + w (E beta + delta) conj(z) / |z|^2 (plus the tau terms), all in base-2 units.
+// v = dt A log2 e (both states), r = 2^v, w = dt x broadcast; (dr, di) delta, tq theta,
+// ntq -theta, t2 theta^2 + tau, (fr, fi) tau ln 2 beta'.
+__device__ __forceinline__ void zoh_update(float2& kr, float2& ki, float2 r, float2 v, float2 w, float2 btr,
+                                           float2 bti, float2 dr, float2 di, float2 tq, float2 ntq, float2 t2,
+                                           float2 fr, float2 fi) {
+  float2 pe = fma2(v, f2(ZOH_C4, ZOH_C4), f2(ZOH_C3, ZOH_C3));
+  pe = fma2(v, pe, f2(ZOH_C2, ZOH_C2));
+  pe = fma2(v, pe, f2(ZOH_C1, ZOH_C1));
+  pe = mul2(v, pe);
+  const float2 rm1 = fma2(r, f2(1.f, 1.f), f2(-1.f, -1.f));
+  const float2 E = f2(fabsf(v.x) < ZOH_V_POLY ? pe.x : rm1.x, fabsf(v.y) < ZOH_V_POLY ? pe.y : rm1.y);
+  const float2 nr = fma2(E, btr, dr), ni = fma2(E, bti, di);
+  const float2 z2 = fma2(v, v, t2);
+  const float2 sw = mul2(w, f2(rcp_approx(z2.x), rcp_approx(z2.y)));
+  const float2 mr = fma2(ni, tq, fma2(nr, v, fr));
+  const float2 mi = fma2(ni, v, fma2(nr, ntq, fi));
+  kr = fma2(r, kr, mul2(sw, mr));
+  ki = fma2(r, ki, mul2(sw, mi));
+}
+
 template <int N, typename Tin, int MODE, int CARRY, bool CKPT = false>
 __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant__ ScanParams p) {
   using TL = Tile<N>;
@@ -467,7 +528,8 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
       const unsigned char* base = smem + slot * SG::BYTES;
       const Tin* sx = reinterpret_cast<const Tin*>(base + SG::OFF_X) + cl;
       const Tin* sdtp = reinterpret_cast<const Tin*>(base + SG::OFF_DT) + cl;
-      const float4* stab = reinterpret_cast<const float4*>(base + SG::OFF_TAB) + g * NS;
+      constexpr int PF4 = SG::TABW / 2;   // table float4 per state pair and step
+      const float4* stab = reinterpret_cast<const float4*>(base + SG::OFF_TAB) + g * NPAIR * PF4;
       const float4* saux = reinterpret_cast<const float4*>(base + SG::OFF_AUX);
       const float4* srot = reinterpret_cast<const float4*>(base + SG::OFF_ROT);
       const int t_sub0 = (s_begin + i) * T_SUB;
@@ -481,15 +543,18 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
       // in the trapezoid mode, the pairs dd0/dd1 carried from the previous step, and row tt + 1
       // of dt; all staged), and the decays' dt broadcast pairs dd0/dd1.
       auto load_step = [&](int tt, StepIn& s, float2& dd0, float2& dd1, bool dd_given) {
-        const float4* trow = stab + tt * N;
+        const float4* trow = stab + tt * (N / 2) * PF4;
 #pragma unroll
-        for (int k = 0; k < 2 * NPAIR; ++k) s.tb[k] = trow[k];
+        for (int q = 0; q < NPAIR; ++q) {
+          s.tb[2 * q] = trow[q * PF4];
+          s.tb[2 * q + 1] = trow[q * PF4 + 1];
+        }
         float2 xx0, xx1;
         PairLoad<Tin>::bcast(sx + tt * DT, sel, swp, xx0, xx1);
         if (!dd_given) PairLoad<Tin>::bcast(sdtp + tt * DT, sel, swp, dd0, dd1);
         s.x = f2(xx0.x, xx1.x);
         s.dv = f2(dd0.x, dd1.x);
-        if (MODE == 0) {
+        if (MODE != 1) {
           s.w0 = mul2(dd0, xx0);
           s.w1 = mul2(dd1, xx1);
           s.pc = f2(0.f, 0.f);
@@ -523,16 +588,29 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
         float2 dd0 = cur.nk, dd1 = cur.no;
         load_step(tt + 1, nxt, dd0, dd1, MODE == 1);
         float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
+        [[maybe_unused]] const float4* zrow = stab + tt * (N / 2) * PF4;   // zero-order hold: this step's row
 #pragma unroll
         for (int q = 0; q < NPAIR; ++q) {
           rn[0][q] = ex2_pair(mul2(dd0, Ap[0][q]));
           rn[1][q] = ex2_pair(mul2(dd1, Ap[1][q]));
           const float4 bt = cur.tb[2 * q];
           const float2 btr = f2(bt.x, bt.y), bti = f2(bt.z, bt.w);
-          kr[0][q] = fma2(rc[0][q], kr[0][q], mul2(cur.w0, btr));
-          ki[0][q] = fma2(rc[0][q], ki[0][q], mul2(cur.w0, bti));
-          kr[1][q] = fma2(rc[1][q], kr[1][q], mul2(cur.w1, btr));
-          ki[1][q] = fma2(rc[1][q], ki[1][q], mul2(cur.w1, bti));
+          if constexpr (MODE == 2) {
+            const float4 dz = zrow[q * PF4 + 2], tz = zrow[q * PF4 + 3];
+            const float2 dr = f2(dz.x, dz.y), di = f2(dz.z, dz.w);
+            const float2 tq = f2(tz.x, tz.y), ntq = f2(-tz.x, -tz.y), t2 = f2(tz.z, tz.w);
+            const float2 fr = mul2(f2(ZOH_TAU_LN2, ZOH_TAU_LN2), btr), fi = mul2(f2(ZOH_TAU_LN2, ZOH_TAU_LN2), bti);
+            // this step's dt broadcast pairs give v = dt A log2 e, the decay's argument
+            const float2 v0 = mul2(f2(cur.dv.x, cur.dv.x), Ap[0][q]);
+            const float2 v1 = mul2(f2(cur.dv.y, cur.dv.y), Ap[1][q]);
+            zoh_update(kr[0][q], ki[0][q], rc[0][q], v0, cur.w0, btr, bti, dr, di, tq, ntq, t2, fr, fi);
+            zoh_update(kr[1][q], ki[1][q], rc[1][q], v1, cur.w1, btr, bti, dr, di, tq, ntq, t2, fr, fi);
+          } else {
+            kr[0][q] = fma2(rc[0][q], kr[0][q], mul2(cur.w0, btr));
+            ki[0][q] = fma2(rc[0][q], ki[0][q], mul2(cur.w0, bti));
+            kr[1][q] = fma2(rc[1][q], kr[1][q], mul2(cur.w1, btr));
+            ki[1][q] = fma2(rc[1][q], ki[1][q], mul2(cur.w1, bti));
+          }
           if (WITH_Y && !CKPT) {
             const float4 ct = cur.tb[2 * q + 1];
             const float2 ctr = f2(ct.x, ct.y), cti = f2(ct.z, ct.w);

@@ -89,7 +89,7 @@ def test_shapes(N, mode, dtype):
 
 @pytest.mark.parametrize("carry", [1, 2])
 @pytest.mark.parametrize("chunk_len", [32, 96])
-@pytest.mark.parametrize("mode,dtype", [(0, "f32"), (1, "bf16"), (1, "f32")])
+@pytest.mark.parametrize("mode,dtype", [(0, "f32"), (1, "bf16"), (1, "f32"), (2, "f32"), (2, "bf16")])
 def test_forced_carry(carry, chunk_len, mode, dtype):
     """Many chunks per row (up to 66), so the serial carry and the windowed look-back (more
     than 32 predecessors) both run."""
@@ -100,14 +100,15 @@ def test_forced_carry(carry, chunk_len, mode, dtype):
 
 
 @pytest.mark.parametrize("carry", [1, 2])
-def test_more_chunks_than_block_slots(carry):
+@pytest.mark.parametrize("mode", [1, 2])
+def test_more_chunks_than_block_slots(carry, mode):
     """More chunk-units (8 rows x 66 chunks) than the GPU holds blocks at once, so later
     chunks start after their predecessors have finished: the decoupled carry then takes the
     predecessor's published final state instead of computing its own aggregate."""
-    w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=8, L=2100, D=24)
+    w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=8, L=2100, D=24, mode=mode)
     inp = wl.generate(w)
     y = gu.run_gpu(gu.to_device(inp), w.mode, carry=carry, chunk_len=32)
-    check(inp, y, f"late-start:carry{carry}")
+    check(inp, y, f"late-start:carry{carry}:m{mode}")
 
 
 def test_dskip_zero():
@@ -171,7 +172,8 @@ def test_lookback_timeout_is_reported(carry):
 @pytest.mark.parametrize("N", [2, 4, 8, 16, 32])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_zoh_shapes(N, dtype):
-    """Mode 2 (its own kernels: time chunks, then the recurrence with y) on ragged shapes."""
+    """Mode 2 (the scan kernel's zero-order-hold step; the small rows run as decoupled time
+    chunks) on ragged shapes."""
     base = wl.WORKLOADS["zoh_bf16_batch"]
     for (B, L, D) in [(1, 1, 8), (2, 13, 8), (1, 95, 24), (2, 300, 72)]:
         w = base.with_shape(B=B, L=L, D=D, N=N, dtype=dtype, seed=base.seed + 13 * N + L)
@@ -186,9 +188,9 @@ def test_zoh_one_chunk_and_small_exponents():
     inp = wl.generate(w)
     check(inp, gu.run_gpu(gu.to_device(inp), w.mode), "zoh:one-chunk", b_rows=[0, 15],
           d_rows=np.array([0, 5, 1000, 2559]))
-    # |z| = |dt A + i theta| around 1e-6 and below: the series branch of (e^z - 1)/z. The
-    # state-space part is then ~1e-5 of the D-skip term, which float32 y could not resolve,
-    # so Dskip = 0 here
+    # |z| = |dt A + i theta| around 1e-6 and below: E from its Taylor polynomial and the weight
+    # held to Bt by the floor of |z|^2. The state-space part is then ~1e-5 of the D-skip term,
+    # which float32 y could not resolve, so Dskip = 0 here
     w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=2, L=200, D=16, dtype="f32", dt_lo=1e-8, dt_hi=1e-6,
                                                   theta_max=1e-6)
     inp = wl.generate(w)
