@@ -521,12 +521,13 @@ def traffic_from_profiles(workload: str):
 
 
 # ------------------------------------------------------------------------------ MIMO workloads
-def mimo_alu_ops_per_elem(P: int) -> float:
-    """FP32 lane-operations per (b,t,h,p,n) element of csscan_forward_mimo, counted from its
-    source: the rank-P injection and the output each cost 2 per element; the decay exponent (1),
-    the transition (2), the trapezoid injection (~8) and the update (4) are per (b,t,h,n),
-    shared by the P channels."""
-    return 4.0 + 15.0 / P
+def mimo_alu_ops_per_elem(P: int, mode: int) -> float:
+    """FP32 lane-operations per (b,t,h,p,n) element of csscan_forward_mimo's output kernel,
+    counted from its source (rotating frame, state pairs): the rank-P injection 2 and the output
+    2.5 (its packed product and the sum of the pair) per element; the decay exponent (1) and
+    the update (exp-Euler 2; trapezoid 6: g, then k with the look-ahead) per (b,t,h,n), shared
+    by the P channels."""
+    return 4.5 + (7.0 if mode == 1 else 3.0) / P
 
 
 def mimo_cpu_sample(inp, target_s: float):
@@ -655,7 +656,7 @@ def run_mimo(args):
     hbm_peak, sm_max_mhz, peak_kind = measured_peaks()
     mean_s = statistics.mean(call_ms) / 1e3
     alu_peak = FP32_LANES_PER_SM * N_SM * sm_max_mhz * 1e6 / 1e12
-    ops = mimo_alu_ops_per_elem(w.P)
+    ops = mimo_alu_ops_per_elem(w.P, w.mode)
     alu = ops * w.elements / mean_s / 1e12
     gbs = w.min_bytes() / mean_s / 1e9
     cpu = None
@@ -664,7 +665,8 @@ def run_mimo(args):
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "seconds": secs}
     import torch as _t
     nsm = _t.cuda.get_device_properties(local).multi_processor_count
-    launches = 2 if w.B * w.H * w.N * w.P >= nsm * 4096 else 4
+    # phase table and output pass; with time chunks also the e^{i theta} table, the chunk pass and the sweep
+    launches = 2 if w.B * w.H * w.N * w.P >= nsm * 4096 else 5
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic", "config": dict(mimo_config(w), l2=l2_note),

@@ -542,7 +542,7 @@ int launch_mimo(const MimoArgs& a, cudaStream_t st) {
   const size_t rot_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float2), 256);
   const size_t chunk_bytes = C > 1 ? size_t(a.B * C * a.H * N) * 2 * sizeof(float2) : 0;
   WsEntry ws;
-  int rc = get_workspace(dev, st, 1, rot_bytes + chunk_bytes, &ws);
+  int rc = get_workspace(dev, st, 1, rot_bytes + chunk_bytes + rot_bytes, &ws);
   if (rc != CSSCAN_OK) return rc;
   char* rest = static_cast<char*>(ws.base) + HDR_BYTES + align_up(ws.flag_cap * 4, 256);
   mimo::Params p;
@@ -554,6 +554,7 @@ int launch_mimo(const MimoArgs& a, cudaStream_t st) {
   p.A = a.A;
   p.Dskip = a.Dskip;
   p.y = a.y;
+  p.phase = reinterpret_cast<const float2*>(rest + rot_bytes + chunk_bytes);
   p.rot = reinterpret_cast<const float2*>(rest);
   p.chunk = C > 1 ? reinterpret_cast<float2*>(rest + rot_bytes) : nullptr;
   p.B = int(a.B);
@@ -566,10 +567,15 @@ int launch_mimo(const MimoArgs& a, cudaStream_t st) {
   const long long n_rot = (long long)a.B * a.L * N;
   const long long n_thr = (long long)a.B * C * a.H * N;
   if (!grid_fits(n_rot) || !grid_fits(n_thr)) return CSSCAN_ERR_UNSUPPORTED;
-  mimo::mimo_rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest),
-                                                                           n_rot);
+  const long long n_ph = (long long)a.B * ((a.L + G - 1) / G) * N;
+  mimo::mimo_phase_kernel<Tin><<<unsigned((n_ph + 255) / 256), 256, 0, st>>>(
+      a.theta, reinterpret_cast<float2*>(rest + rot_bytes + chunk_bytes), int(a.L), N, n_ph);
   CSSCAN_CUDA(cudaGetLastError());
   if (C > 1) {
+    // the time-chunk pass reads e^{i theta} per step
+    mimo::mimo_rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest),
+                                                                             n_rot);
+    CSSCAN_CUDA(cudaGetLastError());
     mimo::mimo_chunk_kernel<Tin, MODE, P><<<unsigned((n_thr + 255) / 256), 256, 0, st>>>(p);
     CSSCAN_CUDA(cudaGetLastError());
     mimo::mimo_combine_kernel<<<unsigned((rows + 255) / 256), 256, 0, st>>>(p);

@@ -7,17 +7,17 @@
 //   y[b,t,h,p] = Re(sum_n Cm[b,t,n,p] h_t[n]) + Dskip[h,p] x[b,t,h,p]
 //
 // "Mamba-3 paper story" (MIMO section) widens B and C to N x P so that one state serves P
-// channels: per state and step the work grows with P while the state's traffic does not. The
-// kernels mirror the zero-order-hold ones:
-//   mimo_rot_kernel     e^{i theta} per (b, t, n)
+// channels: per state and step the work grows with P while the state's traffic does not.
+//   mimo_rot_kernel     e^{i theta} per (b, t, n)                          (chunks > 1 only)
 //   mimo_chunk_kernel   per (b, c, h, n): the chunk's end state from a zero entry state and
 //                       the product of a over the chunk                     (chunks > 1 only)
 //   mimo_combine_kernel per (b, h, n): each chunk's entry state
-//   mimo_out_kernel     blocks of OUT_THREADS / N heads of one (b, c), a thread per (head, n): the
-//                       recurrence over the chunk with y, each 8-step group's shared inputs
-//                       staged in shared memory first; each lane keeps its P partial outputs
-//                       for the group and a reduce-scatter over the head's N lanes leaves
-//                       every (step, channel) sum in one lane
+//   mimo_out_kernel     blocks of heads of one (b, c), a thread per (head, state pair): the
+//                       recurrence over the chunk with y in a rotating frame (real decay),
+//                       each 8-step group's rotated Bm, Cm and its x, dt staged in shared
+//                       memory first; each lane keeps its P partial outputs for the group and
+//                       a reduce-scatter over the head's lanes leaves every (step, channel)
+//                       sum in one lane
 #pragma once
 
 #include "device_util.cuh"
@@ -46,7 +46,8 @@ struct Params {
   const float* A;      // (H, N)
   const float* Dskip;  // (H, P)
   float* y;            // (B, L, H, P)
-  const float2* rot;   // (B, L, N)
+  const float2* phase; // (B, L, N): e^{i Phi_t}, Phi from the step's group start (mimo_phase_kernel)
+  const float2* rot;   // (B, L, N): e^{i theta} (time-chunk pass only)
   float2* chunk;       // (B, C, H, N, 2): end state | entry state, product of a
   int B, L, H, N, P;
   int TC, C;
@@ -59,6 +60,28 @@ __global__ void __launch_bounds__(256) mimo_rot_kernel(const void* theta, float2
   float s, c;
   sincosf(load_in<Tin>(static_cast<const Tin*>(theta), i), &s, &c);
   rot[i] = make_float2(c, s);
+}
+
+// e^{i Phi_t} per (b, t, n), Phi_t the sum of theta from the first step of t's GROUP-step
+// group (groups aligned to multiples of GROUP) through t: the rotating frame of mimo_out_kernel.
+template <typename Tin>
+__global__ void __launch_bounds__(256) mimo_phase_kernel(const void* theta, float2* ph, int L, int N, long long total) {
+  const long long i = (long long)blockIdx.x * 256 + threadIdx.x;   // (b, group, n)
+  if (i >= total) return;
+  const int n = int(i % N);
+  const long long bg = i / N;
+  const int G = (L + GROUP - 1) / GROUP;
+  const long long b = bg / G;
+  const int t0 = int(bg % G) * GROUP;
+  const Tin* th = static_cast<const Tin*>(theta);
+  float phi = 0.f;
+  for (int t = t0; t < min(t0 + GROUP, L); ++t) {
+    const long long e = (b * L + t) * N + n;
+    phi += load_in<Tin>(th, e);
+    float s, c;
+    sincosf(phi, &s, &c);
+    ph[e] = make_float2(c, s);
+  }
 }
 
 struct Thread {
@@ -175,42 +198,42 @@ __global__ void __launch_bounds__(256) mimo_combine_kernel(const Params p) {
   }
 }
 
-// The recurrence over chunk c with y. A block owns HB = OUT_THREADS / N heads of one (b, c): thread
-// (head hl, state n), the N lanes of a head neighbours in a warp (N <= 32). For each group of
-// GROUP steps the block first stages, coalesced, what its lanes share -- e^{i theta}, Bm and Cm
-// per (t, n), x and dt per (t, head), lam per t -- in shared memory. Each lane then keeps its P
-// partial outputs for the group and a reduce-scatter over the head's N lanes leaves every
-// (step, channel) sum in one lane. Grid: (ceil(H / HB), C, B).
+// The recurrence over chunk c with y, in a rotating frame. A block owns HB = OUT_THREADS / NPT
+// heads of one (b, c), NPT = N / 2 threads per head; thread (head hl, state pair g) holds the
+// states 2g, 2g + 1 as packed float32x2. Within each group of GROUP steps, Phi_t is the sum of
+// theta from the group's first step, and with g_t = e^{-i Phi_t} h_t the decay is real. For
+// each group the block first stages what its lanes share: per (t, channel, state pair)
+// Bt = e^{-i Phi_t} Bm and Ct = e^{+i Phi_t} Cm, e^{i Phi} after the group's last step (the
+// frame reset), per (t, head) x and dt (one step more for the trapezoid's look-ahead) and
+// per t lam. The trapezoid carries k_t = g_{t-1} + mu_t V_{t-1} with
+// mu_t = (1 - lam_t) dt_t, q_t = lam_t dt_t and V_t = sum_p x_t[p] Bt_t[p]:
+//     g_t = r_t k_t + q_t V_t,   k_{t+1} = g_t + mu_{t+1} V_t,   y_t[p] = Re(sum_n Ct_t[n,p] g_t) + Dskip x_t[p],
+// with mu_{t+1} = 0 at the chunk's last step (exp-Euler: q = dt, mu = 0, k = g), so that per
+// state and step the work is the rank-P injection and the P outputs on state pairs. Each lane keeps
+// its P partial outputs of the group's steps; a reduce-scatter over the head's NPT lanes then
+// leaves every (step, channel) sum in one lane. Grid: (ceil(H / HB), C, B).
 template <int N, int P> struct MimoStage {
-  static constexpr int HB = OUT_THREADS / N;               // heads per block
-  static constexpr int TN = GROUP * N;                     // (t, n) entries of a group
-  static constexpr int TH = GROUP * HB;                    // (t, head) entries of a group
-  static constexpr int OFF_ROT = 0;                        // float2 [GROUP][N]
-  static constexpr int OFF_BM = OFF_ROT + TN * 8;          // float2 [GROUP][N][P]
-  static constexpr int OFF_CM = OFF_BM + TN * P * 8;       // float2 [GROUP][N][P]
-  static constexpr int OFF_X = OFF_CM + TN * P * 8;        // float [GROUP][HB][P]
-  static constexpr int OFF_DT = OFF_X + TH * P * 4;        // float [GROUP][HB]
-  static constexpr int OFF_LAM = OFF_DT + TH * 4;          // float [GROUP]
-  static constexpr int BYTES = OFF_LAM + GROUP * 4;
+  static_assert(N >= 2 && N <= 32, "mimo_out_kernel handles N = 2 .. 32");
+  static constexpr int NPT = N / 2;                        // threads (state pairs) per head
+  static constexpr int HB = OUT_THREADS / NPT;             // heads per block
 };
 
 template <typename Tin, int MODE, int N, int P>
 __global__ void __launch_bounds__(OUT_THREADS, OutOcc<P>::MIN_BLOCKS) mimo_out_kernel(const Params p) {
   using MS = MimoStage<N, P>;
-  constexpr int HB = MS::HB;
+  constexpr int NPT = MS::NPT, HB = MS::HB;
   constexpr int E = GROUP * P;                   // (step, channel) entries of one group
-  constexpr int HOLD = E >= N ? E / N : 1;
-  constexpr int DUP = N > E ? N / E : 1;
-  __shared__ __align__(16) unsigned char sm[MS::BYTES];
-  float2 (*s_rot)[N] = reinterpret_cast<float2 (*)[N]>(sm + MS::OFF_ROT);
-  float2 (*s_bm)[N][P] = reinterpret_cast<float2 (*)[N][P]>(sm + MS::OFF_BM);
-  float2 (*s_cm)[N][P] = reinterpret_cast<float2 (*)[N][P]>(sm + MS::OFF_CM);
-  float (*s_x)[HB][P] = reinterpret_cast<float (*)[HB][P]>(sm + MS::OFF_X);
-  float (*s_dt)[HB] = reinterpret_cast<float (*)[HB]>(sm + MS::OFF_DT);
-  float* s_lam = reinterpret_cast<float*>(sm + MS::OFF_LAM);
+  constexpr int HOLD = E >= NPT ? E / NPT : 1;
+  constexpr int DUP = NPT > E ? NPT / E : 1;
+  __shared__ float4 s_bt[GROUP][P][N / 2];       // (Btr_n, Btr_n+1, Bti_n, Bti_n+1)
+  __shared__ float4 s_ct[GROUP][P][N / 2];       // (Ctr_n, Ctr_n+1, -Cti_n, -Cti_n+1)
+  __shared__ float2 s_rs[N];                     // e^{i Phi} after the group's last step
+  __shared__ __align__(16) float s_x[GROUP][HB][P];
+  __shared__ float s_dt[GROUP + 1][HB];
+  __shared__ float s_lam[GROUP + 1];
 
   const int tid = threadIdx.x;
-  const int n = tid % N, hl = tid / N;
+  const int g = tid % NPT, hl = tid / NPT;
   const int h0 = blockIdx.x * HB;
   const int h = h0 + hl;
   const bool valid = h < p.H;
@@ -222,94 +245,108 @@ __global__ void __launch_bounds__(OUT_THREADS, OutOcc<P>::MIN_BLOCKS) mimo_out_k
   const Tin* BM = static_cast<const Tin*>(p.Bm);
   const Tin* CM = static_cast<const Tin*>(p.Cm);
   const Tin* LAM = static_cast<const Tin*>(p.lam);
-  const float a2 = p.A[(long long)hc * N + n] * LOG2E;
-  float Ds[P];
-#pragma unroll
-  for (int q = 0; q < P; ++q) Ds[q] = p.Dskip[(long long)hc * P + q];
+  const float2 A2 = f2(p.A[(long long)hc * N + 2 * g] * LOG2E, p.A[(long long)hc * N + 2 * g + 1] * LOG2E);
   const int tc = c * p.TC, te = min(p.L, tc + p.TC);
-  float hr = 0.f, hi = 0.f;
+
+  // k at the chunk's first step, in the standard frame: h_in + mu_tc v_{tc-1}
+  float2 kr = f2(0.f, 0.f), ki = f2(0.f, 0.f);
   if (p.C > 1 && valid) {
-    const float2 hin = rec_of(p, b, c, h, n)[0];
-    hr = hin.x;
-    hi = hin.y;
+    const float2 e0 = rec_of(p, b, c, h, 2 * g)[0], e1 = rec_of(p, b, c, h, 2 * g + 1)[0];
+    kr = f2(e0.x, e1.x);
+    ki = f2(e0.y, e1.y);
   }
-  float2 vp = valid ? v_before<Tin, MODE, P>(p, b, tc, hc, n) : make_float2(0.f, 0.f);
+  if (MODE == 1 && tc > 0 && valid) {
+    const float mu = (1.f - load_in<Tin>(LAM, b * p.L + tc)) * load_in<Tin>(DT, (b * p.L + tc) * p.H + h);
+    const float2 v0 = v_before<Tin, MODE, P>(p, b, tc, h, 2 * g), v1 = v_before<Tin, MODE, P>(p, b, tc, h, 2 * g + 1);
+    kr = fma2(f2(mu, mu), f2(v0.x, v1.x), kr);
+    ki = fma2(f2(mu, mu), f2(v0.y, v1.y), ki);
+  }
+
   for (int t0 = tc; t0 < te; t0 += GROUP) {
     const int ng = min(GROUP, te - t0);
-    // ---- stage the group (steps past te or heads past H as zeros)
-    for (int k = tid; k < GROUP * N * P; k += OUT_THREADS) {
-      const int i = k / (N * P), r = k % (N * P);
-      float2 bb = make_float2(0.f, 0.f), cc = make_float2(0.f, 0.f);
-      if (i < ng) {
-        const long long e = ((b * p.L + t0 + i) * N) * P + r;   // entry (t, n, q), n * P + q = r
-        bb = load_pair<Tin>(BM, e);
-        cc = load_pair<Tin>(CM, e);
-      }
-      (&s_bm[0][0][0])[k] = bb;
-      (&s_cm[0][0][0])[k] = cc;
-    }
+    // ---- stage the group (steps past te and heads past H as zeros, so that those steps
+    // leave k unchanged and add nothing)
     for (int k = tid; k < GROUP * N; k += OUT_THREADS) {
-      const int i = k / N, nn = k % N;
-      s_rot[i][nn] = i < ng ? p.rot[(b * p.L + t0 + i) * N + nn] : make_float2(0.f, 0.f);
+      const int i = k / N, n = k % N;
+      const float2 ph = i < ng ? p.phase[(b * p.L + t0 + i) * N + n] : f2(1.f, 0.f);
+      const float cs = ph.x, sn = ph.y;
+      if (i == ng - 1) s_rs[n] = ph;
+      const int q = n >> 1, odd = n & 1;
+#pragma unroll
+      for (int pp = 0; pp < P; ++pp) {
+        float2 bb = f2(0.f, 0.f), cc = f2(0.f, 0.f);
+        if (i < ng) {
+          const long long e = ((b * p.L + t0 + i) * N + n) * P + pp;
+          bb = load_pair<Tin>(BM, e);
+          cc = load_pair<Tin>(CM, e);
+        }
+        float* bt = reinterpret_cast<float*>(&s_bt[i][pp][q]);
+        bt[odd] = cs * bb.x + sn * bb.y;
+        bt[2 + odd] = cs * bb.y - sn * bb.x;
+        float* ct = reinterpret_cast<float*>(&s_ct[i][pp][q]);
+        ct[odd] = cs * cc.x - sn * cc.y;
+        ct[2 + odd] = -(cs * cc.y + sn * cc.x);
+      }
     }
     for (int k = tid; k < GROUP * HB * P; k += OUT_THREADS) {
       const int i = k / (HB * P), r = k % (HB * P), hh = h0 + r / P;
       (&s_x[0][0][0])[k] = (i < ng && hh < p.H) ? load_in<Tin>(X, ((b * p.L + t0 + i) * p.H + h0) * P + r) : 0.f;
     }
-    for (int k = tid; k < GROUP * HB; k += OUT_THREADS) {
+    for (int k = tid; k < (GROUP + 1) * HB; k += OUT_THREADS) {
       const int i = k / HB, r = k % HB;
-      s_dt[i][r] = (i < ng && h0 + r < p.H) ? load_in<Tin>(DT, (b * p.L + t0 + i) * p.H + h0 + r) : 0.f;
+      s_dt[i][r] = (t0 + i < te && h0 + r < p.H) ? load_in<Tin>(DT, (b * p.L + t0 + i) * p.H + h0 + r) : 0.f;
     }
-    if (MODE == 1 && tid < GROUP) s_lam[tid] = tid < ng ? load_in<Tin>(LAM, b * p.L + t0 + tid) : 0.f;
+    if (MODE == 1 && tid <= GROUP) s_lam[tid] = t0 + tid < te ? load_in<Tin>(LAM, b * p.L + t0 + tid) : 0.f;
     __syncthreads();
 
     float part[1][E];
 #pragma unroll
     for (int i = 0; i < GROUP; ++i) {
+      const float dtt = s_dt[i][hl];
+      const float2 r = ex2_pair(mul2(f2(dtt, dtt), A2));
+      // exp-Euler: w = dt x, g = k; trapezoid: V = sum_p x Bt, g = r k + q V, k = g + mu V
+      const float wq = MODE == 1 ? 1.f : dtt;
+      float2 sr = f2(0.f, 0.f), si = f2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < P; ++q) part[0][i * P + q] = 0.f;
-      if (i < ng) {
-        float vr = 0.f, vi = 0.f;
+      for (int pp = 0; pp < P; ++pp) {
+        const float w = wq * s_x[i][hl][pp];
+        const float4 bt = s_bt[i][pp][g];
+        sr = fma2(f2(w, w), f2(bt.x, bt.y), sr);
+        si = fma2(f2(w, w), f2(bt.z, bt.w), si);
+      }
+      float2 gr, gi;
+      if (MODE == 1) {
+        const float q = s_lam[i] * dtt, mu1 = (1.f - s_lam[i + 1]) * s_dt[i + 1][hl];
+        gr = fma2(r, kr, mul2(f2(q, q), sr));
+        gi = fma2(r, ki, mul2(f2(q, q), si));
+        kr = fma2(f2(mu1, mu1), sr, gr);
+        ki = fma2(f2(mu1, mu1), si, gi);
+      } else {
+        kr = fma2(r, kr, sr);
+        ki = fma2(r, ki, si);
+        gr = kr;
+        gi = ki;
+      }
 #pragma unroll
-        for (int q = 0; q < P; ++q) {
-          const float2 bb = s_bm[i][n][q];
-          vr = fmaf(bb.x, s_x[i][hl][q], vr);
-          vi = fmaf(bb.y, s_x[i][hl][q], vi);
-        }
-        const float dtt = s_dt[i][hl];
-        const float2 ro = s_rot[i][n];
-        const float r = ex2_approx(dtt * a2);
-        const float ar = r * ro.x, ai = r * ro.y;
-        float ur, ui;
-        if (MODE == 0) {
-          ur = dtt * vr;
-          ui = dtt * vi;
-        } else {
-          const float lm = s_lam[i];
-          const float c1 = lm * dtt, c2 = (1.f - lm) * dtt;
-          ur = c1 * vr + c2 * (ar * vp.x - ai * vp.y);
-          ui = c1 * vi + c2 * (ar * vp.y + ai * vp.x);
-          vp = make_float2(vr, vi);
-        }
-        const float nr = fmaf(ar, hr, fmaf(-ai, hi, ur));
-        const float ni = fmaf(ar, hi, fmaf(ai, hr, ui));
-        hr = nr;
-        hi = ni;
-#pragma unroll
-        for (int q = 0; q < P; ++q) {
-          const float2 cc = s_cm[i][n][q];
-          float o = cc.x * hr - cc.y * hi;
-          if (n == 0) o = fmaf(Ds[q], s_x[i][hl][q], o);
-          part[0][i * P + q] = o;
-        }
+      for (int pp = 0; pp < P; ++pp) {
+        const float4 ct = s_ct[i][pp][g];
+        const float2 o = fma2(f2(ct.x, ct.y), gr, mul2(f2(ct.z, ct.w), gi));
+        part[0][i * P + pp] = o.x + o.y;
       }
     }
-    const int base = butterfly<N, 1, E>(part, n);
-    if ((n % DUP) == 0 && valid) {
+    {  // frame reset: back to the standard frame after the group's last step
+      const float2 e0 = s_rs[2 * g], e1 = s_rs[2 * g + 1];
+      const float2 cc = f2(e0.x, e1.x), ss = f2(e0.y, e1.y), nss = f2(-e0.y, -e1.y);
+      const float2 nr = fma2(cc, kr, mul2(nss, ki)), ni = fma2(cc, ki, mul2(ss, kr));
+      kr = nr;
+      ki = ni;
+    }
+    const int base = butterfly<NPT, 1, E>(part, g);
+    if ((g % DUP) == 0 && valid) {
 #pragma unroll
       for (int k = 0; k < HOLD; ++k) {
-        const int e = base + k, i = e / P, q = e % P;
-        if (i < ng) p.y[((b * p.L + t0 + i) * p.H + h) * P + q] = part[0][k];
+        const int e = base + k, i = e / P, pp = e % P;
+        if (i < ng) p.y[((b * p.L + t0 + i) * p.H + h) * P + pp] = fmaf(p.Dskip[(long long)h * P + pp], s_x[i][hl][pp], part[0][k]);
       }
     }
     __syncthreads();
