@@ -26,14 +26,14 @@ namespace csscan {
 namespace mimo {
 
 constexpr int GROUP = 8;
-// Threads per block of mimo_out_kernel. Blocks of 128 threads compiled for 9 resident
-// blocks per SM (56 registers) hold 1152 threads per SM, so 16 x 640 x 16 (b, head, n) rows
-// run in one wave; 256-thread blocks at 64 registers held 1024 and needed a second, 8 %
-// full wave (11.5 -> 8.4 ms). With P = 8 the 56-register cap spills the 64 partial outputs,
-// so those kernels keep 128 registers (4 blocks).
+// Threads per block of mimo_out_kernel and the resident blocks per SM it is compiled for:
+// 128-thread blocks at 5 per SM (96 registers, room for the next group's loads in flight
+// without spills; 80 registers spilled and ran 6 % slower) hold 640 threads per SM, so the
+// 16 x 640 x 16 / 2 (b, head, state pair) threads of the large-batch MIMO workload run in one
+// wave; with P = 8 the 64 partial outputs per lane need 128 registers (4 blocks).
 constexpr int OUT_THREADS = 128;
 template <int P> struct OutOcc {
-  static constexpr int MIN_BLOCKS = P <= 4 ? 9 : 4;
+  static constexpr int MIN_BLOCKS = P <= 4 ? 5 : 4;
 };
 constexpr float LOG2E = 1.4426950408889634f;
 
@@ -262,42 +262,83 @@ __global__ void __launch_bounds__(OUT_THREADS, OutOcc<P>::MIN_BLOCKS) mimo_out_k
     ki = fma2(f2(mu, mu), f2(v0.y, v1.y), ki);
   }
 
-  for (int t0 = tc; t0 < te; t0 += GROUP) {
+  // Staging, split so that a group's global loads are in flight while the previous group is
+  // computed: `fetch` loads this thread's share of a group into registers (steps past te and
+  // heads past H as zeros, so that those steps leave k unchanged and add nothing), `commit`
+  // rotates Bm and Cm into the group's frame and stores everything in shared memory.
+  constexpr int RIT = (GROUP * N + OUT_THREADS - 1) / OUT_THREADS;
+  constexpr int XIT = (GROUP * HB * P + OUT_THREADS - 1) / OUT_THREADS;
+  constexpr int DIT = ((GROUP + 1) * HB + OUT_THREADS - 1) / OUT_THREADS;
+  float2 f_ph[RIT], f_bm[RIT][P], f_cm[RIT][P];
+  float f_x[XIT], f_dt[DIT], f_lam = 0.f;
+  auto fetch = [&](int t0) {
     const int ng = min(GROUP, te - t0);
-    // ---- stage the group (steps past te and heads past H as zeros, so that those steps
-    // leave k unchanged and add nothing)
-    for (int k = tid; k < GROUP * N; k += OUT_THREADS) {
-      const int i = k / N, n = k % N;
-      const float2 ph = i < ng ? p.phase[(b * p.L + t0 + i) * N + n] : f2(1.f, 0.f);
-      const float cs = ph.x, sn = ph.y;
-      if (i == ng - 1) s_rs[n] = ph;
-      const int q = n >> 1, odd = n & 1;
+#pragma unroll
+    for (int it = 0; it < RIT; ++it) {
+      const int k = tid + it * OUT_THREADS, i = k / N, n = k % N;
+      const bool ok = k < GROUP * N && i < ng;
+      f_ph[it] = ok ? p.phase[(b * p.L + t0 + i) * N + n] : f2(1.f, 0.f);
 #pragma unroll
       for (int pp = 0; pp < P; ++pp) {
-        float2 bb = f2(0.f, 0.f), cc = f2(0.f, 0.f);
-        if (i < ng) {
-          const long long e = ((b * p.L + t0 + i) * N + n) * P + pp;
-          bb = load_pair<Tin>(BM, e);
-          cc = load_pair<Tin>(CM, e);
-        }
-        float* bt = reinterpret_cast<float*>(&s_bt[i][pp][q]);
-        bt[odd] = cs * bb.x + sn * bb.y;
-        bt[2 + odd] = cs * bb.y - sn * bb.x;
-        float* ct = reinterpret_cast<float*>(&s_ct[i][pp][q]);
-        ct[odd] = cs * cc.x - sn * cc.y;
-        ct[2 + odd] = -(cs * cc.y + sn * cc.x);
+        const long long e = ((b * p.L + t0 + i) * N + n) * P + pp;
+        f_bm[it][pp] = ok ? load_pair<Tin>(BM, e) : f2(0.f, 0.f);
+        f_cm[it][pp] = ok ? load_pair<Tin>(CM, e) : f2(0.f, 0.f);
       }
     }
-    for (int k = tid; k < GROUP * HB * P; k += OUT_THREADS) {
-      const int i = k / (HB * P), r = k % (HB * P), hh = h0 + r / P;
-      (&s_x[0][0][0])[k] = (i < ng && hh < p.H) ? load_in<Tin>(X, ((b * p.L + t0 + i) * p.H + h0) * P + r) : 0.f;
+#pragma unroll
+    for (int it = 0; it < XIT; ++it) {
+      const int k = tid + it * OUT_THREADS, i = k / (HB * P), r = k % (HB * P), hh = h0 + r / P;
+      f_x[it] = (k < GROUP * HB * P && i < ng && hh < p.H) ? load_in<Tin>(X, ((b * p.L + t0 + i) * p.H + h0) * P + r) : 0.f;
     }
-    for (int k = tid; k < (GROUP + 1) * HB; k += OUT_THREADS) {
-      const int i = k / HB, r = k % HB;
-      s_dt[i][r] = (t0 + i < te && h0 + r < p.H) ? load_in<Tin>(DT, (b * p.L + t0 + i) * p.H + h0 + r) : 0.f;
+#pragma unroll
+    for (int it = 0; it < DIT; ++it) {
+      const int k = tid + it * OUT_THREADS, i = k / HB, r = k % HB;
+      f_dt[it] = (k < (GROUP + 1) * HB && t0 + i < te && h0 + r < p.H)
+                     ? load_in<Tin>(DT, (b * p.L + t0 + i) * p.H + h0 + r) : 0.f;
     }
-    if (MODE == 1 && tid <= GROUP) s_lam[tid] = t0 + tid < te ? load_in<Tin>(LAM, b * p.L + t0 + tid) : 0.f;
-    __syncthreads();
+    if (MODE == 1 && tid <= GROUP) f_lam = t0 + tid < te ? load_in<Tin>(LAM, b * p.L + t0 + tid) : 0.f;
+  };
+  auto commit = [&](int t0) {
+    const int ng = min(GROUP, te - t0);
+#pragma unroll
+    for (int it = 0; it < RIT; ++it) {
+      const int k = tid + it * OUT_THREADS, i = k / N, n = k % N;
+      if (k < GROUP * N) {
+        const float cs = f_ph[it].x, sn = f_ph[it].y;
+        if (i == ng - 1) s_rs[n] = f_ph[it];
+        const int q = n >> 1, odd = n & 1;
+#pragma unroll
+        for (int pp = 0; pp < P; ++pp) {
+          const float2 bb = f_bm[it][pp], cc = f_cm[it][pp];
+          float* bt = reinterpret_cast<float*>(&s_bt[i][pp][q]);
+          bt[odd] = cs * bb.x + sn * bb.y;
+          bt[2 + odd] = cs * bb.y - sn * bb.x;
+          float* ct = reinterpret_cast<float*>(&s_ct[i][pp][q]);
+          ct[odd] = cs * cc.x - sn * cc.y;
+          ct[2 + odd] = -(cs * cc.y + sn * cc.x);
+        }
+      }
+    }
+#pragma unroll
+    for (int it = 0; it < XIT; ++it) {
+      const int k = tid + it * OUT_THREADS;
+      if (k < GROUP * HB * P) (&s_x[0][0][0])[k] = f_x[it];
+    }
+#pragma unroll
+    for (int it = 0; it < DIT; ++it) {
+      const int k = tid + it * OUT_THREADS;
+      if (k < (GROUP + 1) * HB) (&s_dt[0][0])[k] = f_dt[it];
+    }
+    if (MODE == 1 && tid <= GROUP) s_lam[tid] = f_lam;
+  };
+
+  fetch(tc);
+  commit(tc);
+  __syncthreads();
+  for (int t0 = tc; t0 < te; t0 += GROUP) {
+    const int ng = min(GROUP, te - t0);
+    const bool more = t0 + GROUP < te;
+    if (more) fetch(t0 + GROUP);
 
     float part[1][E];
 #pragma unroll
@@ -350,6 +391,10 @@ __global__ void __launch_bounds__(OUT_THREADS, OutOcc<P>::MIN_BLOCKS) mimo_out_k
       }
     }
     __syncthreads();
+    if (more) {
+      commit(t0 + GROUP);
+      __syncthreads();
+    }
   }
 }
 
