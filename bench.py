@@ -490,22 +490,24 @@ def measure_backward(w: wl.Workload, dev: dict, stream, steps: int) -> dict:
 
 KERNEL_SOURCES = ("selective_state_space_diagonal_b300/csrc/scan_kernels.cuh",
                   "selective_state_space_diagonal_b300/csrc/device_util.cuh")
+MIMO_KERNEL_SOURCES = ("selective_state_space_diagonal_b300/csrc/mimo_kernels.cuh",
+                       "selective_state_space_diagonal_b300/csrc/device_util.cuh")
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(workload: str):
-    """DRAM bytes per scan-kernel launch from the committed ncu summary of this workload
-    (profiles/scan_kernel_<workload>.md), or None when there is none or it was taken on
-    other kernel sources than the ones built now."""
-    path = os.path.join(ROOT, "profiles", f"scan_kernel_{workload}.md")
+def traffic_from_profiles(workload: str, kernel: str = "scan_kernel", sources=KERNEL_SOURCES):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of this workload
+    (profiles/<kernel>_<workload>.md), or None when there is none or it was taken on other
+    kernel sources than the ones built now."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         vals = {}
         with open(path) as f:
@@ -513,7 +515,7 @@ def traffic_from_profiles(workload: str):
                 if ":" in line and line.split(":", 1)[0].strip() in ("kernel_source_sha256_16", "dram_bytes_per_launch"):
                     k, v = line.split(":", 1)
                     vals[k.strip()] = v.strip()
-        if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        if vals.get("kernel_source_sha256_16") != kernel_source_hash(sources):
             return None
         return int(vals["dram_bytes_per_launch"])
     except Exception:
@@ -671,7 +673,8 @@ def run_mimo(args):
             "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic", "config": dict(mimo_config(w), l2=l2_note),
             "roofline": {"bound": "alu", "achieved": alu, "peak": alu_peak, "unit": "Tops/s", "frac": alu / alu_peak,
-                         "traffic": None, "kernel": "mimo_out_kernel (+ table and chunk passes)",
+                         "traffic": traffic_from_profiles(w.name, "mimo_out_kernel", MIMO_KERNEL_SOURCES),
+                         "kernel": "mimo_out_kernel (+ table and chunk passes)",
                          "ms_per_launch": 1e3 * mean_s,
                          "peak_note": f"FP32 pipe: {FP32_LANES_PER_SM} lanes/SM x {N_SM} SMs x {sm_max_mhz:.0f} MHz; "
                                       f"{ops:.2f} lane-ops per element"},

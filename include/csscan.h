@@ -83,8 +83,8 @@ enum {
  *   EXP_TRAPEZOID beta_t = (1 - lam_t) dt_t a_t on Bc_{t-1} x_{t-1}, gamma_t = lam_t dt_t
  *   ZOH           gamma_t = dt_t (e^{z_t} - 1) / z_t with z_t = dt_t A + i theta_t (the table's
  *                 A^{-1}(exp(dt A) - I) with the complex exponent of a_t in place of dt A);
- *                 csscan_forward and csscan_forward_ex only (without initial state or halo),
- *                 N <= 32; the other entry points return CSSCAN_ERR_UNSUPPORTED for it */
+ *                 csscan_forward, csscan_forward_ex and csscan_forward_state, N <= 32; the
+ *                 other entry points return CSSCAN_ERR_UNSUPPORTED for it */
 typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1, CSSCAN_MODE_ZOH = 2 } csscan_mode_t;
 typedef enum { CSSCAN_F32 = 0, CSSCAN_BF16 = 1 } csscan_dtype_t;
 
@@ -144,7 +144,7 @@ int csscan_forward_ex(const void* x, const void* delta, const float* A, const vo
  * scan", section 并行扫描的数学本质) that makes the pieces compose exactly.
  * Arguments as csscan_forward, plus:
  *   h0      : device float32 (B, D, N, 2), the state h_{-1} before the first step, or NULL for zero
- *   x_prev, Bc_prev : trapezoid mode only (ignored in exp-Euler mode): the step before the first,
+ *   x_prev, Bc_prev : trapezoid mode only (ignored in the exp-Euler and zero-order-hold modes): the step before the first,
  *             x (B, D) and Bc (B, N, 2) in `dtype`, which the first step's beta term uses;
  *             both NULL means there is no previous step (Bc_{-1} x_{-1} = 0); one NULL is invalid
  *   h_last  : device float32 (B, D, N, 2), receives h_{L-1}, or NULL

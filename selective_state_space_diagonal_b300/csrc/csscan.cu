@@ -416,8 +416,7 @@ csscan_options_t default_options() {
 int forward_impl(const Args& a, const csscan_options_t* opts, cudaStream_t st) {
   csscan_options_t o = opts ? *opts : default_options();
   if (a.mode == CSSCAN_MODE_ZOH) {
-    // the zero-order-hold scan starts from the zero state (no h0, final state or halo)
-    if (a.h0 || a.h_last || a.x_prev || a.Bc_prev) return CSSCAN_ERR_UNSUPPORTED;
+    // initial and final state as in exp-Euler; the trapezoid halo has no meaning here and is ignored
     Args a0 = a;
     a0.mode = CSSCAN_MODE_EXP_EULER;   // same pointer, size and alignment rules
     int rc = validate(a0, o);

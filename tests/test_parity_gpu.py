@@ -203,10 +203,6 @@ def test_zoh_rejected_where_unsupported():
     dev = gu.to_device(wl.generate(w))
     y = torch.empty((1, 16, 16), device="cuda")
     args = (dev["x"], dev["delta"], dev["A"], dev["Bc"], dev["Cc"], dev["theta"], None, dev["Dskip"])
-    h = torch.zeros((1, 16, 16, 2), device="cuda")
-    with pytest.raises(csscan.CsscanError) as e:
-        csscan.csscan_forward_state(*args, y, 2, h0=h)
-    assert e.value.status == csscan.CSSCAN_ERR_UNSUPPORTED
     with pytest.raises(csscan.CsscanError) as e:
         csscan.csscan_backward(*args, torch.zeros_like(y), 2)
     assert e.value.status == csscan.CSSCAN_ERR_UNSUPPORTED

@@ -69,6 +69,9 @@ CASES = [
     ("long-euler-bf16", "euler_bf16_long", dict(B=1, L=3000, D=24)),
     ("long-trap-bf16", "euler_bf16_long", dict(B=1, L=3000, D=24, mode=1)),
     ("mid-euler-f32", "euler_f32_mamba1", dict(B=2, L=300, D=64)),
+    ("rich-zoh-bf16", "zoh_bf16_batch", dict(B=16, L=160, D=2560)),
+    ("mid-zoh-f32", "zoh_bf16_batch", dict(B=2, L=333, D=48, dtype="f32")),
+    ("long-zoh-bf16", "zoh_bf16_batch", dict(B=1, L=3000, D=24)),
 ]
 
 
@@ -95,7 +98,7 @@ def test_forward_state_against_oracle(name, wname, shape):
     assert rel(state_from_device(h_last), h_ref) <= gu.TOL[w.dtype]
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_split_scan_equals_one_scan(mode):
     """[0, t0) then [t0, L) with the carried state and halo = one call over [0, L)."""
     w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=3, L=1000, D=96, mode=mode)
