@@ -83,8 +83,8 @@ enum {
  *   EXP_TRAPEZOID beta_t = (1 - lam_t) dt_t a_t on Bc_{t-1} x_{t-1}, gamma_t = lam_t dt_t
  *   ZOH           gamma_t = dt_t (e^{z_t} - 1) / z_t with z_t = dt_t A + i theta_t (the table's
  *                 A^{-1}(exp(dt A) - I) with the complex exponent of a_t in place of dt A);
- *                 csscan_forward, csscan_forward_ex and csscan_forward_state, N <= 32; the
- *                 other entry points return CSSCAN_ERR_UNSUPPORTED for it */
+ *                 csscan_forward, csscan_forward_ex and csscan_forward_state (N <= 32) and
+ *                 csscan_decode_step; the other entry points return CSSCAN_ERR_UNSUPPORTED for it */
 typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1, CSSCAN_MODE_ZOH = 2 } csscan_mode_t;
 typedef enum { CSSCAN_F32 = 0, CSSCAN_BF16 = 1 } csscan_dtype_t;
 
@@ -167,7 +167,8 @@ int csscan_forward_state(const void* x, const void* delta, const float* A, const
  *   y                 : device float32 (B, D), written
  *   h                 : device float32 (B, D, N, 2), the state, updated in place (16-byte aligned)
  *   x_prev, Bc_prev   : trapezoid mode: the previous step's x (B, D) and Bc (B, N, 2), both NULL
- *                       for the first step of a sequence; ignored in exp-Euler mode
+ *                       for the first step of a sequence; ignored in the other modes
+ *   mode              : any csscan_mode_t (zero-order hold included, every N)
  * The caller keeps the previous step's x and Bc for the trapezoid rule. One kernel launch; the
  * state is read and written once, so the step is bound by memory bandwidth.
  */

@@ -461,8 +461,8 @@ int dispatch_decode(const DecodeParams& dp, cudaStream_t st) {
 int decode_impl(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc, const void* theta,
                 const void* lambda, const float* Dskip, float* y, float* h, const void* x_prev, const void* Bc_prev,
                 int64_t B, int64_t D, int64_t N, int mode, int dtype, cudaStream_t stream) {
-  if (mode == CSSCAN_MODE_ZOH) return CSSCAN_ERR_UNSUPPORTED;
-  if (mode != CSSCAN_MODE_EXP_EULER && mode != CSSCAN_MODE_EXP_TRAPEZOID) return CSSCAN_ERR_INVALID_ARG;
+  if (mode != CSSCAN_MODE_EXP_EULER && mode != CSSCAN_MODE_EXP_TRAPEZOID && mode != CSSCAN_MODE_ZOH)
+    return CSSCAN_ERR_INVALID_ARG;
   if (dtype != CSSCAN_F32 && dtype != CSSCAN_BF16) return CSSCAN_ERR_INVALID_ARG;
   if (B < 0 || D < 0 || N <= 0) return CSSCAN_ERR_INVALID_ARG;
   if (!x || !delta || !A || !Bc || !Cc || !theta || !Dskip || !y || !h) return CSSCAN_ERR_INVALID_ARG;
@@ -493,8 +493,10 @@ int decode_impl(const void* x, const void* delta, const float* A, const void* Bc
   dp.D = int(D);
   dp.N = int(N);
   if (dtype == CSSCAN_F32)
-    return mode == 0 ? dispatch_decode<float, 0>(dp, stream) : dispatch_decode<float, 1>(dp, stream);
-  return mode == 0 ? dispatch_decode<uint16_t, 0>(dp, stream) : dispatch_decode<uint16_t, 1>(dp, stream);
+    return mode == 0 ? dispatch_decode<float, 0>(dp, stream)
+                     : (mode == 1 ? dispatch_decode<float, 1>(dp, stream) : dispatch_decode<float, 2>(dp, stream));
+  return mode == 0 ? dispatch_decode<uint16_t, 0>(dp, stream)
+                   : (mode == 1 ? dispatch_decode<uint16_t, 1>(dp, stream) : dispatch_decode<uint16_t, 2>(dp, stream));
 }
 
 // The checkpoint variants of the scan kernel need the same opt-in shared memory as the others.

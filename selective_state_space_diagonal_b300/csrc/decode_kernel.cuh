@@ -8,6 +8,7 @@
 //   a        = exp(dt[b,d] A[d,n]) e^{i theta[b,n]}
 //   exp-Euler        h[b,d,n] <- a h + dt x[b,d] Bc[b,n]
 //   exp-trapezoidal  h[b,d,n] <- a h + (1 - lam[b]) dt a x_prev[b,d] Bc_prev[b,n] + lam[b] dt x Bc
+//   zero-order hold  h[b,d,n] <- a h + dt (a - 1) / z x Bc,   z = dt A + i theta
 //   y[b,d]   = Re(sum_n Cc[b,n] h[b,d,n]) + Dskip[d] x[b,d]
 //
 // One thread updates two consecutive states of one (b, d) row; the N / 2 threads of a row are
@@ -69,6 +70,24 @@ __global__ void __launch_bounds__(256) decode_kernel(DecodeParams p) {
       const float g = dv * xv;
       ur = g * br;
       ui = g * bi;
+    } else if (MODE == 2) {
+      // (e^z - 1) / z without cancellation: e^z - 1 = expm1(dt A) e^{i theta} + (e^{i theta} - 1),
+      // cos theta - 1 = -2 sin^2(theta / 2); the limit 1 where |z|^2 underflows
+      const float u = dv * p.A[(long long)d * p.N + n + k], th = load_in<Tin>(TH, bn + k);
+      const float em = expm1f(u);
+      float sh, chh;
+      sincosf(0.5f * th, &sh, &chh);
+      const float cm1 = -2.f * sh * sh, s1 = 2.f * sh * chh;
+      const float er = fmaf(em, 1.f + cm1, cm1), ei = (1.f + em) * s1;
+      const float z2 = fmaf(u, u, th * th);
+      float gr = 1.f, gi = 0.f;
+      if (z2 > 1e-30f) {
+        gr = fmaf(er, u, ei * th) / z2;
+        gi = fmaf(ei, u, -er * th) / z2;
+      }
+      const float g = dv * xv;
+      ur = g * (gr * br - gi * bi);
+      ui = g * (gr * bi + gi * br);
     } else {
       const float lam = load_in<Tin>(static_cast<const Tin*>(p.lam), b);
       const float g = lam * dv * xv;

@@ -94,6 +94,7 @@ def test_state_and_decode_reject_bad_arguments_on_host(lib):
     assert dec(*args(x=None)) == csscan.CSSCAN_ERR_INVALID_ARG
     assert dec(*args(mode=1, lam=None)) == csscan.CSSCAN_ERR_INVALID_ARG
     assert dec(*args(mode=1, xp=A16)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert dec(*args(mode=3)) == csscan.CSSCAN_ERR_INVALID_ARG           # modes 0, 1, 2 only
 
 
 def test_backward_rejects_bad_arguments_on_host(lib):

@@ -123,7 +123,7 @@ def test_split_scan_equals_one_scan(mode):
 
 
 @pytest.mark.parametrize("N", [2, 16, 64])
-@pytest.mark.parametrize("mode,dtype", [(0, "f32"), (1, "bf16"), (1, "f32")])
+@pytest.mark.parametrize("mode,dtype", [(0, "f32"), (1, "bf16"), (1, "f32"), (2, "f32"), (2, "bf16")])
 def test_decode_steps_against_oracle(N, mode, dtype):
     """L decode steps from a random state equal the oracle's scan of the same L steps."""
     w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=3, L=40, D=24, N=N, mode=mode, dtype=dtype, seed=777 + N)
@@ -150,10 +150,11 @@ def test_decode_steps_against_oracle(N, mode, dtype):
     assert rel(state_from_device(h), h_ref) <= gu.TOL[dtype]
 
 
-def test_decode_continues_a_prefill():
+@pytest.mark.parametrize("mode", [1, 2])
+def test_decode_continues_a_prefill(mode):
     """Prefill with the scan (final state out), then decode the next steps one at a time: the
     result equals one scan over the whole sequence."""
-    w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=2, L=300, D=64)
+    w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=2, L=300, D=64, mode=mode)
     inp = wl.generate(w)
     dev = gu.to_device(inp)
     t0 = 280
@@ -166,7 +167,8 @@ def test_decode_continues_a_prefill():
     for t in range(t0, w.L):
         y = torch.empty((w.B, 1, w.D), device="cuda")
         sl = lambda k: dev[k][:, t].contiguous()
-        csscan.csscan_decode_step(sl("x"), sl("delta"), dev["A"], sl("Bc"), sl("Cc"), sl("theta"), sl("lam"),
+        csscan.csscan_decode_step(sl("x"), sl("delta"), dev["A"], sl("Bc"), sl("Cc"), sl("theta"),
+                                  sl("lam") if mode == 1 else None,
                                   dev["Dskip"], y, h, w.mode, x_prev=dev["x"][:, t - 1].contiguous(),
                                   Bc_prev=dev["Bc"][:, t - 1].contiguous())
         ys.append(y)
