@@ -83,8 +83,8 @@ enum {
  *   EXP_TRAPEZOID beta_t = (1 - lam_t) dt_t a_t on Bc_{t-1} x_{t-1}, gamma_t = lam_t dt_t
  *   ZOH           gamma_t = dt_t (e^{z_t} - 1) / z_t with z_t = dt_t A + i theta_t (the table's
  *                 A^{-1}(exp(dt A) - I) with the complex exponent of a_t in place of dt A);
- *                 csscan_forward, csscan_forward_ex and csscan_forward_state (N <= 32) and
- *                 csscan_decode_step; the other entry points return CSSCAN_ERR_UNSUPPORTED for it */
+ *                 the scans (csscan_forward, _ex, _state, _noalloc; N <= 32) and
+ *                 csscan_decode_step; csscan_backward returns CSSCAN_ERR_UNSUPPORTED for it */
 typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1, CSSCAN_MODE_ZOH = 2 } csscan_mode_t;
 typedef enum { CSSCAN_F32 = 0, CSSCAN_BF16 = 1 } csscan_dtype_t;
 
@@ -254,7 +254,8 @@ const char* csscan_status_string(int status);
  *                   status bits (0 = ok, 1 = a carry wait timed out, 2 = a tile copy timed out)
  *
  * Returns CSSCAN_ERR_SCRATCH_LIMIT, before any launch, when the problem needs more scratch
- * than the fixed array holds (roughly B*L*N*16 bytes of tables plus 8 to 16 bytes per state
+ * than the fixed array holds (roughly B*L*N*16 bytes of tables, 32 in the zero-order-hold mode,
+ * plus 8 to 16 bytes per state
  * of every chunk); csscan_forward has no such limit. The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress, which may load the library's GPU code on
  * that device), so make that first call before any stream capture. All calls share the one

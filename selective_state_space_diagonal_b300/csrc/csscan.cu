@@ -874,7 +874,9 @@ int dispatch_noalloc(const Args& a, uint32_t* device_status, cudaStream_t st) {
     case 8: return launch_noalloc<8, Tin, MODE>(a, device_status, st);
     case 16: return launch_noalloc<16, Tin, MODE>(a, device_status, st);
     case 32: return launch_noalloc<32, Tin, MODE>(a, device_status, st);
-    case 64: return launch_noalloc<64, Tin, MODE>(a, device_status, st);
+    case 64:
+      if constexpr (MODE == 2) return CSSCAN_ERR_UNSUPPORTED;
+      else return launch_noalloc<64, Tin, MODE>(a, device_status, st);
     default: return CSSCAN_ERR_UNSUPPORTED;
   }
 }
@@ -940,18 +942,22 @@ int csscan_decode_step(const void* x, const void* delta, const float* A, const v
 int csscan_forward_noalloc(const void* x, const void* delta, const float* A, const void* Bc, const void* Cc,
                            const void* theta, const void* lambda, const float* Dskip, float* y, int64_t B, int64_t L,
                            int64_t D, int64_t N, int mode, int dtype, uint32_t* device_status, cudaStream_t stream) {
-  if (mode == CSSCAN_MODE_ZOH) return CSSCAN_ERR_UNSUPPORTED;
   Args a{x, delta, Bc, Cc, theta, lambda, A, Dskip, y, nullptr, nullptr, nullptr, nullptr, B, L, D, N, mode, dtype};
   const csscan_options_t o = default_options();
-  int rc = validate(a, o);
+  Args av = a;
+  if (mode == CSSCAN_MODE_ZOH) av.mode = CSSCAN_MODE_EXP_EULER;   // same pointer, size and alignment rules
+  int rc = validate(av, o);
   if (rc != CSSCAN_OK) return rc;
+  if (mode == CSSCAN_MODE_ZOH && N > 32) return CSSCAN_ERR_UNSUPPORTED;
   if (device_status && (reinterpret_cast<uintptr_t>(device_status) % 4) != 0) return CSSCAN_ERR_MISALIGNED;
   if (a.B == 0 || a.L == 0 || a.D == 0) return CSSCAN_OK;
   if (a.dtype == CSSCAN_F32)
     return a.mode == 0 ? dispatch_noalloc<float, 0>(a, device_status, stream)
-                       : dispatch_noalloc<float, 1>(a, device_status, stream);
+                       : (a.mode == 1 ? dispatch_noalloc<float, 1>(a, device_status, stream)
+                                      : dispatch_noalloc<float, 2>(a, device_status, stream));
   return a.mode == 0 ? dispatch_noalloc<uint16_t, 0>(a, device_status, stream)
-                     : dispatch_noalloc<uint16_t, 1>(a, device_status, stream);
+                     : (a.mode == 1 ? dispatch_noalloc<uint16_t, 1>(a, device_status, stream)
+                                    : dispatch_noalloc<uint16_t, 2>(a, device_status, stream));
 }
 
 int csscan_forward_mimo(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
@@ -997,7 +1003,7 @@ const char* csscan_status_string(int status) {
     case CSSCAN_ERR_MISALIGNED: return "misaligned pointer or row stride (x/delta need 16-byte alignment and D*sizeof(dtype) % 16 == 0)";
     case CSSCAN_ERR_UNSUPPORTED:
       return "unsupported size or mode for this entry point (N in {2, 4, 8, 16, 32, 64}; N <= 32 for the backward and "
-             "the zero-order-hold mode, which only csscan_forward / csscan_forward_ex take)";
+             "for the zero-order-hold scan, which the backward does not take)";
     case CSSCAN_ERR_CUDA: return g_last_cuda_error[0] ? g_last_cuda_error : "CUDA error";
     case CSSCAN_ERR_LOOKBACK_TIMEOUT: return "a chunk's carry wait timed out on the device";
     case CSSCAN_ERR_PIPELINE_TIMEOUT: return "a tile copy did not arrive within its limit on the device";

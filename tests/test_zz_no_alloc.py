@@ -39,6 +39,7 @@ def rel_diff(a: torch.Tensor, b: torch.Tensor) -> float:
 @pytest.mark.parametrize("name,shape", [
     ("trap_bf16_batch", dict(B=2, L=2048, D=256)),
     ("euler_f32_mamba1", dict(B=1, L=1000, D=64)),
+    ("zoh_bf16_batch", dict(B=2, L=2048, D=256)),
 ])
 def test_noalloc_matches_forward_twice(name, shape):
     w = wl.WORKLOADS[name].with_shape(**shape)
