@@ -1,0 +1,66 @@
+"""Host-side bookkeeping of bench.py on CPU: launch counts, lane-operation counts, and how the
+bench reads DRAM traffic from the committed ncu summaries (only while their recorded kernel
+source hash matches the sources being built)."""
+import os
+
+import pytest
+
+import bench
+from selective_state_space_diagonal_b300 import workloads as wl
+
+PROFILES = [
+    # summary, kernel prefix, workload, the kernel sources its hash covers
+    ("scan_kernel_trap_bf16_batch.md", "scan_kernel", wl.WORKLOADS["trap_bf16_batch"], bench.KERNEL_SOURCES),
+    ("scan_kernel_zoh_bf16_batch.md", "scan_kernel", wl.WORKLOADS["zoh_bf16_batch"], bench.KERNEL_SOURCES),
+    ("mimo_out_kernel_mimo_trap_bf16_batch.md", "mimo_out_kernel", wl.MIMO_WORKLOADS["mimo_trap_bf16_batch"],
+     bench.MIMO_KERNEL_SOURCES),
+]
+
+
+def machine_values(path):
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.split(":", 1)[0].strip() in ("kernel_source_sha256_16", "dram_bytes_per_launch"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    return vals
+
+
+@pytest.mark.parametrize("name,kernel,w,sources", PROFILES, ids=[p[0] for p in PROFILES])
+def test_profile_traffic_is_near_the_algorithmic_bytes(name, kernel, w, sources):
+    """Each summary records DRAM bytes per launch within a few percent above the workload's
+    algorithmic bytes (more would be re-reads; less is impossible for a kernel that reads its
+    inputs and writes its output once)."""
+    vals = machine_values(os.path.join(bench.ROOT, "profiles", name))
+    assert len(vals["kernel_source_sha256_16"]) == 16
+    traffic = int(vals["dram_bytes_per_launch"])
+    assert 1.0 <= traffic / w.min_bytes() <= 1.05
+
+
+def test_traffic_read_only_for_matching_sources(tmp_path, monkeypatch):
+    src = tmp_path / "k.cuh"
+    src.write_text("// kernel v1\n")
+    (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.kernel_source_hash(("k.cuh",))
+    (tmp_path / "profiles" / "scan_kernel_demo.md").write_text(
+        f"# demo\n\nkernel_source_sha256_16: {h}\ndram_bytes_per_launch: 1234\n")
+    assert bench.traffic_from_profiles("demo", "scan_kernel", ("k.cuh",)) == 1234
+    src.write_text("// kernel v2\n")   # the sources changed since the capture: the figure is stale
+    assert bench.traffic_from_profiles("demo", "scan_kernel", ("k.cuh",)) is None
+    assert bench.traffic_from_profiles("absent", "scan_kernel", ("k.cuh",)) is None
+
+
+def test_launch_and_operation_counts():
+    for w in wl.WORKLOADS.values():
+        assert bench.launches_per_step(w) == 2        # table kernel + scan kernel in every mode
+    assert bench.mimo_alu_ops_per_elem(4, 1) == pytest.approx(6.25)
+    assert bench.mimo_alu_ops_per_elem(4, 0) == pytest.approx(5.25)
+    assert bench.mimo_alu_ops_per_elem(1, 1) == pytest.approx(11.5)
+    assert bench.ZOH_ALU_OPS_PER_ELEM > bench.ALU_OPS_PER_ELEM
+
+
+def test_workload_config_names_the_mode():
+    names = {w.mode: bench.workload_config(w)["mode"] for w in wl.WORKLOADS.values()}
+    assert names == {0: "exp-Euler", 1: "exp-trapezoidal", 2: "zero-order hold"}
