@@ -248,9 +248,10 @@ def pin_linearity_and_causality(lib):
 
 def pin_split_invariance(lib):
     """Running [0, t0) and then [t0, L) from the carried state (and, in the trapezoid mode,
-    step t0-1's x and Bc as the halo) equals one run over [0, L)."""
+    step t0-1's x and Bc as the halo) equals one run over [0, L); in every mode, the
+    zero-order hold included (whose step ignores the halo)."""
     rng = np.random.default_rng(19)
-    for mode in (0, 1):
+    for mode in (0, 1, 2):
         c = random_case(rng, 2, 64, 3, 4, mode)
         y_full, h_full = run(lib, c, mode, want_h_last=True)
         for t0 in (1, 17, 63):
