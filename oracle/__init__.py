@@ -134,7 +134,8 @@ def forward(x, delta, A, Bc, Cc, theta, lam, Dskip, mode: int, *, h0=None, x_pre
 
 
 def backward(x, delta, A, Bc, Cc, theta, lam, Dskip, dy, mode: int, *, nthreads: int = 0, lib=None) -> dict:
-    """Reverse-mode gradients of l = sum(dy * y) for ``forward`` from the zero state (no halo).
+    """Reverse-mode gradients of l = sum(dy * y) for ``forward`` from the zero state (no halo),
+    in any of the three modes.
 
     Same input shapes as ``forward``, plus dy (B,L,D) real. Returns a dict with dx, ddelta
     (B,L,D), dA (D,N), dBc, dCc (B,L,N) complex (d/dRe + i d/dIm), dtheta (B,L,N),

@@ -222,7 +222,9 @@ int oracle_forward(const double* x, const double* dt, const double* A, const dou
  * and ghat_t is the gradient of the step-t injection u_t; the transition a_t = exp(z_t),
  * z_t = dt_t A + i theta_t, receives G(a_t) = ghat_t conj(h_{t-1}) (plus, in the trapezoid
  * mode, ghat_t conj((1 - lam_t) dt_t x_{t-1} Bc_{t-1}) from beta_t), so that
- * d l / d(dt_t A) = Re G(z_t) and d l / d theta_t = Im G(z_t).
+ * d l / d(dt_t A) = Re G(z_t) and d l / d theta_t = Im G(z_t). In the zero-order hold the
+ * injection's gamma_t = dt_t phi(z_t) depends on z_t too: G(z_t) gains conj(phi'(z_t)) dt_t
+ * x_t conj(Bc_t) ghat_t, and dt_t's own factor gives Re(conj(phi) x_t conj(Bc_t) ghat_t).
  *
  * Outputs are fully written (zeroed first); complex gradients are (d/dRe, d/dIm) pairs in the
  * layouts of their inputs: dx, ddt (B,L,D); dA (D,N); dBc, dCc (B,L,N) complex;
@@ -236,6 +238,16 @@ typedef struct {
   int mode;
   int64_t row_begin, row_step;
 } bjob_t;
+
+/* Zero-order hold: phi(z) = (e^z - 1) / z, as in oracle_operator, and its derivative
+ * phi'(z) = (e^z (z - 1) + 1) / z^2, from its power series sum_{k>=1} k z^{k-1} / (k+1)! where
+ * the closed form would cancel (|z| < 1e-2: the first omitted term is below 1e-13 of 1/2). */
+static cplx zoh_phi(cplx z) { return cabs(z) < 1e-6 ? 1.0 + z / 2.0 + z * z / 6.0 : (cexp(z) - 1.0) / z; }
+static cplx zoh_dphi(cplx z) {
+  if (cabs(z) < 1e-2)
+    return 0.5 + z * (1.0 / 3.0 + z * (1.0 / 8.0 + z * (1.0 / 30.0 + z * (1.0 / 144.0 + z / 840.0))));
+  return (cexp(z) * (z - 1.0) + 1.0) / (z * z);
+}
 
 static void backward_row(const bjob_t* j, int64_t b, int64_t d, cplx* hs, cplx* as, cplx* carry) {
   const int64_t L = j->L, D = j->D, N = j->N;
@@ -267,6 +279,7 @@ static void backward_row(const bjob_t* j, int64_t b, int64_t d, cplx* hs, cplx* 
     double P = 0.0;   /* sum_n Re(conj(Bc_t) ghat_t): d l / d(coefficient of Bc_t) */
     double R = 0.0;   /* sum_n Re(conj(a_t Bc_{t-1}) ghat_t): the same for beta_t's term */
     double dz_re = 0.0;
+    double Q = 0.0;   /* zero-order hold: d l / d dt_t through gamma's factor dt_t */
     for (int64_t n = 0; n < N; ++n) {
       const int64_t tn = (b * L + t) * N + n;
       const cplx a = as[t * N + n];
@@ -278,9 +291,20 @@ static void backward_row(const bjob_t* j, int64_t b, int64_t d, cplx* hs, cplx* 
       /* injection */
       const cplx Bt = load_c(j->Bc, tn);
       cplx Ga = ghat * conj(h_prev);
+      cplx Gz_phi = 0.0;   /* zero-order hold: G(z) through gamma = dt phi(z) */
       if (j->mode == 0) {
         store_c(j->dBc, tn, load_c(j->dBc, tn) + (dtt * xt) * ghat);
         P += creal(conj(Bt) * ghat);
+      } else if (j->mode == 2) {
+        /* u_t = gamma_t x_t Bc_t: G(gamma) = x conj(Bc) ghat, G(phi) = dt G(gamma),
+         * G(z) += conj(phi'(z)) G(phi); the factor dt in gamma gives Re(conj(phi) G(gamma)) */
+        const cplx z = dtt * j->A[d * N + n] + I * j->theta[tn];
+        const cplx phi = zoh_phi(z), gam = dtt * phi;
+        const cplx Ggam = xt * conj(Bt) * ghat;
+        store_c(j->dBc, tn, load_c(j->dBc, tn) + (xt * conj(gam)) * ghat);
+        P += creal(conj(gam * Bt) * ghat);
+        Q += creal(conj(phi) * Ggam);
+        Gz_phi = conj(zoh_dphi(z)) * (dtt * Ggam);
       } else {
         store_c(j->dBc, tn, load_c(j->dBc, tn) + (lam * dtt * xt) * ghat);
         P += creal(conj(Bt) * ghat);
@@ -292,8 +316,8 @@ static void backward_row(const bjob_t* j, int64_t b, int64_t d, cplx* hs, cplx* 
           Ga += ghat * conj(c2 * Bp);
         }
       }
-      /* transition a_t = exp(dt_t A + i theta_t) */
-      const cplx Gz = conj(a) * Ga;
+      /* transition a_t = exp(dt_t A + i theta_t) (and, in mode 2, gamma's phi(z)) */
+      const cplx Gz = conj(a) * Ga + Gz_phi;
       j->dA[d * N + n] += dtt * creal(Gz);
       dz_re += j->A[d * N + n] * creal(Gz);
       j->dtheta[tn] += cimag(Gz);
@@ -303,6 +327,9 @@ static void backward_row(const bjob_t* j, int64_t b, int64_t d, cplx* hs, cplx* 
     if (j->mode == 0) {
       gx = dtt * P;
       gdt = xt * P;
+    } else if (j->mode == 2) {
+      gx = P;
+      gdt = Q;
     } else {
       gx = lam * dtt * P;
       gdt = lam * xt * P + (1.0 - lam) * x_prev * R;
@@ -336,7 +363,7 @@ int oracle_backward(const double* x, const double* dt, const double* A, const do
                     double* dx, double* ddt, double* dA, double* dBc, double* dCc, double* dtheta, double* dlam,
                     double* dDskip, int64_t B, int64_t L, int64_t D, int64_t N, int mode, int nthreads) {
   if (B < 0 || L < 0 || D < 0 || N < 0) return -1;
-  if (mode != 0 && mode != 1) return -2;
+  if (mode != 0 && mode != 1 && mode != 2) return -2;
   if (mode == 1 && (!lam || !dlam) && B * L > 0) return -3;
   const size_t nBLD = (size_t)(B * L * D), nDN = (size_t)(D * N), nBLN = (size_t)(B * L * N), nBL = (size_t)(B * L);
   for (size_t i = 0; i < nBLD; ++i) { dx[i] = 0.0; ddt[i] = 0.0; }

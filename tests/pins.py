@@ -425,12 +425,16 @@ def run_backward(lib, c, dy, mode):
 
 def pin_backward_finite_differences(lib):
     """Every gradient of l = sum(dy * y) equals the central finite difference of the forward
-    oracle (itself pinned above), entry by entry, for both modes on tiny inputs. The
+    oracle (itself pinned above), entry by entry, for all three modes on tiny inputs. The
     backward's formulas come from differentiating the recurrence; this checks them against
     the definition of a derivative, with no shared arithmetic."""
     rng = np.random.default_rng(23)
-    for mode in (0, 1):
-        c = random_case(rng, 2, 6, 2, 3, mode)
+    # the last case keeps |z| = |dt A + i theta| below 1e-2, where the zero-order hold's
+    # phi'(z) comes from its power series; there the forward's (e^z - 1) / z carries ~1e-12
+    # relative rounding, so its differences take a larger step (truncation ~1e-8)
+    cases = [(0, {}, 1e-6), (1, {}, 1e-6), (2, {}, 1e-6), (2, dict(dt_range=(1e-4, 1e-3), theta_max=3e-3), 1e-4)]
+    for mode, kw, step in cases:
+        c = random_case(rng, 2, 6, 2, 3, mode, **kw)
         dy = rng.standard_normal((2, 6, 2))
         g = run_backward(lib, c, dy, mode)
         loss = lambda cc: float(np.sum(dy * run(lib, cc, mode)))
@@ -441,7 +445,7 @@ def pin_backward_finite_differences(lib):
             for unit in units:
                 fd = np.zeros(c[key].shape)
                 for idx in np.ndindex(c[key].shape):
-                    h = 1e-6 * max(1.0, abs(c[key][idx]))
+                    h = step * max(1.0, abs(c[key][idx]))
                     cp = dict(c)
                     cp[key] = c[key].copy()
                     cp[key][idx] += h * unit
@@ -461,12 +465,13 @@ def pin_backward_identities(lib):
     y is homogeneous of degree one in x, and y - Dskip x is so in Bc and in Cc (the
     injection is linear in x and Bc, the output linear in Cc), so by Euler's theorem
     <dx, x> = <dy, y>, <dBc, Bc> = <dCc, Cc> = <dy, y - Dskip x>, <dDskip, Dskip> = <dy, Dskip x>.
-    Scaling A by c and dt by 1/c leaves every a_t unchanged and scales every injection
-    (both modes carry one factor dt_t) by 1/c, so sum A dA - sum dt ddt = -<dy, y - Dskip x>.
+    Scaling A by c and dt by 1/c leaves every a_t (and the zero-order hold's z_t) unchanged and
+    scales every injection (each mode carries one factor dt_t) by 1/c, so
+    sum A dA - sum dt ddt = -<dy, y - Dskip x>.
     y is affine in each lam_t, so a central difference of any step is exact: checked on a
     few steps with a large step size."""
     rng = np.random.default_rng(29)
-    for mode in (0, 1):
+    for mode in (0, 1, 2):
         c = random_case(rng, 2, 40, 5, 4, mode)
         dy = rng.standard_normal((2, 40, 5))
         y = run(lib, c, mode)

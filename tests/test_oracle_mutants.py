@@ -70,7 +70,7 @@ MUTANTS = [
     ("adjoint drops the carry", "const cplx ghat = dyt * conj(load_c(j->Cc, tn)) + carry[n];",
      "const cplx ghat = dyt * conj(load_c(j->Cc, tn));"),
     ("transition gradient from h_t", "cplx Ga = ghat * conj(h_prev);", "cplx Ga = ghat * conj(h);"),
-    ("exp chain rule without conj(a)", "const cplx Gz = conj(a) * Ga;", "const cplx Gz = Ga;"),
+    ("exp chain rule without conj(a)", "const cplx Gz = conj(a) * Ga + Gz_phi;", "const cplx Gz = Ga + Gz_phi;"),
     ("theta gradient from the real part", "j->dtheta[tn] += cimag(Gz);", "j->dtheta[tn] += creal(Gz);"),
     ("A gradient without dt", "j->dA[d * N + n] += dtt * creal(Gz);", "j->dA[d * N + n] += creal(Gz);"),
     ("C gradient unconjugated", "load_c(j->dCc, tn) + dyt * conj(h)", "load_c(j->dCc, tn) + dyt * h"),
@@ -84,6 +84,12 @@ MUTANTS = [
     ("D-skip gradient without dy", "j->dD[d] += dyt * xt;", "j->dD[d] += xt;"),
     ("x gradient misses the D-skip", "j->dx[td] += gx + j->Dskip[d] * dyt;", "j->dx[td] += gx;"),
     ("dt gradient misses the decay", "j->ddt[td] += gdt + dz_re;", "j->ddt[td] += gdt;"),
+    ("zoh gradient without phi'(z)", "Gz_phi = conj(zoh_dphi(z)) * (dtt * Ggam);", "Gz_phi = 0.0 * (dtt * Ggam);"),
+    ("zoh gradient with phi'(z) unconjugated", "Gz_phi = conj(zoh_dphi(z)) * (dtt * Ggam);",
+     "Gz_phi = zoh_dphi(z) * (dtt * Ggam);"),
+    ("zoh dt gradient without gamma's factor", "Q += creal(conj(phi) * Ggam);", "Q += 0.0;"),
+    ("zoh B gradient with gamma unconjugated", "(xt * conj(gam)) * ghat", "(xt * gam) * ghat"),
+    ("zoh phi' series term wrong", "z * (1.0 / 3.0 + z", "z * (1.0 / 2.0 + z"),
 ]
 
 
