@@ -68,6 +68,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.oracle_backward.restype = ctypes.c_int
     lib.oracle_forward_mimo.argtypes = [dp] * 9 + [i64] * 5 + [ctypes.c_int, ctypes.c_int]
     lib.oracle_forward_mimo.restype = ctypes.c_int
+    lib.oracle_backward_mimo.argtypes = [dp] * 17 + [i64] * 5 + [ctypes.c_int]
+    lib.oracle_backward_mimo.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
     lib.oracle_default_threads.restype = ctypes.c_int
     _lib_cache[path] = lib
@@ -187,6 +189,38 @@ def forward_mimo(x, delta, A, Bm, Cm, theta, lam, Dskip, mode: int, *, nthreads:
     if rc <= 0:
         raise RuntimeError(f"oracle_forward_mimo failed with code {rc}")
     return y
+
+
+def backward_mimo(x, delta, A, Bm, Cm, theta, lam, Dskip, dy, mode: int, *, lib=None) -> dict:
+    """Reverse-mode gradients of l = sum(dy * y) for ``forward_mimo`` (from the zero state).
+
+    Same input shapes as ``forward_mimo``, plus dy (B,L,H,P) real. Returns a dict with dx
+    (B,L,H,P), ddelta (B,L,H), dA (H,N), dBm, dCm (B,L,N,P) complex (d/dRe + i d/dIm),
+    dtheta (B,L,N), dlam (B,L) (trapezoid, else None) and dDskip (H,P), float64 / complex128.
+    """
+    lib = lib or load()
+    x = _f64(x)
+    Bsz, L, H, P = x.shape
+    N = np.asarray(A).shape[1]
+    delta = _f64(delta, (Bsz, L, H))
+    A = _f64(A, (H, N))
+    Bm = _f64(np.asarray(Bm, dtype=np.complex128), (Bsz, L, N, P))
+    Cm = _f64(np.asarray(Cm, dtype=np.complex128), (Bsz, L, N, P))
+    theta = _f64(theta, (Bsz, L, N))
+    lam = _f64(lam, (Bsz, L)) if lam is not None else None
+    Dskip = _f64(Dskip, (H, P))
+    dy = _f64(dy, (Bsz, L, H, P))
+    out = dict(dx=np.zeros((Bsz, L, H, P)), ddelta=np.zeros((Bsz, L, H)), dA=np.zeros((H, N)),
+               dBm=np.zeros((Bsz, L, N, P), dtype=np.complex128), dCm=np.zeros((Bsz, L, N, P), dtype=np.complex128),
+               dtheta=np.zeros((Bsz, L, N)), dlam=np.zeros((Bsz, L)) if mode == 1 else None,
+               dDskip=np.zeros((H, P)))
+    rc = lib.oracle_backward_mimo(_ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(theta), _ptr(lam),
+                                  _ptr(Dskip), _ptr(dy), _ptr(out["dx"]), _ptr(out["ddelta"]), _ptr(out["dA"]),
+                                  _ptr(out["dBm"]), _ptr(out["dCm"]), _ptr(out["dtheta"]), _ptr(out["dlam"]),
+                                  _ptr(out["dDskip"]), Bsz, L, H, P, N, int(mode))
+    if rc != 0:
+        raise RuntimeError(f"oracle_backward_mimo failed with code {rc}")
+    return out
 
 
 def last_thread_count(nthreads: int = 0, rows: int = 1 << 30, lib=None) -> int:

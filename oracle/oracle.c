@@ -504,3 +504,119 @@ int oracle_forward_mimo(const double* x, const double* dt, const double* A, cons
   free(jobs);
   return rc < 0 ? rc : nthreads;
 }
+
+/* ===================================================================================== *
+ * Backward (reverse mode) of the MIMO scan, from the zero state: the gradients of
+ * l = sum dy[b,t,h,p] y[b,t,h,p], written out with the rules of the single-input backward
+ * above. Per (b, head) and state n the adjoint is
+ *   ghat_t = sum_p dy_t[p] conj(Cm_t[n,p]) + conj(a_{t+1}) ghat_{t+1},
+ * the gradient of the step-t injection u_t. exp-Euler u_t = dt_t v_t gives
+ * G(v_t) = dt_t ghat_t; the trapezoid u_t = c1 v_t + c2 a_t v_{t-1} (c1 = lam_t dt_t,
+ * c2 = (1 - lam_t) dt_t) gives G(v_t) = c1 ghat_t + c2' conj(a_{t+1}) ghat_{t+1} (c2' of step
+ * t + 1) and G(a_t) gains ghat_t conj(c2 v_{t-1}). v_t[n] = sum_p Bm_t[n,p] x_t[p] then gives
+ * G(Bm_t[n,p]) = x_t[p] G(v_t[n]) and dx_t[p] += Re(conj(Bm_t[n,p]) G(v_t[n])).
+ * Outputs are zeroed first and fully written: dx (B,L,H,P), ddt (B,L,H), dA (H,N),
+ * dBm, dCm (B,L,N,P) complex, dtheta (B,L,N), dlam (B,L) (trapezoid; may be NULL otherwise),
+ * dDskip (H,P). Single-threaded (a test reference for small sizes). Returns 0, or a negative
+ * value on bad arguments or allocation failure.
+ * ===================================================================================== */
+int oracle_backward_mimo(const double* x, const double* dt, const double* A, const double* Bm, const double* Cm,
+                         const double* theta, const double* lam, const double* Dskip, const double* dy,
+                         double* dx, double* ddt, double* dA, double* dBm, double* dCm, double* dtheta,
+                         double* dlam, double* dDskip, int64_t B, int64_t L, int64_t H, int64_t P, int64_t N,
+                         int mode) {
+  if (B < 0 || L < 0 || H < 0 || P < 0 || N < 0) return -1;
+  if (mode != 0 && mode != 1) return -2;
+  if (mode == 1 && (!lam || !dlam) && B * L > 0) return -3;
+  for (int64_t i = 0; i < B * L * H * P; ++i) dx[i] = 0.0;
+  for (int64_t i = 0; i < B * L * H; ++i) ddt[i] = 0.0;
+  for (int64_t i = 0; i < H * N; ++i) dA[i] = 0.0;
+  for (int64_t i = 0; i < 2 * B * L * N * P; ++i) { dBm[i] = 0.0; dCm[i] = 0.0; }
+  for (int64_t i = 0; i < B * L * N; ++i) dtheta[i] = 0.0;
+  if (dlam) for (int64_t i = 0; i < B * L; ++i) dlam[i] = 0.0;
+  for (int64_t i = 0; i < H * P; ++i) dDskip[i] = 0.0;
+  const size_t LN = (size_t)(L > 0 ? L : 1) * (size_t)(N > 0 ? N : 1);
+  cplx* hs = (cplx*)malloc(sizeof(cplx) * LN);
+  cplx* as = (cplx*)malloc(sizeof(cplx) * LN);
+  cplx* vs = (cplx*)malloc(sizeof(cplx) * LN);
+  cplx* cg = (cplx*)malloc(sizeof(cplx) * (size_t)(N > 0 ? 2 * N : 2));
+  if (!hs || !as || !vs || !cg) { free(hs); free(as); free(vs); free(cg); return -4; }
+  cplx* cv = cg + N;   /* G(v_t) carried from step t + 1 (trapezoid) */
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t hd = 0; hd < H; ++hd) {
+      /* forward sweep: keep h_t, a_t and v_t of this row */
+      for (int64_t n = 0; n < N; ++n) cg[n] = 0.0;   /* used as h here */
+      for (int64_t t = 0; t < L; ++t) {
+        const double dtt = dt[(b * L + t) * H + hd];
+        const double lm = mode == 1 ? lam[b * L + t] : 0.0;
+        const double* xt = &x[((b * L + t) * H + hd) * P];
+        for (int64_t n = 0; n < N; ++n) {
+          const int64_t tn = (b * L + t) * N + n;
+          cplx v = 0.0;
+          for (int64_t p = 0; p < P; ++p) v += load_c(Bm, tn * P + p) * xt[p];
+          const cplx a = transition(dtt, A[hd * N + n], theta[tn]);
+          const cplx vp = t > 0 ? vs[(t - 1) * N + n] : 0.0;
+          const cplx u = mode == 0 ? dtt * v : (1.0 - lm) * dtt * a * vp + lm * dtt * v;
+          cg[n] = a * cg[n] + u;
+          hs[t * N + n] = cg[n];
+          as[t * N + n] = a;
+          vs[t * N + n] = v;
+        }
+      }
+      /* reverse sweep */
+      for (int64_t n = 0; n < N; ++n) { cg[n] = 0.0; cv[n] = 0.0; }
+      for (int64_t t = L - 1; t >= 0; --t) {
+        const int64_t th = (b * L + t) * H + hd;
+        const double dtt = dt[th];
+        const double lm = mode == 1 ? lam[b * L + t] : 0.0;
+        const double c1 = mode == 0 ? dtt : lm * dtt, c2 = (1.0 - lm) * dtt;
+        const double* xt = &x[th * P];
+        const double* dyt = &dy[th * P];
+        double dc1 = 0.0, dc2 = 0.0, dz_re = 0.0;
+        for (int64_t n = 0; n < N; ++n) {
+          const int64_t tn = (b * L + t) * N + n;
+          const cplx a = as[t * N + n], h = hs[t * N + n];
+          const cplx h_prev = t > 0 ? hs[(t - 1) * N + n] : 0.0;
+          const cplx v = vs[t * N + n];
+          cplx ghat = cg[n];
+          for (int64_t p = 0; p < P; ++p) {
+            ghat += dyt[p] * conj(load_c(Cm, tn * P + p));
+            store_c(dCm, tn * P + p, load_c(dCm, tn * P + p) + dyt[p] * conj(h));
+          }
+          const cplx Gv = c1 * ghat + cv[n];
+          dc1 += creal(conj(v) * ghat);
+          cplx Ga = ghat * conj(h_prev);
+          cplx next_cv = 0.0;
+          if (mode == 1 && t > 0) {
+            const cplx vp = vs[(t - 1) * N + n];
+            Ga += ghat * conj(c2 * vp);
+            dc2 += creal(conj(a * vp) * ghat);
+            next_cv = c2 * conj(a) * ghat;   /* G(v_{t-1}) from this step's beta term */
+          }
+          for (int64_t p = 0; p < P; ++p) {
+            store_c(dBm, tn * P + p, load_c(dBm, tn * P + p) + xt[p] * Gv);
+            dx[th * P + p] += creal(conj(load_c(Bm, tn * P + p)) * Gv);
+          }
+          const cplx Gz = conj(a) * Ga;
+          dA[hd * N + n] += dtt * creal(Gz);
+          dz_re += A[hd * N + n] * creal(Gz);
+          dtheta[tn] += cimag(Gz);
+          cg[n] = conj(a) * ghat;
+          cv[n] = next_cv;
+        }
+        if (mode == 0) {
+          ddt[th] += dc1 + dz_re;
+        } else {
+          ddt[th] += lm * dc1 + (1.0 - lm) * dc2 + dz_re;
+          dlam[b * L + t] += dtt * dc1 - dtt * dc2;
+        }
+        for (int64_t p = 0; p < P; ++p) {
+          dDskip[hd * P + p] += dyt[p] * xt[p];
+          dx[th * P + p] += Dskip[hd * P + p] * dyt[p];
+        }
+      }
+    }
+  }
+  free(hs); free(as); free(vs); free(cg);
+  return 0;
+}

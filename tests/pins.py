@@ -499,8 +499,67 @@ def pin_backward_identities(lib):
                 close(g["dlam"][b, t], lp - lm, f"dlam[{b},{t}] (y is affine in lam)")
 
 
+# ---------------------------------------------------------------------------- MIMO backward
+MIMO_GRAD_OF = {"x": "dx", "delta": "ddelta", "A": "dA", "Bm": "dBm", "Cm": "dCm", "theta": "dtheta",
+                "lam": "dlam", "Dskip": "dDskip"}
+
+
+def run_backward_mimo(lib, c, dy, mode):
+    return oracle.backward_mimo(c["x"], c["delta"], c["A"], c["Bm"], c["Cm"], c["theta"], c["lam"], c["Dskip"], dy,
+                                mode, lib=lib)
+
+
+def pin_mimo_backward_finite_differences(lib):
+    """Every gradient of l = sum(dy * y) for the MIMO scan equals the central finite difference
+    of the MIMO forward oracle (pinned above), entry by entry, both modes, tiny inputs."""
+    rng = np.random.default_rng(53)
+    for mode in (0, 1):
+        c = mimo_case(rng, 2, 5, 2, 2, 2, mode)
+        dy = rng.standard_normal((2, 5, 2, 2))
+        g = run_backward_mimo(lib, c, dy, mode)
+        loss = lambda cc: float(np.sum(dy * run_mimo(lib, cc, mode)))
+        for key, gname in MIMO_GRAD_OF.items():
+            if c[key] is None:
+                continue
+            for unit in ([1.0, 1j] if np.iscomplexobj(c[key]) else [1.0]):
+                fd = np.zeros(c[key].shape)
+                for idx in np.ndindex(c[key].shape):
+                    h = 1e-6 * max(1.0, abs(c[key][idx]))
+                    cp = dict(c)
+                    cp[key] = c[key].copy()
+                    cp[key][idx] += h * unit
+                    lp = loss(cp)
+                    cp[key][idx] -= 2 * h * unit
+                    fd[idx] = (lp - loss(cp)) / (2 * h)
+                an = g[gname]
+                if np.iscomplexobj(an):
+                    an = an.real if unit == 1.0 else an.imag
+                e = rel_err(an, fd)
+                assert e < 1e-6, f"mimo mode {mode}: d/d{key} differs from finite differences: {e:.2e}"
+
+
+def pin_mimo_backward_one_channel_is_siso(lib):
+    """P = 1: the MIMO gradients are the single-input backward's (itself pinned above) with one
+    channel per head, at a size beyond the finite-difference pin."""
+    rng = np.random.default_rng(59)
+    for mode in (0, 1):
+        c = mimo_case(rng, 2, 40, 3, 1, 4, mode)
+        dy = rng.standard_normal((2, 40, 3, 1))
+        g = run_backward_mimo(lib, c, dy, mode)
+        s = oracle.backward(c["x"][..., 0], c["delta"], c["A"], c["Bm"][..., 0], c["Cm"][..., 0], c["theta"], c["lam"],
+                            c["Dskip"][:, 0], dy[..., 0], mode, lib=lib)
+        pairs = [("dx", g["dx"][..., 0], s["dx"]), ("ddelta", g["ddelta"], s["ddelta"]), ("dA", g["dA"], s["dA"]),
+                 ("dBm", g["dBm"][..., 0], s["dBc"]), ("dCm", g["dCm"][..., 0], s["dCc"]),
+                 ("dtheta", g["dtheta"], s["dtheta"]), ("dDskip", g["dDskip"][:, 0], s["dDskip"])]
+        if mode == 1:
+            pairs.append(("dlam", g["dlam"], s["dlam"]))
+        for name, a, b in pairs:
+            assert rel_err(a, b) <= 1e-12, f"mimo mode {mode}: {name} differs from the single-input backward"
+
+
 ALL_PINS = [pin_combine_associative, pin_combine_is_composition, pin_bruteforce, pin_closed_form,
             pin_real_reduction, pin_rotation, pin_lambda_one, pin_linearity_and_causality,
             pin_split_invariance, pin_golden, pin_zoh_exact_hold, pin_zoh_real_reduction, pin_zoh_small_step_limit,
             pin_mimo_one_channel_is_siso, pin_mimo_superposition,
-            pin_backward_finite_differences, pin_backward_identities]
+            pin_backward_finite_differences, pin_backward_identities,
+            pin_mimo_backward_finite_differences, pin_mimo_backward_one_channel_is_siso]

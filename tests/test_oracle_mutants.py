@@ -90,6 +90,16 @@ MUTANTS = [
     ("zoh dt gradient without gamma's factor", "Q += creal(conj(phi) * Ggam);", "Q += 0.0;"),
     ("zoh B gradient with gamma unconjugated", "(xt * conj(gam)) * ghat", "(xt * gam) * ghat"),
     ("zoh phi' series term wrong", "z * (1.0 / 3.0 + z", "z * (1.0 / 2.0 + z"),
+    # MIMO backward
+    ("mimo adjoint reads Cm unconjugated", "ghat += dyt[p] * conj(load_c(Cm, tn * P + p));",
+     "ghat += dyt[p] * load_c(Cm, tn * P + p);"),
+    ("mimo v gradient drops the next step's beta term", "const cplx Gv = c1 * ghat + cv[n];",
+     "const cplx Gv = c1 * ghat;"),
+    ("mimo x gradient with Bm unconjugated", "dx[th * P + p] += creal(conj(load_c(Bm, tn * P + p)) * Gv);",
+     "dx[th * P + p] += creal(load_c(Bm, tn * P + p) * Gv);"),
+    ("mimo lam gradient sign", "dlam[b * L + t] += dtt * dc1 - dtt * dc2;", "dlam[b * L + t] += dtt * dc1 + dtt * dc2;"),
+    ("mimo Bm gradient from the wrong channel's x", "load_c(dBm, tn * P + p) + xt[p] * Gv",
+     "load_c(dBm, tn * P + p) + xt[0] * Gv"),
 ]
 
 
