@@ -18,6 +18,8 @@ computes and which page it follows:
 The backward (``backward``) is reverse-mode differentiation of that recurrence written out
 step by step in ``oracle.c``; the pages name a backward pass with recomputed states
 ("Complex parallel scan", sections 一个问题，两种命运 and 硬件落地的挑战) but give no formulas.
+The MIMO scan (``forward_mimo``: P channels of a head share one state, "Mamba-3 paper story",
+MIMO section) and its backward (``backward_mimo``) are written out the same way.
 
 This module only marshals numpy arrays into that library (``ctypes``) and builds it.
 """
