@@ -107,8 +107,9 @@ int csscan_forward(const void* x, const void* delta, const float* A, const void*
 
 /*
  * Launch options for csscan_forward_ex. Zero-initialise and set only what you need.
- *   cta_warps     : reserved, must be 0 (a block is 4 warps covering 2 * 32 * 4 / NG channels,
- *                   NG = N / 8 lanes sharing a channel pair for N >= 16, else 1)
+ *   cta_warps     : reserved, must be 0 (a block is 4 warps; in the exp-Euler and trapezoid
+ *                   modes a thread owns one channel and 8 or 16 of its states, in the
+ *                   zero-order-hold mode two channels and 8 states)
  *   chunk_len     : sequence chunk per thread block (multiple of 32); 0 = automatic
  *   carry         : 0 automatic, 1 serial (each chunk waits for its predecessor's final state),
  *                   2 decoupled (each chunk first computes its own aggregate, then looks back)

@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(256) chunk_adj_kernel(const Params p) {
 
 // Walk the chunks of (b, d, n): rec[0] <- entry state h_in, rec[2] <- true adjoint at the
 // chunk's first step.
-__global__ void __launch_bounds__(256) chunk_combine_kernel(const Params p) {
+static __global__ void __launch_bounds__(256) chunk_combine_kernel(const Params p) {
   const long long gid = (long long)blockIdx.x * 256 + threadIdx.x;
   if (gid >= (long long)p.B * p.D * p.N) return;
   const int n = int(gid % p.N);

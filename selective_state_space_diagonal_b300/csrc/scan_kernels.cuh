@@ -131,6 +131,8 @@ struct TableParams {
   float* rot;  // (B, S, 4, N, 2): e^{i Phi} of sub-chunk s after its local steps 7, 15, 23 and
                // after its last step (row r: local step min(8 r + 7, last))
   int B, L, N, S;
+  int ng;      // nscan table only: lane groups per channel; state pairs are stored interleaved
+               // by group (pair q of group g at position q * ng + g)
 };
 
 template <typename Tin, int MODE>

@@ -3,6 +3,7 @@ bench reads DRAM traffic from the committed ncu summaries (only while their reco
 source hash matches the sources being built)."""
 import os
 
+import numpy as np
 import pytest
 
 import bench
@@ -10,8 +11,7 @@ from selective_state_space_diagonal_b300 import workloads as wl
 
 PROFILES = [
     # summary, kernel prefix, workload, the kernel sources its hash covers
-    ("scan_kernel_trap_bf16_batch.md", "scan_kernel", wl.WORKLOADS["trap_bf16_batch"], bench.KERNEL_SOURCES),
-    ("scan_kernel_zoh_bf16_batch.md", "scan_kernel", wl.WORKLOADS["zoh_bf16_batch"], bench.KERNEL_SOURCES),
+    ("scan_kernel_zoh_bf16_batch.md", "scan_kernel", wl.WORKLOADS["zoh_bf16_batch"], bench.ZOH_KERNEL_SOURCES),
     ("mimo_out_kernel_mimo_trap_bf16_batch.md", "mimo_out_kernel", wl.MIMO_WORKLOADS["mimo_trap_bf16_batch"],
      bench.MIMO_KERNEL_SOURCES),
 ]
@@ -58,9 +58,37 @@ def test_launch_and_operation_counts():
     assert bench.mimo_alu_ops_per_elem(4, 1) == pytest.approx(6.25)
     assert bench.mimo_alu_ops_per_elem(4, 0) == pytest.approx(5.25)
     assert bench.mimo_alu_ops_per_elem(1, 1) == pytest.approx(11.5)
-    assert bench.ZOH_ALU_OPS_PER_ELEM > bench.ALU_OPS_PER_ELEM
+    assert bench.ALU_OPS_PER_ELEM[0] == bench.ALU_OPS_PER_ELEM[1] == 6
+    assert bench.ZOH_ALU_OPS_PER_ELEM == bench.ALU_OPS_PER_ELEM[2] > bench.ALU_OPS_PER_ELEM[1]
+    assert bench.scan_kernel_name(wl.WORKLOADS["trap_bf16_batch"]) == "nscan_kernel"
+    assert bench.scan_kernel_name(wl.WORKLOADS["zoh_bf16_batch"]) == "scan_kernel"
 
 
 def test_workload_config_names_the_mode():
     names = {w.mode: bench.workload_config(w)["mode"] for w in wl.WORKLOADS.values()}
     assert names == {0: "exp-Euler", 1: "exp-trapezoidal", 2: "zero-order hold"}
+
+
+def test_clock_summary_and_alu_roofline():
+    s = bench.clock_summary([(2032.0, 2032.0, 700.0, []), (1990.0, 2032.0, 900.0, ["sw_power_cap"]),
+                             (2010.0, 2032.0, 800.0, [])])
+    assert s["sm_mhz"] == 2010.0 and s["sm_max_mhz"] == 2032.0 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"] and s["power_w_max"] == 900.0
+    empty = bench.clock_summary([])
+    assert empty["sm_mhz"] is None and empty["reasons"] == ["unsampled"]
+    # the FP32 peak follows the sampled clock; without a sample the fraction is unknown
+    r = bench.alu_roofline(6, 10 ** 9, 1e-3, s)
+    assert r["peak"] == pytest.approx(128 * 148 * 2010e6 / 1e12)
+    assert r["achieved"] == pytest.approx(6.0) and r["frac"] == pytest.approx(6.0 / r["peak"])
+    assert bench.alu_roofline(6, 10 ** 9, 1e-3, empty)["frac"] is None
+
+
+def test_parity_errors():
+    x = np.ones((1, 4, 2))
+    d = np.array([2.0, 0.0])
+    y_ref = np.array([[[3.0, 1.0], [2.5, 0.5], [2.0, 0.0], [4.0, 2.0]]])
+    y = y_ref.copy()
+    y[0, 3, 1] += 0.01
+    e, e_ssm = bench.parity_errors(y, y_ref, x, d)
+    assert e == pytest.approx(0.01 / 4.0)
+    assert e_ssm == pytest.approx(0.01 / 2.0)   # the state-space part y - Dskip x peaks at 2

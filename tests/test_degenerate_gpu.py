@@ -2,7 +2,9 @@
 trapezoid weight at its ends (lam = 1 is exp-Euler, lam = 0 keeps only the beta term), no
 rotation with real Bc and Cc (the real selective scan), no decay (A = 0: pure rotation, the
 memory longer than the sequence), decays so strong that 2^x underflows to zero, and a zero
-input (y must be exactly zero). Same tolerances as the parity tests (forward cases with
+input (y must vanish: |y| <= 1e-14; the exp-Euler and trapezoid kernels keep the state divided
+by its injection weight, whose magnitude is floored at 1e-20, so a zero weight still injects
+1e-20 Bc per step -- a state below 1e-17 and an output below 1e-15 at these sizes). Same tolerances as the parity tests (forward cases with
 Dskip = 0, so that y is the state-space part alone); backward tolerance as in its own tests."""
 import numpy as np
 import pytest
@@ -69,7 +71,7 @@ def test_degenerate_forward(kind, mode):
         inp = case(kind, mode, dtype, dskip=False)
         y = gu.run_gpu(gu.to_device(inp), mode)
         if kind == "zero_x":
-            assert float(y.abs().max()) == 0.0, f"{kind} m{mode} {dtype}: y not exactly zero"
+            assert float(y.abs().max()) <= 1e-14, f"{kind} m{mode} {dtype}: y does not vanish"
         else:
             check(inp, y, f"degenerate:{kind}:m{mode}:{dtype}")
 
