@@ -24,13 +24,6 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
-// Hardware base-2 logarithm (MUFU.LG2); denormal inputs flush to zero (giving -inf).
-__device__ __forceinline__ float lg2_approx(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 // Packed float32x2 fused multiply-add / multiply (one instruction for two lanes).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }

@@ -211,6 +211,8 @@ inline TableParams table_params(const Args& a, const Plan& pl, char* rest, int N
   tp.N = N;
   tp.S = int(pl.S);
   tp.ng = 1;
+  tp.planes = 2;
+  tp.plane_w = 2 * N;
   return tp;
 }
 
@@ -218,7 +220,9 @@ inline TableParams table_params(const Args& a, const Plan& pl, char* rest, int N
 template <int N, int NS, typename Tin, int MODE>
 struct NScan {
   using SG = NStage<N, NS, Tin, MODE>;
-  static constexpr KernelShape shape() { return KernelShape{NTile<N, NS>::DT, SG::SMEM, 4 * N, MODE == 1 ? 4 : 0}; }
+  static constexpr KernelShape shape() {
+    return KernelShape{NTile<N, NS>::DT, SG::SMEM, NTile<N, NS>::PLANES * NTile<N, NS>::W, MODE == 1 ? 4 : 0};
+  }
   static int occ(int carry, int dev, int* out) {
     if (carry == CARRY_SERIAL) return occupancy_of(nscan_kernel<N, NS, Tin, MODE, CARRY_SERIAL>, dev, SG::SMEM, out);
     if (carry == CARRY_DECOUPLED)
@@ -228,15 +232,18 @@ struct NScan {
   static int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* hdr, uint32_t* flags,
                      char* rest, cudaStream_t st) {
     TableParams tp = table_params(a, pl, rest, N);
-    tp.ng = NTile<N, NS>::NG;
+    using TL = NTile<N, NS>;
+    tp.ng = TL::NG;
+    tp.planes = TL::PLANES;
+    tp.plane_w = TL::W;
     ScanParams sp;
     std::memset(&sp, 0, sizeof(sp));
     const CUtensorMapDataType tin = sizeof(Tin) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const uint64_t s_in = sizeof(Tin);
     const uint64_t B = uint64_t(a.B), L = uint64_t(a.L), D = uint64_t(a.D), S = uint64_t(pl.S);
-    const uint64_t tdims[4] = {2 * N, 2, L, B};
-    const uint64_t tstrides[3] = {2 * N * 4, 4 * N * 4, L * 4 * N * 4};
-    const uint32_t tbox[4] = {2 * N, 2, SG::TAB_ROWS, 1};
+    const uint64_t tdims[4] = {TL::W, TL::PLANES, L, B};
+    const uint64_t tstrides[3] = {TL::W * 4, TL::PLANES * TL::W * 4, L * TL::PLANES * TL::W * 4};
+    const uint32_t tbox[4] = {TL::W, TL::PLANES, SG::TAB_ROWS, 1};
     bool ok = map3(&sp.tm_x, tin, a.x, D, L, B, D * s_in, L * D * s_in, pl.DT, SG::X_ROWS, 1) &&
               map3(&sp.tm_dt, tin, a.delta, D, L, B, D * s_in, L * D * s_in, pl.DT, SG::DT_ROWS, 1) &&
               make_map(&sp.tm_tab, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.tab, 4, tdims, tstrides, tbox) &&

@@ -15,17 +15,15 @@
 //    exp-Euler w_t = dt_t x_t; trapezoid (look-ahead form of scan_kernels.cuh, k_{t+1} there)
 //    w_t = x_t (lam_t dt_t + (1 - lam_{t+1}) dt_{t+1}). With sigma_t = w_t + sign(w_t) FLOOR and
 //    s_t = k_t / sigma_t this is
-//        s_t = rho_t s_{t-1} + Bt_t,   rho_t = r_t sigma_{t-1} / sigma_t,
+//        s_t = rho_t s_{t-1} + Bt_t,   rho_t = 2^{dt_t A log2 e} (sigma_{t-1} / sigma_t),
 //        y_t = sigma_t Re(sum_n Ct_t s_t) (+ the trapezoid correction and Dskip x_t):
-//    the injection is the table entry itself and the per-element product w_t Bt_t disappears.
-//    rho_t is formed either as 2^{dt_t A log2 e + lg2|sigma_{t-1}| - lg2|sigma_t|} with the sign
-//    of sigma_{t-1} sigma_t XORed into its sign bit (the ratio enters the exponent's FMA, the sign
-//    costs an integer op on the ALU pipe), or as 2^{dt_t A log2 e} times the signed ratio (one
-//    packed multiply): NSCAN_SIGN_MUL selects. Per element that is 5 or 6 FP32 lane-ops where the
-//    unnormalised update takes 7, and every lane of a warp reads the same table row, so the
-//    shared-memory loads are broadcasts. The hardware logarithms of consecutive steps cancel in
-//    the product of the ratios, so their errors do not accumulate; FLOOR (1e-20) changes an
-//    injection by at most 1e-20 |Bt| (a zero input gives an output of order 1e-20, not 0).
+//    the injection is the table entry itself, the per-(t, d) ratio costs one MUFU reciprocal per
+//    channel and step, and the per-element product w_t Bt_t becomes one packed multiply of the
+//    decay by the ratio: 6 FP32 lane-ops per element where the unnormalised update takes 7, and
+//    every lane of a warp reads the same table row (broadcast shared-memory loads). FLOOR
+//    (1e-20) changes an injection by at most 1e-20 |Bt| (a zero input gives an output of order
+//    1e-20, not 0). The ratio's rounding is a relative error of a few ulps per step, the same
+//    order as that of the hardware 2^x.
 // 3. Thread tile. A thread owns one channel and NS consecutive states of it (NG = N / NS lanes
 //    per channel, combined with shuffles); a block of 4 warps owns DT = 128 / NG channels.
 //    The per-channel scalars (x, dt, the weight, its logarithm) are formed once per step for
@@ -39,13 +37,11 @@
 namespace csscan {
 
 constexpr float NSCAN_FLOOR = 1e-20f;
-#ifndef NSCAN_SIGN_MUL
-#define NSCAN_SIGN_MUL 1
-#endif
-#ifndef NSCAN_RING_KB
-#define NSCAN_RING_KB 80
-#endif
-constexpr int NRING_BYTES = NSCAN_RING_KB * 1024;   // shared memory for the ring of one block (at least 2 stages)
+// Shared memory for the ring of one block (at least 2 stages): 80 KB holds three stages of the
+// bf16 N = 16 tile, which leaves two blocks per SM; measured on B300, a third stage (the warps
+// release stages independently and drift apart) with two resident blocks beats two stages with
+// three resident blocks.
+constexpr int NRING_BYTES = 80 * 1024;
 
 template <int N, int NS>
 struct NTile {
@@ -53,6 +49,10 @@ struct NTile {
   static constexpr int NPAIR = NS / 2;
   static constexpr int CPW = 32 / NG;
   static constexpr int DT = WARPS * CPW;
+  // table row: two planes (Bt, Ct) of W = 2N floats, state pairs interleaved by lane group
+  static constexpr int PLANES = 2;
+  static constexpr int W = 2 * N;
+  static constexpr int W4 = W / 4;
   static_assert(NS >= 2 && NS % 2 == 0 && N % NS == 0 && NG <= 32 && (NG & (NG - 1)) == 0, "unsupported tile");
 };
 
@@ -68,7 +68,7 @@ struct NStage {
   static constexpr int AUX_ROWS = T_SUB + 1;
   static constexpr int X_BYTES = X_ROWS * DT * SIN;
   static constexpr int DT_BYTES = DT_ROWS * DT * SIN;
-  static constexpr int TAB_BYTES = TAB_ROWS * 4 * N * 4;
+  static constexpr int TAB_BYTES = TAB_ROWS * NTile<N, NS>::PLANES * NTile<N, NS>::W * 4;
   static constexpr int AUX_BYTES = MODE == 1 ? AUX_ROWS * 16 : 0;
   static constexpr int ROT_BYTES = 2 * N * 4;
   static constexpr int OFF_X = 0;
@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(256) ntable_kernel(TableParams p) {
   // group g = j / npair, stored at float4 q * ng + g (neighbouring groups read neighbouring banks)
   const int npair = p.N / (2 * p.ng);
   const int idx = (((n >> 1) % npair) * p.ng + (n >> 1) / npair) * 4 + (n & 1);
-  const int N2 = 2 * p.N;
+  const int W = p.plane_w;
   float phi = 0.f, cs = 1.f, sn = 0.f;
   float* rr = p.rot + ((int64_t(b) * p.S + s) * 4 * p.N + n) * 2;
   // E_t by a shuffle sum over the N lanes of (b, s), neighbours in a warp when N <= 32
@@ -123,11 +123,15 @@ __global__ void __launch_bounds__(256) ntable_kernel(TableParams p) {
     const float cr = load_in<Tin>(Cc, 2 * tn), ci = load_in<Tin>(Cc, 2 * tn + 1);
     const float btr = cs * br + sn * bi;   // Re(e^{-i Phi} Bc)
     const float bti = cs * bi - sn * br;   // Im(e^{-i Phi} Bc)
-    float* row = p.tab + (int64_t(b) * p.L + t) * (2 * N2);
+    float* row = p.tab + (int64_t(b) * p.L + t) * (p.planes * W);
     row[idx] = btr;
     row[idx + 2] = bti;
-    row[N2 + idx] = cs * cr - sn * ci;        // Re(e^{+i Phi} Cc)
-    row[N2 + idx + 2] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
+    row[W + idx] = cs * cr - sn * ci;        // Re(e^{+i Phi} Cc)
+    row[W + idx + 2] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
+    if (p.planes == 3) {
+      row[2 * W + idx] = -btr;
+      row[2 * W + idx + 2] = -bti;
+    }
     if (lane_sum) {
       float E = cr * br - ci * bi;
       for (int o = p.N / 2; o >= 1; o >>= 1) E += __shfl_xor_sync(gmask, E, o);
@@ -162,9 +166,9 @@ __global__ void __launch_bounds__(256) ntable_kernel(TableParams p) {
 // Parameters: ScanParams of scan_kernels.cuh, with tm_tab a 4-D map (2N, 2, L, B) boxed
 // (2N, 2, T_SUB, 1), tm_aux (4, L, B) boxed (4, AUX_ROWS, 1), tm_rot boxed (2N, 1, 1), tm_x boxed
 // (DT, X_ROWS, 1) and tm_dt boxed (DT, DT_ROWS, 1).
-#ifndef NSCAN_MIN_BLOCKS
-#define NSCAN_MIN_BLOCKS 2
-#endif
+// Two resident blocks per SM (the ring allows no more for the large tiles): up to 255 registers,
+// which the decoupled variant needs to hold its look-back state without spilling.
+constexpr int NSCAN_MIN_BLOCKS = 2;
 
 template <int N, int NS, typename Tin, int MODE, int CARRY>
 __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const __grid_constant__ ScanParams p) {
@@ -172,7 +176,8 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
   using SG = NStage<N, NS, Tin, MODE>;
   constexpr int NG = TL::NG, NPAIR = TL::NPAIR, CPW = TL::CPW, DT = TL::DT;
   constexpr int NST = SG::NST;
-  constexpr int HN = N / 2;   // float4 per table plane
+  constexpr int W4 = TL::W4;  // float4 per table plane (with padding)
+  constexpr int PL = TL::PLANES;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
@@ -299,12 +304,10 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
   bool aborted = false;
 
   // Per-step scalars of the software pipeline: what the output of a step needs (x, the signed
-  // weight scale sigma, the trapezoid's correction p_{t+1} E_t), and what the next step's decay
-  // needs (lg2 |sigma| and the sign bit of sigma, or sigma itself). The step's decays live
-  // beside it in a float2[NPAIR].
+  // weight scale sigma, the trapezoid's correction p_{t+1} E_t) and what the next step needs
+  // (sigma, and the trapezoid's dt_{t+1}). The step's decays live beside it in a float2[NPAIR].
   struct Scal {
-    float x, sig, lg, pc, E, dt, dtn;
-    uint32_t sbit;
+    float x, sig, pc, E, dt, dtn;
   };
 
   // One pass over the chunk's sub-chunks, starting from the true state in (sr, si). WITH_Y: write
@@ -355,40 +358,24 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
         }
         sc.x = x;
         sc.dt = dt;
-        sc.sbit = __float_as_uint(w) & 0x80000000u;
-        const float aw = fabsf(w) + NSCAN_FLOOR;
-        sc.sig = __uint_as_float(__float_as_uint(aw) | sc.sbit);
+        // sigma = w + sign(w) FLOOR
+        sc.sig = __uint_as_float(__float_as_uint(fabsf(w) + NSCAN_FLOOR) | (__float_as_uint(w) & 0x80000000u));
         const float2 dt2 = f2(dt, dt);
-#if NSCAN_SIGN_MUL
         // decay times sigma_{t-1} / sigma_t as a packed multiply by the signed ratio
         const float q = pv.sig * rcp_approx(sc.sig);
         const float2 q2 = f2(q, q);
 #pragma unroll
         for (int k = 0; k < NPAIR; ++k) e[k] = mul2(ex2_pair(mul2(dt2, Ap[k])), q2);
-#else
-        // |sigma_{t-1} / sigma_t| in the exponent, its sign as the sign bit of the decay
-        sc.lg = lg2_approx(aw);
-        const float l = pv.lg - sc.lg;
-        const float2 l2 = f2(l, l);
-        const uint32_t flip = sc.sbit ^ pv.sbit;
-#pragma unroll
-        for (int k = 0; k < NPAIR; ++k) {
-          const float2 r = ex2_pair(fma2(dt2, Ap[k], l2));
-          e[k] = f2(__uint_as_float(__float_as_uint(r.x) ^ flip), __uint_as_float(__float_as_uint(r.y) ^ flip));
-        }
-#endif
       };
       if (i == 0) {   // the pass starts from the unscaled state: sigma_{-1} = 1
         Scal one;
         one.sig = 1.f;
-        one.lg = 0.f;
-        one.sbit = 0u;
         one.dtn = smem_in<Tin>(sdt, 0);
         prep(0, one, cur, ec);
       }
 
       auto step = [&](int tt) {
-        const float4* row = stab + tt * (2 * HN);
+        const float4* row = stab + tt * (PL * W4);
         Scal nxt;
         float2 en[NPAIR];
         prep(tt + 1, cur, nxt, en);
@@ -399,7 +386,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
           sr[q] = fma2(ec[q], sr[q], f2(bb.x, bb.y));
           si[q] = fma2(ec[q], si[q], f2(bb.z, bb.w));
           if (WITH_Y) {
-            const float4 cc = row[HN + q * NG];
+            const float4 cc = row[W4 + q * NG];
             float2& acc = (q & 1) ? acc1 : acc0;
             acc = fma2(f2(cc.z, cc.w), si[q], fma2(f2(cc.x, cc.y), sr[q], acc));
           }

@@ -133,6 +133,8 @@ struct TableParams {
   int B, L, N, S;
   int ng;      // nscan table only: lane groups per channel; state pairs are stored interleaved
                // by group (pair q of group g at position q * ng + g)
+  int planes;  // nscan table only: planes per row (Bt, Ct, and -Bt when 3)
+  int plane_w; // nscan table only: floats per plane (2N plus padding)
 };
 
 template <typename Tin, int MODE>

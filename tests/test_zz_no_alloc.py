@@ -4,8 +4,9 @@ Some callers cannot call cudaMalloc: a serving loop that must not allocate once 
 (cudaMalloc may synchronise the device and has no latency bound), or a program whose device
 memory is owned entirely by another allocator or a fixed budget. For them the library keeps
 its scratch in one fixed array and never allocates. This test checks, through the C ABI, that
-two calls in a row give the same output as csscan_forward within the parity tolerance, and
-that a problem too large for the fixed array is refused before any launch.
+two calls in a row give the same output as csscan_forward within the parity tolerance, that
+both match the float64 oracle on sampled rows within the same tolerance, and that a problem
+too large for the fixed array is refused before any launch.
 
 Kept in a file of its own that pytest collects last; it passes alone in a fresh process and
 after the other tests.
@@ -43,7 +44,8 @@ def rel_diff(a: torch.Tensor, b: torch.Tensor) -> float:
 ])
 def test_noalloc_matches_forward_twice(name, shape):
     w = wl.WORKLOADS[name].with_shape(**shape)
-    dev = gu.to_device(wl.generate(w))
+    inp = wl.generate(w)
+    dev = gu.to_device(inp)
     args = (dev["x"], dev["delta"], dev["A"], dev["Bc"], dev["Cc"], dev["theta"], dev["lam"], dev["Dskip"])
     y_ref = torch.full((w.B, w.L, w.D), float("nan"), device="cuda")
     csscan.csscan_forward(*args, y_ref, w.mode)
@@ -58,6 +60,14 @@ def test_noalloc_matches_forward_twice(name, shape):
         assert bool(torch.isfinite(y).all()), f"call {call}: unwritten or non-finite outputs"
         e = rel_diff(y, y_ref)
         assert e <= gu.TOL[w.dtype], f"call {call}: differs from csscan_forward by {e:.3e}"
+        # and against the oracle: the first and last batch rows, six channels
+        ds = np.array([0, 5, w.D // 3, w.D // 2, w.D - 7, w.D - 1])
+        for b in sorted({0, w.B - 1}):
+            y_or = gu.oracle_y(inp, b_rows=[b], d_rows=ds)
+            x64 = wl.widen(inp, b=slice(b, b + 1), d=ds)["x"]
+            e_or, _ = gu.errors(y[b:b + 1][:, :, ds].cpu().numpy().astype(np.float64), y_or, x64,
+                                inp.Dskip.astype(np.float64)[ds])
+            assert e_or <= gu.TOL[w.dtype], f"call {call}, batch row {b}: differs from the oracle by {e_or:.3e}"
 
 
 def test_noalloc_refuses_oversized_problem():
