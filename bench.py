@@ -81,7 +81,17 @@ def parse_args(argv=None):
     p.add_argument("--backward-steps", type=int, default=5)
     p.add_argument("--no-per-config", action="store_true", help="skip the other benchmark shapes")
     p.add_argument("--config-steps", type=int, default=20, help="timed steps of each per-config entry")
+    p.add_argument("--batch", type=int, default=0, help="override the workload's B (smaller profiling cases)")
+    p.add_argument("--length", type=int, default=0, help="override the workload's L (smaller profiling cases)")
     return p.parse_args(argv)
+
+
+def selected_workload(args):
+    """The workload named by --workload, with --batch / --length applied."""
+    table = wl.MIMO_WORKLOADS if args.workload in wl.MIMO_WORKLOADS else wl.WORKLOADS
+    w = table[args.workload]
+    kw = {k: v for k, v in (("B", args.batch), ("L", args.length)) if v}
+    return w.with_shape(**kw) if kw else w
 
 
 def measured_peaks():
@@ -389,7 +399,7 @@ def run_reference(args):
     rank, world, _ = rank_info()
     if rank != 0:
         return 0
-    w = wl.WORKLOADS[args.workload]
+    w = selected_workload(args)
     inp = wl.generate(w)
     per_step = max(1.0, min(5.0, 150.0 / max(1, args.steps + args.warmup)))
     value, cores, desc, _, _ = cpu_oracle_sample(inp, per_step)
@@ -571,7 +581,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     csscan.load_library()
-    w = rank_workload(wl.WORKLOADS[args.workload], rank)
+    w = rank_workload(selected_workload(args), rank)
     inp = wl.generate(w)
     keys = ("x", "delta", "A", "Bc", "Cc", "theta", "lam", "Dskip")
     host, dev = to_device(inp, keys, pinned=True)
@@ -645,7 +655,8 @@ def run_ours(args):
     kernel = scan_kernel_name(w)
     hbm_achieved = w.min_bytes() / scan_s / 1e9
     roofline = {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": hbm_achieved / hbm_peak, "traffic": traffic_from_profiles(w.name, kernel),
+                "frac": hbm_achieved / hbm_peak,
+                "traffic": None if (args.batch or args.length) else traffic_from_profiles(w.name, kernel),
                 "kernel": kernel, "ms_per_launch": 1e3 * scan_s, "peak_kind": peak_kind,
                 "frac_of_nominal": hbm_achieved / HBM_NOMINAL_GBS, "nominal_peak": HBM_NOMINAL_GBS,
                 "algorithmic_bytes_per_launch": w.min_bytes(),
@@ -905,7 +916,7 @@ def run_mimo(args):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        w = wl.MIMO_WORKLOADS[args.workload]
+        w = selected_workload(args)
         inp = wl.generate_mimo(w)
         v, cores, desc, secs = mimo_cpu_sample(inp, max(1.0, min(5.0, 150.0 / max(1, args.steps + args.warmup))))
         line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
@@ -920,7 +931,7 @@ def run_mimo(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     csscan.load_library()
-    w = rank_workload(wl.MIMO_WORKLOADS[args.workload], rank)
+    w = rank_workload(selected_workload(args), rank)
     inp = wl.generate_mimo(w)
     keys = ("x", "delta", "A", "Bm", "Cm", "theta", "lam", "Dskip")
     host, dev = to_device(inp, keys, pinned=True)
