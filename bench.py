@@ -743,10 +743,11 @@ KERNEL_SOURCES = ("selective_state_space_diagonal_b300/csrc/nscan_kernels.cuh",
                   "selective_state_space_diagonal_b300/csrc/device_util.cuh")
 ZOH_KERNEL_SOURCES = ("selective_state_space_diagonal_b300/csrc/scan_kernels.cuh",
                       "selective_state_space_diagonal_b300/csrc/device_util.cuh")
-MIMO_KERNEL_SOURCES = ("selective_state_space_diagonal_b300/csrc/mimo_kernels.cuh",
+MIMO_KERNEL_SOURCES = ("selective_state_space_diagonal_b300/csrc/mscan_kernels.cuh",
+                       "selective_state_space_diagonal_b300/csrc/scan_kernels.cuh",
                        "selective_state_space_diagonal_b300/csrc/device_util.cuh")
 SOURCES_OF = {"nscan_kernel": KERNEL_SOURCES, "scan_kernel": ZOH_KERNEL_SOURCES,
-              "mimo_out_kernel": MIMO_KERNEL_SOURCES}
+              "mscan_kernel": MIMO_KERNEL_SOURCES}
 
 
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
@@ -780,12 +781,12 @@ def traffic_from_profiles(workload: str, kernel: str = "nscan_kernel", sources=N
 
 # ------------------------------------------------------------------------------ MIMO workloads
 def mimo_alu_ops_per_elem(P: int, mode: int) -> float:
-    """FP32 lane-operations per (b,t,h,p,n) element of csscan_forward_mimo's output kernel,
-    counted from its source (rotating frame, state pairs): the rank-P injection 2 and the output
-    2.5 (its packed product and the sum of the pair) per element; the decay exponent (1) and
-    the update (exp-Euler 2; trapezoid 6: g, then k with the look-ahead) per (b,t,h,n), shared
+    """FP32 lane-operations per (b,t,h,p,n) element of csscan_forward_mimo's staged kernel
+    (mscan_kernel), counted from its formulation (rotating frame, trapezoid in look-ahead form,
+    so both modes do the same per-element work): the rank-P injection (re, im) 2 and the output
+    Re(Ct k) 2 per element; the decay exponent 1 and the update (re, im) 2 per (b,t,h,n), shared
     by the P channels."""
-    return 4.5 + (7.0 if mode == 1 else 3.0) / P
+    return 4.0 + 3.0 / P
 
 
 def mimo_cpu_sample(inp, target_s: float):
@@ -822,8 +823,18 @@ def mimo_config(w) -> dict:
             "elements": w.elements, "elements_note": "B*L*H*P*N channel-state pairs", "min_bytes": w.min_bytes()}
 
 
+def mimo_staged(w) -> bool:
+    """Whether csscan_forward_mimo takes the staged kernel for this shape (device buffers from
+    the caching allocator are 16-byte aligned)."""
+    s = w.in_bytes
+    return w.N in (8, 16, 32) and w.P * w.N <= 128 and (w.H * w.P * s) % 16 == 0 and (w.H * s) % 16 == 0
+
+
 def mimo_launches(w, nsm: int) -> int:
-    # phase table and output pass; with time chunks also the e^{i theta} table, the chunk pass and the sweep
+    if mimo_staged(w):
+        return 2   # table kernel + mscan_kernel
+    # per-state kernels: phase table and output pass; with time chunks also the e^{i theta}
+    # table, the chunk pass and the sweep
     return 2 if w.B * w.H * w.N * w.P >= nsm * 4096 else 5
 
 
@@ -899,7 +910,7 @@ def measure_mimo_config(label, name, args, stream, local, scratch, hbm_peak) -> 
            "hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
                    "frac_of_nominal": gbs / HBM_NOMINAL_GBS},
            "alu": alu_roofline(mimo_alu_ops_per_elem(w.P, w.mode), w.elements, mean_s, t["clocks"]),
-           "kernel": "mimo_out_kernel (+ table and chunk passes)", "clocks": t["clocks"],
+           "kernel": "mscan_kernel (+ table pass)", "clocks": t["clocks"],
            "gpu_launches": mimo_launches(w, nsm) * steps, "parity": mimo_parity(inp, y)}
     del dev, y
     torch.cuda.empty_cache()
@@ -974,8 +985,8 @@ def run_mimo(args):
             "ms_per_step": t["elapsed_ms"] / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic", "config": dict(mimo_config(w), l2=l2_note(w, t["flush"])),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-                         "traffic": traffic_from_profiles(w.name, "mimo_out_kernel"),
-                         "kernel": "mimo_out_kernel (+ table and chunk passes)", "ms_per_launch": 1e3 * mean_s,
+                         "traffic": traffic_from_profiles(w.name, "mscan_kernel"),
+                         "kernel": "mscan_kernel (+ table pass)", "ms_per_launch": 1e3 * mean_s,
                          "peak_kind": peak_kind, "frac_of_nominal": gbs / HBM_NOMINAL_GBS},
             "alu": alu_roofline(mimo_alu_ops_per_elem(w.P, w.mode), w.elements, mean_s, t["clocks"]),
             "parity": mimo_parity(inp, y),

@@ -14,10 +14,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 SOURCES = [os.path.join(CSRC, f) for f in ("csscan.cu", "forward_f32.cu", "forward_bf16.cu", "backward_f32.cu",
-                                           "backward_bf16.cu", "mimo.cu")]
+                                           "backward_bf16.cu", "mimo_f32.cu", "mimo_bf16.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("scan_kernels.cuh", "nscan_kernels.cuh", "device_util.cuh",
-                                           "decode_kernel.cuh", "backward_kernels.cuh", "mimo_kernels.cuh",
-                                           "forward_launch.cuh", "backward_launch.cuh", "host_common.h")] + \
+                                           "decode_kernel.cuh", "backward_kernels.cuh", "mimo_kernels.cuh", "mscan_kernels.cuh",
+                                           "forward_launch.cuh", "backward_launch.cuh", "mimo_launch.cuh", "host_common.h")] + \
           [os.path.join(ROOT, "include", "csscan.h")]
 OUTPUT = os.path.join(HERE, "libcsscan.so")
 BUILD_DIR = os.path.join(HERE, "_build")

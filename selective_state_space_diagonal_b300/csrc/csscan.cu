@@ -1,6 +1,6 @@
 // csscan.cu -- the C ABI declared in include/csscan.h: argument checks, the per-(device,
 // stream) workspace, the decode step and the no-allocation entry point. The scans themselves
-// are planned and launched by the per-dtype units (forward_*.cu, backward_*.cu, mimo.cu).
+// are planned and launched by the per-dtype units (forward_*.cu, backward_*.cu, mimo_*.cu).
 #include <cudaTypedefs.h>
 
 #include <algorithm>

@@ -54,14 +54,51 @@ template <> __device__ __forceinline__ float smem_in<uint16_t>(const uint16_t* p
   return bf16_bits_to_float(p[i]);
 }
 
+// The K consecutive values p[0 .. K-1] widened to float, with vector loads (p aligned to
+// K * sizeof(Tin) bytes; K = 1, 2, 4 or 8).
+template <typename Tin, int K>
+__device__ __forceinline__ void smem_row(const Tin* p, float (&v)[K]) {
+  if constexpr (sizeof(Tin) == 4) {
+    if constexpr (K % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < K / 4; ++i) {
+        const float4 f = reinterpret_cast<const float4*>(p)[i];
+        v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+      }
+    } else if constexpr (K == 2) {
+      const float2 f = *reinterpret_cast<const float2*>(p);
+      v[0] = f.x; v[1] = f.y;
+    } else {
+      v[0] = p[0];
+    }
+  } else {
+    uint32_t w[(K + 1) / 2];
+    if constexpr (K == 8) {
+      const uint4 u = *reinterpret_cast<const uint4*>(p);
+      w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    } else if constexpr (K == 4) {
+      const uint2 u = *reinterpret_cast<const uint2*>(p);
+      w[0] = u.x; w[1] = u.y;
+    } else if constexpr (K == 2) {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    } else {
+      w[0] = uint32_t(p[0]);
+    }
+#pragma unroll
+    for (int i = 0; i < K; ++i)
+      v[i] = __uint_as_float((i & 1) ? (w[i / 2] & 0xffff0000u) : (w[i / 2] << 16));
+  }
+}
+
 // ---------------------------------------------------------------------------- lane sums
 // Reduce-scatter of NARR arrays v[k][0 .. LEN-1] over the N lanes of a lane group (lane bits
 // below N; N and LEN powers of two): rounds with the high masks halve the arrays (each lane
 // keeps one half and adds its partner's copy of it), rounds with the remaining masks add whole
 // values. Afterwards a lane holds the group sums for entries base .. base + max(1, LEN/N) - 1 in
 // v[k][0 ..]; lanes that differ only in bits below max(1, N/LEN) hold the same entries.
-// Returns base. `lane` is the lane's index within its group.
-template <int N, int NARR, int LEN>
+// Returns base. `lane` is the lane's index within its group; the group's lanes are STRIDE apart
+// in the warp (partners differ by m * STRIDE).
+template <int N, int NARR, int LEN, int STRIDE = 1>
 __device__ __forceinline__ int butterfly(float (&v)[NARR][LEN], int lane) {
   int base = 0;
   int len = LEN;
@@ -77,15 +114,27 @@ __device__ __forceinline__ int butterfly(float (&v)[NARR][LEN], int lane) {
           if (i < half) {
             const float send = upper ? v[k][i] : v[k][i + half];
             const float keep = upper ? v[k][i + half] : v[k][i];
-            v[k][i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            v[k][i] = keep + __shfl_xor_sync(0xffffffffu, send, m * STRIDE);
           }
       if (upper) base += half;
       len = half;
     } else {
 #pragma unroll
-      for (int k = 0; k < NARR; ++k) v[k][0] += __shfl_xor_sync(0xffffffffu, v[k][0], m);
+      for (int k = 0; k < NARR; ++k) v[k][0] += __shfl_xor_sync(0xffffffffu, v[k][0], m * STRIDE);
     }
   }
+  return base;
+}
+// The base butterfly<N, NARR, LEN> returns for a lane, without the sums.
+template <int N, int LEN>
+__device__ __forceinline__ int butterfly_base(int lane) {
+  int base = 0, len = LEN;
+#pragma unroll
+  for (int m = N / 2; m >= 1; m >>= 1)
+    if (len > 1) {
+      if (lane & m) base += len / 2;
+      len /= 2;
+    }
   return base;
 }
 

@@ -41,7 +41,8 @@ using OccFn = int (*)(int carry, int dev, int* occ);
 
 // Blocks of THREADS threads with `smem` dynamic bytes resident per SM (cached per kernel and
 // device; the opt-in shared-memory limit is raised once per kernel and device).
-inline int occupancy_of(void (*kern)(ScanParams), int dev, int smem, int* out) {
+template <typename PT>
+int occupancy_of(void (*kern)(PT), int dev, int smem, int* out) {
   static std::mutex mu;
   static std::map<std::tuple<const void*, int, int>, int> cache;
   static std::map<std::pair<const void*, int>, bool> attr_set;

@@ -101,7 +101,7 @@ int forward_bf16(const Args& a, const csscan_options_t& o, cudaStream_t st, cons
 // Backward of a validated, non-empty problem. Defined in backward_f32.cu / backward_bf16.cu.
 int backward_f32(const BwdArgs& a, cudaStream_t st);
 int backward_bf16(const BwdArgs& a, cudaStream_t st);
-// MIMO scan of a validated, non-empty problem. Defined in mimo.cu.
+// MIMO scan of a validated, non-empty problem. Defined in mimo_f32.cu / mimo_bf16.cu.
 int mimo_f32(const MimoArgs& a, cudaStream_t st);
 int mimo_bf16(const MimoArgs& a, cudaStream_t st);
 

@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(256) mimo_chunk_kernel(const Params p) {
   rec[1] = make_float2(Pr, Pi);
 }
 
-__global__ void __launch_bounds__(256) mimo_combine_kernel(const Params p) {
+static __global__ void __launch_bounds__(256) mimo_combine_kernel(const Params p) {
   const long long gid = (long long)blockIdx.x * 256 + threadIdx.x;
   if (gid >= (long long)p.B * p.H * p.N) return;
   const int n = int(gid % p.N);

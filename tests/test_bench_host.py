@@ -56,9 +56,11 @@ def test_traffic_read_only_for_matching_sources(tmp_path, monkeypatch):
 def test_launch_and_operation_counts():
     for w in wl.WORKLOADS.values():
         assert bench.launches_per_step(w) == 2        # table kernel + scan kernel in every mode
-    assert bench.mimo_alu_ops_per_elem(4, 1) == pytest.approx(6.25)
-    assert bench.mimo_alu_ops_per_elem(4, 0) == pytest.approx(5.25)
-    assert bench.mimo_alu_ops_per_elem(1, 1) == pytest.approx(11.5)
+    assert bench.mimo_alu_ops_per_elem(4, 1) == bench.mimo_alu_ops_per_elem(4, 0) == pytest.approx(4.75)
+    assert bench.mimo_alu_ops_per_elem(1, 1) == pytest.approx(7.0)
+    w = wl.MIMO_WORKLOADS["mimo_trap_bf16_batch"]
+    assert bench.mimo_staged(w) and bench.mimo_launches(w, 148) == 2
+    assert not bench.mimo_staged(w.with_shape(H=5)) and not bench.mimo_staged(w.with_shape(N=4))
     assert bench.ALU_OPS_PER_ELEM[0] == bench.ALU_OPS_PER_ELEM[1] == 6
     assert bench.ZOH_ALU_OPS_PER_ELEM == bench.ALU_OPS_PER_ELEM[2] > bench.ALU_OPS_PER_ELEM[1]
     assert bench.scan_kernel_name(wl.WORKLOADS["trap_bf16_batch"]) == "nscan_kernel"

@@ -113,3 +113,34 @@ def test_mimo_rejects():
         csscan.csscan_forward_mimo(dev["x"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], dev["theta"], None,
                                    dev["Dskip"], y, 1)   # trapezoid without lambda
     assert e.value.status == csscan.CSSCAN_ERR_INVALID_ARG
+
+
+# Shapes whose (b, t) rows of x and dt are whole multiples of 16 bytes take the staged kernel
+# (mscan_kernel) for N = 8, 16, 32 with P N <= 128; the shapes above (3 or 5 heads, N = 2, 4)
+# take the per-state kernels. H = 40 leaves a partial head tile, L = 130 a ragged sub-chunk,
+# and the few tiles split the sequence into decoupled chunks.
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+@pytest.mark.parametrize("N", [8, 16, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_mimo_staged_matches_oracle(P, N, mode):
+    for (B, L, H, dtype) in [(2, 45, 8, "f32"), (1, 130, 40, "bf16"), (3, 300, 16, "f32")]:
+        w = BASE.with_shape(B=B, L=L, H=H, P=P, N=N, mode=mode, dtype=dtype, seed=BASE.seed + 13 * P + 5 * N + L)
+        inp = wl.generate_mimo(w)
+        check(inp, run(inp), f"staged P{P}:N{N}:m{mode}:{dtype}:{B}x{L}x{H}")
+
+
+def test_mimo_staged_serial_chunks():
+    """More head tiles than resident blocks: the planner splits the sequence into serial chunks."""
+    w = BASE.with_shape(B=32, L=200)
+    inp = wl.generate_mimo(w)
+    y = run(inp)
+    assert np.isfinite(y).all()
+    check(inp, y, "serial b0", b=slice(0, 1), h=np.array([0, 31, 32, 639]))
+    check(inp, y, "serial b31", b=slice(31, 32), h=np.array([3, 320]))
+
+
+def test_mimo_staged_long_decoupled():
+    """One head tile over a long sequence: many decoupled chunks and their look-back windows."""
+    w = BASE.with_shape(B=1, L=20000, H=32, P=4, N=16, mode=1, dtype="bf16", dt_lo=1e-4, dt_hi=1e-2)
+    inp = wl.generate_mimo(w)
+    check(inp, run(inp), "staged long", h=np.array([0, 17, 31]))
