@@ -13,7 +13,7 @@ PROFILES = [
     # summary, kernel prefix, workload, the kernel sources its hash covers
     ("nscan_kernel_trap_bf16_batch.md", "nscan_kernel", wl.WORKLOADS["trap_bf16_batch"], bench.KERNEL_SOURCES),
     ("scan_kernel_zoh_bf16_batch.md", "scan_kernel", wl.WORKLOADS["zoh_bf16_batch"], bench.ZOH_KERNEL_SOURCES),
-    ("mimo_out_kernel_mimo_trap_bf16_batch.md", "mimo_out_kernel", wl.MIMO_WORKLOADS["mimo_trap_bf16_batch"],
+    ("mscan_kernel_mimo_trap_bf16_batch.md", "mscan_kernel", wl.MIMO_WORKLOADS["mimo_trap_bf16_batch"],
      bench.MIMO_KERNEL_SOURCES),
 ]
 
