@@ -28,6 +28,7 @@ __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b
 // Packed float32x2 fused multiply-add / multiply (one instruction for two lanes).
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 // 2^z for both halves of a pair.
 __device__ __forceinline__ float2 ex2_pair(float2 z) { return make_float2(ex2_approx(z.x), ex2_approx(z.y)); }
 

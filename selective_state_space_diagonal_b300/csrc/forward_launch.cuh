@@ -218,20 +218,23 @@ inline TableParams table_params(const Args& a, const Plan& pl, char* rest, int N
 }
 
 // ============================================================================ nscan family
-template <int N, int NS, typename Tin, int MODE>
+// CKPT: the checkpoint variant (no y; the rotated-frame state before every 8-step segment into
+// `ckpt`), which the backward pass launches.
+template <int N, int NS, typename Tin, int MODE, bool CKPT = false>
 struct NScan {
   using SG = NStage<N, NS, Tin, MODE>;
   static constexpr KernelShape shape() {
     return KernelShape{NTile<N, NS>::DT, SG::SMEM, NTile<N, NS>::PLANES * NTile<N, NS>::W, MODE == 1 ? 4 : 0};
   }
   static int occ(int carry, int dev, int* out) {
-    if (carry == CARRY_SERIAL) return occupancy_of(nscan_kernel<N, NS, Tin, MODE, CARRY_SERIAL>, dev, SG::SMEM, out);
+    if (carry == CARRY_SERIAL)
+      return occupancy_of(nscan_kernel<N, NS, Tin, MODE, CARRY_SERIAL, CKPT>, dev, SG::SMEM, out);
     if (carry == CARRY_DECOUPLED)
-      return occupancy_of(nscan_kernel<N, NS, Tin, MODE, CARRY_DECOUPLED>, dev, SG::SMEM, out);
-    return occupancy_of(nscan_kernel<N, NS, Tin, MODE, CARRY_NONE>, dev, SG::SMEM, out);
+      return occupancy_of(nscan_kernel<N, NS, Tin, MODE, CARRY_DECOUPLED, CKPT>, dev, SG::SMEM, out);
+    return occupancy_of(nscan_kernel<N, NS, Tin, MODE, CARRY_NONE, CKPT>, dev, SG::SMEM, out);
   }
   static int enqueue(const Args& a, const csscan_options_t& o, const Plan& pl, uint32_t* hdr, uint32_t* flags,
-                     char* rest, cudaStream_t st) {
+                     char* rest, cudaStream_t st, float2* ckpt = nullptr, int64_t S8 = 0) {
     TableParams tp = table_params(a, pl, rest, N);
     using TL = NTile<N, NS>;
     tp.ng = TL::NG;
@@ -256,6 +259,8 @@ struct NScan {
       return CSSCAN_ERR_CUDA;
     }
     fill_common(sp, a, pl, hdr, flags, rest, o);
+    sp.ckpt = reinterpret_cast<float4*>(ckpt);
+    sp.S8 = int(S8);
     const int64_t table_threads = a.B * pl.S * N;
     if (!grid_fits(table_threads)) return CSSCAN_ERR_UNSUPPORTED;
     ntable_kernel<Tin, MODE><<<unsigned((table_threads + 255) / 256), 256, 0, st>>>(tp);
@@ -263,11 +268,11 @@ struct NScan {
     if (o.scan_begin) CSSCAN_CUDA(cudaEventRecord(o.scan_begin, st));
     const dim3 grid{unsigned(pl.n_units)}, block{unsigned(THREADS)};
     if (pl.carry == CARRY_NONE)
-      nscan_kernel<N, NS, Tin, MODE, CARRY_NONE><<<grid, block, unsigned(pl.smem), st>>>(sp);
+      nscan_kernel<N, NS, Tin, MODE, CARRY_NONE, CKPT><<<grid, block, unsigned(pl.smem), st>>>(sp);
     else if (pl.carry == CARRY_SERIAL)
-      nscan_kernel<N, NS, Tin, MODE, CARRY_SERIAL><<<grid, block, unsigned(pl.smem), st>>>(sp);
+      nscan_kernel<N, NS, Tin, MODE, CARRY_SERIAL, CKPT><<<grid, block, unsigned(pl.smem), st>>>(sp);
     else
-      nscan_kernel<N, NS, Tin, MODE, CARRY_DECOUPLED><<<grid, block, unsigned(pl.smem), st>>>(sp);
+      nscan_kernel<N, NS, Tin, MODE, CARRY_DECOUPLED, CKPT><<<grid, block, unsigned(pl.smem), st>>>(sp);
     CSSCAN_CUDA(cudaGetLastError());
     if (o.scan_end) CSSCAN_CUDA(cudaEventRecord(o.scan_end, st));
     return CSSCAN_OK;

@@ -170,7 +170,11 @@ __global__ void __launch_bounds__(256) ntable_kernel(TableParams p) {
 // which the decoupled variant needs to hold its look-back state without spilling.
 constexpr int NSCAN_MIN_BLOCKS = 2;
 
-template <int N, int NS, typename Tin, int MODE, int CARRY>
+// CKPT: the checkpoint variant the backward pass launches: no y; instead, before every 8-step
+// segment s >= 1, the state after step 8 s - 1 in the rotating frame of the 32-step sub-chunk
+// that holds step 8 s (the look-ahead state k in the trapezoid mode; the true state after the
+// frame reset when 8 s starts a sub-chunk) into p.ckpt, (B, S8, D, N) complex.
+template <int N, int NS, typename Tin, int MODE, int CARRY, bool CKPT = false>
 __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const __grid_constant__ ScanParams p) {
   using TL = NTile<N, NS>;
   using SG = NStage<N, NS, Tin, MODE>;
@@ -316,7 +320,9 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
   // the state update never waits for the MUFU; the stage holds row 32 of x, aux and dt (and 33 of
   // dt), i.e. the next sub-chunk's first step, so the pipeline runs on across sub-chunks.
   auto run_pass = [&](auto with_y_tag) {
-    constexpr bool WITH_Y = decltype(with_y_tag)::value;
+    constexpr bool WITH_Y = decltype(with_y_tag)::value;   // the final pass (from the true carry-in)
+    constexpr bool OUT = WITH_Y && !CKPT;                  // ... writing y
+    constexpr bool CK = WITH_Y && CKPT;                    // ... writing checkpoints
     Scal cur;
     float2 ec[NPAIR];
     for (int i = 0; i < n_sub; ++i, ++gstage) {
@@ -385,19 +391,19 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
           const float4 bb = row[q * NG];
           sr[q] = fma2(ec[q], sr[q], f2(bb.x, bb.y));
           si[q] = fma2(ec[q], si[q], f2(bb.z, bb.w));
-          if (WITH_Y) {
+          if (OUT) {
             const float4 cc = row[W4 + q * NG];
             float2& acc = (q & 1) ? acc1 : acc0;
             acc = fma2(f2(cc.z, cc.w), si[q], fma2(f2(cc.x, cc.y), sr[q], acc));
           }
         }
-        if (WITH_Y) {
+        if (OUT) {
           float ys = (acc0.x + acc0.y) + (acc1.x + acc1.y);
 #pragma unroll
           for (int o = 1; o < NG; o <<= 1) ys += __shfl_xor_sync(0xffffffffu, ys, o);
           const float yv = fmaf(cur.sig, ys, fmaf(-cur.pc, cur.E, Dsk * cur.x));
           if (g == 0 && dvalid) __stcs(yrow + tt * D, yv);
-        } else {
+        } else if (!WITH_Y) {
           sdt_acc += cur.dt;
         }
         aw_last = cur.sig;
@@ -406,10 +412,19 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
         for (int q = 0; q < NPAIR; ++q) ec[q] = en[q];
       };
 
+      // the true state (sigma of the last step times s) before segment s8, as (re, im) per state
+      auto store_ckpt = [&](int s8) {
+        if (!dvalid) return;
+        float4* r4 = p.ckpt + ((int64_t(b) * p.S8 + s8) * D + d) * (N / 2) + n0 / 2;
+#pragma unroll
+        for (int q = 0; q < NPAIR; ++q)
+          __stcg(r4 + q, make_float4(aw_last * sr[q].x, aw_last * si[q].x, aw_last * sr[q].y, aw_last * si[q].y));
+      };
       int tt = 0;
       for (; tt + 8 <= nt; tt += 8) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) step(tt + u);
+        if (CK && tt + 8 < T_SUB && t_sub0 + tt + 8 < p.L) store_ckpt((t_sub0 + tt + 8) / 8);
       }
       for (; tt < nt; ++tt) step(tt);
 
@@ -429,6 +444,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
           Ri[q] = i2;
         }
       }
+      if (CK && nt == T_SUB && t_sub0 + T_SUB < p.L) store_ckpt((t_sub0 + T_SUB) / 8);
       // release the stage: the last warp to finish with it refills the slot with stage
       // gstage + NST, so the warps of a block never wait for one another between stages
       // (every value the warp loaded from the stage has been consumed by arithmetic above, so
