@@ -144,7 +144,7 @@ int launch_backward_rot(const BwdArgs& a, cudaStream_t st) {
 
   // gradient blocks: (channel tile, b, time chunk); time chunks of whole 32-step sub-chunks, as
   // many as make the blocks fill the resident slots in nearly whole waves (more than one chunk
-  // costs the chunk-adjoint passes, about 0.15 of a wave)
+  // costs the chunk-carry passes, about 0.05 of a wave)
   int occ = 0;
   rc = occupancy_of(ngrad::ngrad_kernel<Tin, MODE, N>, dev, GS::SMEM, &occ);
   if (rc != CSSCAN_OK) return rc;
@@ -159,7 +159,7 @@ int launch_backward_rot(const BwdArgs& a, cudaStream_t st) {
   {
     double best = 1e30;
     for (int64_t cc = 1; cc <= std::min<int64_t>(S32, 256); ++cc) {
-      const double t = double((tiles * cc + slots - 1) / slots) / double(cc) + (cc > 1 ? 0.15 : 0.0);
+      const double t = double((tiles * cc + slots - 1) / slots) / double(cc) + (cc > 1 ? 0.05 : 0.0);
       if (t < best - 1e-9) {
         best = t;
         C = cc;
@@ -170,13 +170,15 @@ int launch_backward_rot(const BwdArgs& a, cudaStream_t st) {
   C = (a.L + TC - 1) / TC;
   if (C > 65535 || n_dtiles > 0x7fffffff) return CSSCAN_ERR_UNSUPPORTED;
 
-  // workspace: the forward plan's region (tables, carries), checkpoints, and with chunks
-  // e^{i theta}, the chunk records and the chunk-start terms of ddt; G(E) sums (trapezoid)
+  // workspace: the forward plan's region (tables, carries), checkpoints, and with chunks the
+  // chunk carries (V, sum dt, phase, kappa) and the chunk-start terms of ddt; G(E) sums (trapezoid)
   size_t off = align_up(fpl.rest_bytes, 256);
   auto take = [&](size_t bytes) { const size_t r = off; off = align_up(off + bytes, 256); return r; };
   const size_t o_ckpt = take(size_t(a.B * S8 * a.D * N) * sizeof(float2));
-  const size_t o_erot = C > 1 ? take(size_t(a.B * a.L * N) * sizeof(float2)) : 0;
-  const size_t o_chunk = C > 1 ? take(size_t(a.B * C * a.D * N) * 5 * sizeof(float2)) : 0;
+  const size_t o_V = C > 1 ? take(size_t(a.B * C * a.D * N) * sizeof(float2)) : 0;
+  const size_t o_kap = C > 1 ? take(size_t(a.B * C * a.D * N) * sizeof(float2)) : 0;
+  const size_t o_sdt = C > 1 ? take(size_t(a.B * C * a.D) * 4) : 0;
+  const size_t o_ph = C > 1 ? take(size_t(a.B * C * N) * sizeof(float2)) : 0;
   const size_t o_xb = C > 1 && MODE == 1 ? take(size_t(a.B * C * a.D) * 4) : 0;
   const size_t o_ge = MODE == 1 ? take(size_t(a.B * a.L) * 4) : 0;
   WsEntry ws;
@@ -202,34 +204,34 @@ int launch_backward_rot(const BwdArgs& a, cudaStream_t st) {
   rc = KF::enqueue(fa, fo, fpl, hdr, reinterpret_cast<uint32_t*>(base + HDR_BYTES), rest, st, ckpt, S8);
   if (rc != CSSCAN_OK) return rc;
 
-  // ---- chunk adjoints: the true adjoint at every chunk's first step
+  // ---- chunk carries: kappa_c entering every chunk's last step
   if (C > 1) {
-    bwd::Params cp;
-    std::memset(&cp, 0, sizeof(cp));
-    cp.dt = a.delta;
-    cp.Cc = a.Cc;
-    cp.A = a.A;
-    cp.dy = a.dy;
-    cp.rot = reinterpret_cast<const float2*>(rest + o_erot);
-    cp.chunk = reinterpret_cast<float2*>(rest + o_chunk);
-    cp.B = int(a.B);
-    cp.L = int(a.L);
-    cp.D = int(a.D);
-    cp.N = N;
-    cp.S = int(S8);
-    cp.TC = int(TC);
-    cp.C = int(C);
-    cp.fwd_ckpt = 1;   // entry states are not needed: the checkpoints hold them
-    const long long n_rot = (long long)a.B * a.L * N;
-    if (!grid_fits(n_rot)) return CSSCAN_ERR_UNSUPPORTED;
-    bwd::rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest + o_erot),
-                                                                      n_rot);
+    ngrad::AdjParams ap;
+    ap.tab = reinterpret_cast<const float4*>(rest + fpl.o_tab);
+    ap.rot = reinterpret_cast<const float2*>(rest + fpl.o_rot);
+    ap.dy = a.dy;
+    ap.dt = a.delta;
+    ap.A = a.A;
+    ap.V = reinterpret_cast<float2*>(rest + o_V);
+    ap.Sdt = reinterpret_cast<float*>(rest + o_sdt);
+    ap.P = reinterpret_cast<float2*>(rest + o_ph);
+    ap.kap = reinterpret_cast<float2*>(rest + o_kap);
+    ap.B = int(a.B);
+    ap.L = int(a.L);
+    ap.D = int(a.D);
+    ap.S32 = int(S32);
+    ap.TC = int(TC);
+    ap.C = int(C);
+    ap.tab_ng = NTile<N, NSF>::NG;
+    constexpr int NGA = N >= 16 ? N / 16 : 1;
+    const dim3 agrid{unsigned((a.D * NGA + 127) / 128), unsigned(C - 1), unsigned(a.B)};
+    ngrad::nadj_kernel<Tin, N><<<agrid, 128, 0, st>>>(ap);
     CSSCAN_CUDA(cudaGetLastError());
-    const dim3 agrid{unsigned((a.D + 256 / N - 1) / (256 / N)), unsigned(C), unsigned(a.B)};
-    bwd::chunk_adj_kernel<Tin, MODE, N><<<agrid, 256, 0, st>>>(cp);
+    const long long n_ph = (long long)a.B * C * N, n_cb = (long long)a.B * a.D * N;
+    if (!grid_fits(n_ph) || !grid_fits(n_cb)) return CSSCAN_ERR_UNSUPPORTED;
+    ngrad::nphase_kernel<<<unsigned((n_ph + 255) / 256), 256, 0, st>>>(ap, N);
     CSSCAN_CUDA(cudaGetLastError());
-    const long long n_cb = (long long)a.B * a.D * N;
-    bwd::chunk_combine_kernel<<<unsigned((n_cb + 255) / 256), 256, 0, st>>>(cp);
+    ngrad::ncombine_kernel<<<unsigned((n_cb + 255) / 256), 256, 0, st>>>(ap, N);
     CSSCAN_CUDA(cudaGetLastError());
   }
 
@@ -257,9 +259,7 @@ int launch_backward_rot(const BwdArgs& a, cudaStream_t st) {
   gp.A = a.A;
   gp.Dskip = a.Dskip;
   gp.ckpt = reinterpret_cast<const float4*>(ckpt);
-  gp.chunk = C > 1 ? reinterpret_cast<const float2*>(rest + o_chunk) : nullptr;
-  gp.erot = C > 1 ? reinterpret_cast<const float2*>(rest + o_erot) : nullptr;
-  gp.dt = a.delta;
+  gp.kap = C > 1 ? reinterpret_cast<const float2*>(rest + o_kap) : nullptr;
   gp.dx = a.dx;
   gp.ddt = a.ddelta;
   gp.dA = a.dA;

@@ -60,14 +60,16 @@ struct GTile {
   static constexpr int SLOTS = WARPS * M;             // threads sharing a state pair
   static constexpr int NGR = NG > 8 ? 8 : NG;         // lanes per channel summed in shared memory
   static constexpr int ROWS = THREADS / BC;           // threads per channel in the per-(t, d) phase
+  static constexpr int MIN_BLOCKS = 4;                // resident blocks per SM the kernel is compiled for
 };
 
 // One stage: x rows ts .. ts+7, dt rows ts .. ts+8, dy rows ts .. ts+7 of the block's channels,
 // the trapezoid rows (lam_t, 1 - lam_{t+1}, E_t, 0), the two table planes (Bt, Ct) of rows ts ..
-// ts+7 and e^{i Phi} after the last step of the sub-chunk holding ts. Then the scratch region
-// shared by the per-(t, d) partials [SEG][BC][TDW] float2 and the per-(t, n) partials of half a
-// segment [SEG / 2][5][NG][SROW] floats (rows padded so that neither the writes nor the row sums
-// meet bank conflicts).
+// ts+7 and e^{i Phi} after the last step of the sub-chunk holding ts. Rows past the sequence's end
+// arrive as zeros. Then the scratch region: the segment's (dt, w) per (t, channel) [SEG][BC]
+// float2, and the per-(t, d) partials of half a segment [SEG / 2][BC][TDW] float2, which the
+// per-(t, n) partials of the half [SEG / 2][5][NG][SROW] floats overwrite once consumed (rows
+// padded so that neither the writes nor the row sums meet bank conflicts).
 template <int N, typename Tin, int MODE>
 struct GStage {
   using GT = GTile<N>;
@@ -88,9 +90,10 @@ struct GStage {
   static constexpr int TX_BYTES = X_BYTES + DT_BYTES + DY_BYTES + AUX_BYTES + TAB_BYTES + ROT_BYTES;
   static constexpr int SROW = 2 * GT::SLOTS + 8;      // floats per (t, kind, pair) row
   static constexpr int TDW = GT::NGR + 2;             // float2 per (t, channel) row
-  static constexpr int TD_BYTES = SEG * GT::BC * TDW * 8;
+  static constexpr int PRE_BYTES = SEG * GT::BC * 8;  // (dt, w) per (t, channel)
+  static constexpr int TD_BYTES = (SEG / 2) * GT::BC * TDW * 8;
   static constexpr int TN_BYTES = (SEG / 2) * 5 * GT::NG * SROW * 4;
-  static constexpr int SCR_BYTES = TD_BYTES > TN_BYTES ? TD_BYTES : TN_BYTES;
+  static constexpr int SCR_BYTES = PRE_BYTES + (TD_BYTES > TN_BYTES ? TD_BYTES : TN_BYTES);
   static constexpr int SMEM = 2 * BYTES + SCR_BYTES + 128;
 };
 
@@ -104,9 +107,7 @@ struct GradParams {
   const float* A;       // (D, N)
   const float* Dskip;   // (D)
   const float4* ckpt;   // (B, S8, D, N/2) state pairs (re, im, re', im') before segment s >= 1
-  const float2* chunk;  // (B, C, D, N, 5) chunk records; [2]: the true adjoint at the chunk's first step
-  const float2* erot;   // (B, L, N) e^{i theta}                                    (C > 1)
-  const void* dt;       // (B, L, D) input dtype, for a_t at the chunks' ends          (C > 1)
+  const float2* kap;    // (B, C, D, N) the true-frame adjoint carry entering chunk c's last step (C > 1)
   float* dx;            // (B, L, D) written
   float* ddt;           // (B, L, D) written (chunk starts completed by ngrad_fix_kernel)
   float* dA;            // (D, N) accumulated
@@ -123,7 +124,7 @@ struct GradParams {
 };
 
 template <typename Tin, int MODE, int N>
-__global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant__ GradParams p) {
+__global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(const __grid_constant__ GradParams p) {
   using GT = GTile<N>;
   using SG = GStage<N, Tin, MODE>;
   constexpr int NG = GT::NG, M = GT::M, K = GT::K, BC = GT::BC, NGR = GT::NGR, ROWS = GT::ROWS;
@@ -131,11 +132,14 @@ __global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
-  float* scr = reinterpret_cast<float*>(smem + 2 * SG::BYTES);
+  float2* pre = reinterpret_cast<float2*>(smem + 2 * SG::BYTES);                  // (dt, w) per (t, channel)
+  float* scr = reinterpret_cast<float*>(smem + 2 * SG::BYTES + SG::PRE_BYTES);   // per-(t, n) partials
+  float2* tdp = reinterpret_cast<float2*>(scr);                                  // per-(t, d) partials
   __shared__ __align__(8) uint64_t bar[2];
   __shared__ float4 s_carry[K][THREADS];   // per (channel, thread): the adjoint carry rho (re pair, im pair)
   __shared__ float2 s_dA[K][THREADS];      // per (channel, thread): dA of the pair
   __shared__ float s_pend[2][BC];          // ddt at a segment's first step without the previous step's term
+  __shared__ float s_hpend[BC];            // the same at the segment's middle step
   __shared__ float s_lam[SEG + 1];         // per step of the segment (and the next segment's first)
   __shared__ float s_ge[SEG];
 
@@ -174,32 +178,21 @@ __global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant
     issue(s_last, 0);
   }
 
-  // ---- per (channel, thread): the absolute carry conj(a_te) ghat_te entering the chunk's last
-  // step from the next chunk (zero at the sequence's end), and the dA sums
+  // ---- per (channel, thread): the true-frame carry entering the chunk's last step from the next
+  // chunk (zero at the sequence's end), and the dA sums
 #pragma unroll 1
   for (int k = 0; k < K; ++k) {
     const int d = d0 + (k * WARPS + w) * M + c;
     float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (chunk + 1 < p.C && d < p.D) {
-      const Tin* DTp = static_cast<const Tin*>(p.dt);
-      const float dtn = load_in<Tin>(DTp, (int64_t(b) * L + te) * D + d);
-      float cr[2], ci[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int n = 2 * g + u;
-        const float2 gh = p.chunk[((((int64_t(b) * p.C + chunk + 1) * D + d) * N) + n) * 5 + 2];
-        const float2 ro = p.erot[(int64_t(b) * L + te) * N + n];
-        const float r = ex2_approx(dtn * p.A[int64_t(d) * N + n] * LOG2E_F);
-        const float ar = r * ro.x, ai = r * ro.y;
-        cr[u] = ar * gh.x + ai * gh.y;
-        ci[u] = ar * gh.y - ai * gh.x;
-      }
-      cv = make_float4(cr[0], cr[1], ci[0], ci[1]);
+      const float4 v = reinterpret_cast<const float4*>(p.kap + ((int64_t(b) * p.C + chunk) * D + d) * N)[g];
+      cv = make_float4(v.x, v.z, v.y, v.w);
     }
     s_carry[k][tid] = cv;
     s_dA[k][tid] = f2(0.f, 0.f);
   }
   for (int i = tid; i < 2 * BC; i += THREADS) (&s_pend[0][0])[i] = 0.f;
+  for (int i = tid; i < BC; i += THREADS) s_hpend[i] = 0.f;
   if (tid <= SEG) s_lam[tid] = 0.f;
   if (tid < SEG) s_ge[tid] = 0.f;
 
@@ -209,12 +202,6 @@ __global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant
   const bool validA = dA_ < p.D;
   const float DsA = validA ? p.Dskip[dA_] : 0.f;
   float dD_acc = 0.f;
-
-  float2 aT[SEG], aBr[SEG], aBi[SEG], aCr[SEG], aCi[SEG];   // per-(t, n) sums over this thread's channels
-#pragma unroll
-  for (int i = 0; i < SEG; ++i) {
-    aT[i] = aBr[i] = aBi[i] = aCr[i] = aCi[i] = f2(0.f, 0.f);
-  }
   __syncthreads();
 
   bool aborted = false;
@@ -238,67 +225,93 @@ __global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant
     const float4 rot = reinterpret_cast<const float4*>(base + SG::OFF_ROT)[g];   // (c, s) of states 2g, 2g+1
     const int ts = s * SEG;
     const int nt = min(SEG, p.L - ts);
-    // the carry arrives from the next sub-chunk's frame (or the next chunk at a sub-chunk boundary)
-    const bool frame_in = ((ts + SEG) % T_SUB) == 0;
+    // (dt, w) once per (t, channel) for every lane of the channel
+    for (int e = tid; e < SEG * BC; e += THREADS) {
+      const float x = smem_in<Tin>(sX, e), dt = smem_in<Tin>(sDT, e);
+      float wt;
+      if constexpr (MODE == 1) {
+        const float4 ax = sAUX[e / BC];
+        wt = x * fmaf(ax.x, dt, ax.y * smem_in<Tin>(sDT, e + BC));
+      } else {
+        wt = x * dt;
+      }
+      pre[e] = f2(dt, wt);
+    }
+    __syncthreads();
 
+    // Two halves, the later steps first: the per-(t, n) sums of a half live in registers only
+    // while its four steps are worked, and its per-(t, d) partials share one scratch region with
+    // them. Each half regenerates g from the segment's checkpoint (the later half through all
+    // eight steps, keeping the last five states; the earlier half through its four).
+#pragma unroll
+    for (int half = 1; half >= 0; --half) {
+      constexpr int H = SEG / 2;
+      const int i0 = half * H;
+      float2 aT[H], aBr[H], aBi[H], aCr[H], aCi[H];   // per-(t, n) sums over this thread's channels
+#pragma unroll
+      for (int ii = 0; ii < H; ++ii) aT[ii] = aBr[ii] = aBi[ii] = aCr[ii] = aCi[ii] = f2(0.f, 0.f);
+
+      auto ckpt_of = [&](int k) {
+        const int d = d0 + (k * WARPS + w) * M + c;
+        return (s > 0 && d < p.D) ? __ldcg(p.ckpt + ((int64_t(b) * p.S8 + s) * D + d) * (N / 2) + g)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      };
+      float4 ck_next = ckpt_of(0);
 #pragma unroll 1
-    for (int k = 0; k < K; ++k) {
-      const int cb = (k * WARPS + w) * M + c;
-      const int d = d0 + cb;
-      const bool valid = d < p.D;
-      const int64_t dd = valid ? d : 0;
-      const float2 A2 = valid ? f2(p.A[dd * N + 2 * g], p.A[dd * N + 2 * g + 1]) : f2(0.f, 0.f);
-      const float2 a2 = mul2(A2, f2(LOG2E_F, LOG2E_F));
-      float4 cv = s_carry[k][tid];
-      float2 cr = f2(cv.x, cv.y), ci = f2(cv.z, cv.w);
-      if (frame_in) {   // into this frame: multiply by e^{-i Phi_last}
-        const float2 cc = f2(rot.x, rot.z), ss = f2(rot.y, rot.w);
-        const float2 nr = fma2(cc, cr, mul2(ss, ci));
-        const float2 ni = fma2(cc, ci, mul2(f2(-ss.x, -ss.y), cr));
-        cr = nr;
-        ci = ni;
-      }
-      // ---- regenerate g over the segment from its checkpoint
-      float2 hr[SEG + 1], hi[SEG + 1];
-      hr[0] = hi[0] = f2(0.f, 0.f);
-      if (s > 0 && valid) {
-        const float4 v = __ldcg(p.ckpt + ((int64_t(b) * p.S8 + s) * D + d) * (N / 2) + g);
-        hr[0] = f2(v.x, v.z);
-        hi[0] = f2(v.y, v.w);
-      }
-      float wv[SEG];
-#pragma unroll
-      for (int i = 0; i < SEG; ++i) {
-        wv[i] = 0.f;
-        hr[i + 1] = hr[i];
-        hi[i + 1] = hi[i];
-        if (i < nt) {
-          const float x = smem_in<Tin>(sX, i * BC + cb);
-          const float dt = smem_in<Tin>(sDT, i * BC + cb);
-          float wt;
-          if constexpr (MODE == 1) {
-            const float4 ax = sAUX[i];
-            wt = x * fmaf(ax.x, dt, ax.y * smem_in<Tin>(sDT, (i + 1) * BC + cb));
-          } else {
-            wt = x * dt;
-          }
-          wv[i] = wt;
-          const float2 r2 = ex2_pair(mul2(f2(dt, dt), a2));
-          const float4 bt = sTAB[(i * 2) * (N / 2) + pos];
-          const float2 w2 = f2(wt, wt);
-          hr[i + 1] = fma2(r2, hr[i], mul2(w2, f2(bt.x, bt.y)));
-          hi[i + 1] = fma2(r2, hi[i], mul2(w2, f2(bt.z, bt.w)));
+      for (int k = 0; k < K; ++k) {
+        const float4 ck = ck_next;
+        if (k + 1 < K) ck_next = ckpt_of(k + 1);   // in flight while this channel is worked
+        const int cb = (k * WARPS + w) * M + c;
+        const int d = d0 + cb;
+        const bool valid = d < p.D;
+        const int64_t dd = valid ? d : 0;
+        const float2 A2 = valid ? f2(p.A[dd * N + 2 * g], p.A[dd * N + 2 * g + 1]) : f2(0.f, 0.f);
+        const float2 a2 = mul2(A2, f2(LOG2E_F, LOG2E_F));
+        float4 cv = s_carry[k][tid];
+        float2 cr = f2(cv.x, cv.y), ci = f2(cv.z, cv.w);
+        // the carry arrives from the next sub-chunk's frame (or the next chunk at a sub-chunk
+        // boundary): into this frame by e^{-i Phi_last}
+        if (half == 1 && ((ts + SEG) % T_SUB) == 0) {
+          const float2 cc = f2(rot.x, rot.z), ss = f2(rot.y, rot.w);
+          const float2 nr = fma2(cc, cr, mul2(ss, ci));
+          const float2 ni = fma2(cc, ci, mul2(f2(-ss.x, -ss.y), cr));
+          cr = nr;
+          ci = ni;
         }
-      }
-      // ---- backwards through the segment
-      float2 dA2 = s_dA[k][tid];
+        // ---- regenerate g (steps past the sequence's end have dt = 0 and a zero table row:
+        // they leave g unchanged, and the adjoint below stays zero there)
+        float2 gr0 = f2(ck.x, ck.z), gi0 = f2(ck.y, ck.w);
 #pragma unroll
-      for (int i = SEG - 1; i >= 0; --i) {
-        float2 pq = f2(0.f, 0.f);   // (Gw, sum A Re G(z)) partials of this pair
-        if (i < nt) {
+        for (int i = 0; i < i0; ++i) {
+          const float2 pv = pre[i * BC + cb];
+          const float2 r2 = ex2_pair(mul2(f2(pv.x, pv.x), a2));
+          const float4 bt = sTAB[(i * 2) * (N / 2) + pos];
+          const float2 w2 = f2(pv.y, pv.y);
+          gr0 = fma2(r2, gr0, mul2(w2, f2(bt.x, bt.y)));
+          gi0 = fma2(r2, gi0, mul2(w2, f2(bt.z, bt.w)));
+        }
+        float2 hr[H + 1], hi[H + 1], r2s[H];   // g_{i0-1} .. g_{i0+3}; decays of the half's steps
+        hr[0] = gr0;
+        hi[0] = gi0;
+#pragma unroll
+        for (int ii = 0; ii < H; ++ii) {
+          const int i = i0 + ii;
+          const float2 pv = pre[i * BC + cb];
+          const float2 r2 = ex2_pair(mul2(f2(pv.x, pv.x), a2));
+          r2s[ii] = r2;
+          const float4 bt = sTAB[(i * 2) * (N / 2) + pos];
+          const float2 w2 = f2(pv.y, pv.y);
+          hr[ii + 1] = fma2(r2, hr[ii], mul2(w2, f2(bt.x, bt.y)));
+          hi[ii + 1] = fma2(r2, hi[ii], mul2(w2, f2(bt.z, bt.w)));
+        }
+        // ---- backwards through the half
+        float2 dA2 = s_dA[k][tid];
+#pragma unroll
+        for (int ii = H - 1; ii >= 0; --ii) {
+          const int i = i0 + ii;
+          const float2 pv = pre[i * BC + cb];   // dt, w
           const float dy = sDY[i * BC + cb];
-          const float dt = smem_in<Tin>(sDT, i * BC + cb);
-          const float2 r2 = ex2_pair(mul2(f2(dt, dt), a2));
+          const float2 r2 = r2s[ii];
           const float4 bt = sTAB[(i * 2) * (N / 2) + pos];
           const float4 ct = sTAB[(i * 2 + 1) * (N / 2) + pos];   // (Re, Re', -Im, -Im')
           const float2 dy2 = f2(dy, dy);
@@ -306,141 +319,128 @@ __global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant
           const float2 gi = fma2(dy2, f2(ct.z, ct.w), ci);
           const float2 P2 = fma2(f2(bt.x, bt.y), gr, mul2(f2(bt.z, bt.w), gi));   // Re(conj(Bt) gamma)
           const float2 rr = mul2(r2, gr), ri = mul2(r2, gi);                      // rho = r gamma
-          const float2 zr = fma2(rr, hr[i], mul2(ri, hi[i]));                     // Re G(z) = Re(rho conj(g_{t-1}))
-          const float2 zi = fma2(ri, hr[i], mul2(f2(-rr.x, -rr.y), hi[i]));        // Im G(z)
+          const float2 zr = fma2(rr, hr[ii], mul2(ri, hi[ii]));                   // Re G(z) = Re(rho conj(g_{t-1}))
+          const float2 zi = fma2(ri, hr[ii], mul2(f2(-rr.x, -rr.y), hi[ii]));      // Im G(z)
           const float2 Q2 = mul2(A2, zr);
-          dA2 = fma2(f2(dt, dt), zr, dA2);
-          aT[i] = add2(aT[i], zi);
-          const float2 w2 = f2(wv[i], wv[i]);
-          aBr[i] = fma2(w2, gr, aBr[i]);
-          aBi[i] = fma2(w2, gi, aBi[i]);
-          aCr[i] = fma2(dy2, hr[i + 1], aCr[i]);
-          aCi[i] = fma2(f2(-dy, -dy), hi[i + 1], aCi[i]);
-          pq = f2(P2.x + P2.y, Q2.x + Q2.y);
+          dA2 = fma2(f2(pv.x, pv.x), zr, dA2);
+          aT[ii] = add2(aT[ii], zi);
+          const float2 w2 = f2(pv.y, pv.y);
+          aBr[ii] = fma2(w2, gr, aBr[ii]);
+          aBi[ii] = fma2(w2, gi, aBi[ii]);
+          aCr[ii] = fma2(dy2, hr[ii + 1], aCr[ii]);
+          aCi[ii] = fma2(f2(-dy, -dy), hi[ii + 1], aCi[ii]);
+          float2 pq = f2(P2.x + P2.y, Q2.x + Q2.y);   // (Gw, sum A Re G(z)) partials of this pair
           cr = rr;
           ci = ri;
-        }
-        if constexpr (NG > NGR) {   // N = 32: fold the upper half of the channel's lanes first
-          pq.x += __shfl_xor_sync(0xffffffffu, pq.x, NGR * M);
-          pq.y += __shfl_xor_sync(0xffffffffu, pq.y, NGR * M);
-        }
-        if (g < NGR) reinterpret_cast<float2*>(scr)[(i * BC + cb) * TDW + g] = pq;
-      }
-      s_carry[k][tid] = make_float4(cr.x, cr.y, ci.x, ci.y);
-      s_dA[k][tid] = dA2;
-    }
-    __syncthreads();
-
-    // ---- per (t, d): dx, ddt, dlam, G(E), dDskip
-    {
-      const float2* td = reinterpret_cast<const float2*>(scr);
-      auto sums = [&](int i) {   // (Gw, sum A Re G(z)) of (step i, channel cbA)
-        if constexpr (NGR == 1) {
-          return td[(i * BC + cbA) * TDW];
-        } else {
-          const float4* r4 = reinterpret_cast<const float4*>(td + (i * BC + cbA) * TDW);
-          float4 v = r4[0];
-#pragma unroll
-          for (int u = 1; u < NGR / 2; ++u) {
-            const float4 a = r4[u];
-            v.x += a.x;
-            v.y += a.y;
-            v.z += a.z;
-            v.w += a.w;
+          if constexpr (NG > NGR) {   // N = 32: fold the upper half of the channel's lanes first
+            pq.x += __shfl_xor_sync(0xffffffffu, pq.x, NGR * M);
+            pq.y += __shfl_xor_sync(0xffffffffu, pq.y, NGR * M);
           }
-          return f2(v.x + v.z, v.y + v.w);
+          if (g < NGR) tdp[(ii * BC + cb) * TDW + g] = pq;
         }
-      };
-#pragma unroll
-      for (int i0 = 0; i0 < SEG; i0 += ROWS) {
-        const int i = i0 + rA;
-        float lam_i = 0.f, ge_i = 0.f, lam_next = 0.f;
-        if (i < nt && validA) {
-          const float2 gq = sums(i);
-          const float x = smem_in<Tin>(sX, i * BC + cbA);
-          const float dt = smem_in<Tin>(sDT, i * BC + cbA);
-          const float dy = sDY[i * BC + cbA];
-          const int64_t row = (int64_t(b) * L + ts + i) * D + dA_;
-          dD_acc = fmaf(dy, x, dD_acc);
-          if constexpr (MODE == 0) {
-            p.dx[row] = fmaf(dt, gq.x, DsA * dy);
-            p.ddt[row] = fmaf(x, gq.x, gq.y);
+        s_carry[k][tid] = make_float4(cr.x, cr.y, ci.x, ci.y);
+        s_dA[k][tid] = dA2;
+      }
+      __syncthreads();
+
+      // ---- per (t, d) of the half: dx, ddt, dlam, G(E), dDskip
+      {
+        auto sums = [&](int ii) {   // (Gw, sum A Re G(z)) of (half step ii, channel cbA)
+          if constexpr (NGR == 1) {
+            return tdp[(ii * BC + cbA) * TDW];
           } else {
-            const float4 ax = sAUX[i];   // lam_t, mu_t, E_t
-            const float dtn = smem_in<Tin>(sDT, (i + 1) * BC + cbA);
-            const float m = ax.y * dtn;
-            p.dx[row] = fmaf(fmaf(ax.x, dt, m), gq.x, fmaf(-dy * m, ax.z, DsA * dy));
-            const float own = fmaf(x * ax.x, gq.x, gq.y);
-            lam_i = x * dt * gq.x;
-            ge_i = -dy * x * m;
-            if (i > 0) {   // the previous step's terms of ddt_t and dlam_t
-              const float2 gp = sums(i - 1);
-              const float xp = smem_in<Tin>(sX, (i - 1) * BC + cbA);
-              const float4 ap = sAUX[i - 1];
-              const float dyp = sDY[(i - 1) * BC + cbA];
-              const float gwe = fmaf(-dyp, ap.z, gp.x);
-              p.ddt[row] = fmaf(xp * ap.y, gwe, own);
-              lam_i = fmaf(-xp * dt, gwe, lam_i);
-            } else {
-              s_pend[s & 1][cbA] = own;
+            const float4* r4 = reinterpret_cast<const float4*>(tdp + (ii * BC + cbA) * TDW);
+            float4 v = r4[0];
+#pragma unroll
+            for (int u = 1; u < NGR / 2; ++u) {
+              const float4 a = r4[u];
+              v.x += a.x;
+              v.y += a.y;
+              v.z += a.z;
+              v.w += a.w;
             }
-            if (i == SEG - 1 && ts + SEG < p.L) {   // this step's terms of ddt and dlam at ts + SEG
-              const float gwe = fmaf(-dy, ax.z, gq.x);
-              const float crs = x * ax.y * gwe;
-              lam_next = -x * dtn * gwe;
-              if (s < s_last) {
-                p.ddt[row + D] = s_pend[(s + 1) & 1][cbA] + crs;
+            return f2(v.x + v.z, v.y + v.w);
+          }
+        };
+#pragma unroll
+        for (int j0 = 0; j0 < H; j0 += ROWS) {
+          const int ii = j0 + rA;
+          const int i = i0 + ii;
+          float lam_i = 0.f, ge_i = 0.f, lam_next = 0.f;
+          if (i < nt && validA) {
+            const float2 gq = sums(ii);
+            const float x = smem_in<Tin>(sX, i * BC + cbA);
+            const float dt = pre[i * BC + cbA].x;
+            const float dy = sDY[i * BC + cbA];
+            const int64_t row = (int64_t(b) * L + ts + i) * D + dA_;
+            dD_acc = fmaf(dy, x, dD_acc);
+            if constexpr (MODE == 0) {
+              p.dx[row] = fmaf(dt, gq.x, DsA * dy);
+              p.ddt[row] = fmaf(x, gq.x, gq.y);
+            } else {
+              const float4 ax = sAUX[i];   // lam_t, mu_t, E_t
+              const float dtn = smem_in<Tin>(sDT, (i + 1) * BC + cbA);
+              const float m = ax.y * dtn;
+              p.dx[row] = fmaf(fmaf(ax.x, dt, m), gq.x, fmaf(-dy * m, ax.z, DsA * dy));
+              const float own = fmaf(x * ax.x, gq.x, gq.y);
+              lam_i = x * dt * gq.x;
+              ge_i = -dy * x * m;
+              if (ii > 0) {   // the previous step's terms of ddt_t and dlam_t
+                const float2 gp = sums(ii - 1);
+                const float xp = smem_in<Tin>(sX, (i - 1) * BC + cbA);
+                const float4 ap = sAUX[i - 1];
+                const float gwe = fmaf(-sDY[(i - 1) * BC + cbA], ap.z, gp.x);
+                p.ddt[row] = fmaf(xp * ap.y, gwe, own);
+                lam_i = fmaf(-xp * dt, gwe, lam_i);
+              } else if (half == 1) {
+                s_hpend[cbA] = own;          // completed by the earlier half's last step
               } else {
-                p.xb[(int64_t(b) * p.C + chunk + 1) * D + dA_] = crs;
+                s_pend[s & 1][cbA] = own;    // completed by the next segment's last step
+              }
+              if (ii == H - 1 && (half == 0 ? i + 1 < nt : ts + SEG < p.L)) {   // this step's terms at i + 1
+                const float gwe = fmaf(-dy, ax.z, gq.x);
+                const float crs = x * ax.y * gwe;
+                lam_next = -x * dtn * gwe;
+                if (half == 0) {
+                  p.ddt[row + D] = s_hpend[cbA] + crs;
+                } else if (s < s_last) {
+                  p.ddt[row + D] = s_pend[(s + 1) & 1][cbA] + crs;
+                } else {
+                  p.xb[(int64_t(b) * p.C + chunk + 1) * D + dA_] = crs;
+                }
               }
             }
           }
-        }
-        if constexpr (MODE == 1) {
-          // sums over the warp's channels (a warp's threads share the step), one shared add per warp
+          if constexpr (MODE == 1) {
+            // sums over the warp's channels (a warp's threads share the step), one shared add per warp
 #pragma unroll
-          for (int o = 16; o >= 1; o >>= 1) {
-            lam_i += __shfl_xor_sync(0xffffffffu, lam_i, o);
-            ge_i += __shfl_xor_sync(0xffffffffu, ge_i, o);
-            lam_next += __shfl_xor_sync(0xffffffffu, lam_next, o);
-          }
-          if (lane == 0) {
-            atomicAdd(&s_lam[i], lam_i);
-            atomicAdd(&s_ge[i], ge_i);
-            if (i == SEG - 1) atomicAdd(&s_lam[SEG], lam_next);
+            for (int o = 16; o >= 1; o >>= 1) {
+              lam_i += __shfl_xor_sync(0xffffffffu, lam_i, o);
+              ge_i += __shfl_xor_sync(0xffffffffu, ge_i, o);
+              lam_next += __shfl_xor_sync(0xffffffffu, lam_next, o);
+            }
+            if (lane == 0) {
+              atomicAdd(&s_lam[i], lam_i);
+              atomicAdd(&s_ge[i], ge_i);
+              if (ii == H - 1) atomicAdd(&s_lam[i + 1], lam_next);
+            }
           }
         }
       }
-    }
-    __syncthreads();
-    if constexpr (MODE == 1) {
-      if (tid <= SEG) {
-        const int t = ts + tid;
-        if (t < p.L && (tid < nt || tid == SEG)) atomicAdd(&p.dlam[int64_t(b) * L + t], s_lam[tid]);
-        s_lam[tid] = 0.f;
-      }
-      if (tid < SEG) {
-        if (tid < nt) atomicAdd(&p.ge[int64_t(b) * L + ts + tid], s_ge[tid]);
-        s_ge[tid] = 0.f;
-      }
-    }
+      __syncthreads();
 
-    // ---- per (t, n): sums over the block's channels of dtheta, dBc, dCc (rotated frame), half a
-    // segment at a time
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
+      // ---- per (t, n) of the half: sums over the block's channels of dtheta, dBc, dCc (rotated
+      // frame), written over the per-(t, d) partials
       {
         const int slot2 = w * M + c;
 #pragma unroll
-        for (int ii = 0; ii < SEG / 2; ++ii) {
-          const int i = h2 * (SEG / 2) + ii;
+        for (int ii = 0; ii < H; ++ii) {
           float2* row = reinterpret_cast<float2*>(scr + ((ii * 5) * NG + g) * SROW) + slot2;
-          row[0] = aT[i];
-          row[(NG * SROW) / 2] = aBr[i];
-          row[2 * ((NG * SROW) / 2)] = aBi[i];
-          row[3 * ((NG * SROW) / 2)] = aCr[i];
-          row[4 * ((NG * SROW) / 2)] = aCi[i];
-          aT[i] = aBr[i] = aBi[i] = aCr[i] = aCi[i] = f2(0.f, 0.f);
+          row[0] = aT[ii];
+          row[(NG * SROW) / 2] = aBr[ii];
+          row[2 * ((NG * SROW) / 2)] = aBi[ii];
+          row[3 * ((NG * SROW) / 2)] = aCr[ii];
+          row[4 * ((NG * SROW) / 2)] = aCi[ii];
         }
       }
       __syncthreads();
@@ -458,10 +458,10 @@ __global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant
           }
           return f2(v.x + v.z, v.y + v.w);   // (state 2gg, state 2gg + 1)
         };
-        const int nh = min(SEG / 2, nt - h2 * (SEG / 2));
+        const int nh = min(H, nt - i0);
         for (int o = tid; o < nh * 3 * NG; o += THREADS) {
           const int ii = o / (3 * NG), rem = o % (3 * NG), kind = rem / NG, gg = rem % NG;
-          const int64_t tn = (int64_t(b) * L + ts + h2 * (SEG / 2) + ii) * N + 2 * gg;
+          const int64_t tn = (int64_t(b) * L + ts + i0 + ii) * N + 2 * gg;
           if (kind == 0) {
             atomicAdd(reinterpret_cast<float2*>(p.dtheta + tn), rsum(ii, 0, gg));
           } else {
@@ -472,6 +472,19 @@ __global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant
         }
       }
       __syncthreads();
+    }
+
+    if constexpr (MODE == 1) {
+      if (tid <= SEG) {
+        const int t = ts + tid;
+        if (t < p.L && (tid < nt || tid == SEG)) atomicAdd(&p.dlam[int64_t(b) * L + t], s_lam[tid]);
+        s_lam[tid] = 0.f;
+      }
+      if (tid < SEG) {
+        if (tid < nt) atomicAdd(&p.ge[int64_t(b) * L + ts + tid], s_ge[tid]);
+        s_ge[tid] = 0.f;
+      }
+      // (the next segment's first use of s_lam / s_ge comes after at least two barriers)
     }
   }
 
@@ -492,6 +505,132 @@ __global__ void __launch_bounds__(THREADS, 3) ngrad_kernel(const __grid_constant
     const int d = d0 + (k * WARPS + w) * M + c;
     if (d < p.D) atomicAdd(reinterpret_cast<float2*>(p.dA + int64_t(d) * N + 2 * g), s_dA[k][tid]);
   }
+}
+
+// ---------------------------------------------------------------------------- chunk carries
+// Where the sequence is cut into C time chunks (whole 32-step sub-chunks), the gradient block of
+// chunk c needs the adjoint carry entering its last step from chunk c + 1. The adjoint recurrence
+// is affine per chunk: with kappa_c that (true-frame) carry,
+//   kappa_{c-1} = V_c + G_c kappa_c,   G_c = exp(A sum_{t in c} dt_t) e^{-i sum_{t in c} theta_t},
+// V_c being the carry out of chunk c's first step from a zero carry (the sub-chunk frames make the
+// decays real; crossing into an earlier sub-chunk multiplies by e^{-i Phi_last} of that sub-chunk).
+struct AdjParams {
+  const float4* tab;   // (B, L, 2, N/2) float4: the forward table (Bt and Ct planes)
+  const float2* rot;   // (B, S32, 4, N) e^{i Phi} rows; row 3: after the sub-chunk's last step
+  const float* dy;     // (B, L, D)
+  const void* dt;      // (B, L, D) input dtype
+  const float* A;      // (D, N)
+  float2* V;           // (B, C, D, N)
+  float* Sdt;          // (B, C, D)
+  float2* P;           // (B, C, N) e^{-i sum theta} per chunk
+  float2* kap;         // (B, C, D, N) kappa_c: the carry entering chunk c's last step
+  int B, L, D, S32, TC, C, tab_ng;
+};
+
+// V_c and the chunk's sum of dt, for c >= 1: a thread per (b, c, channel, state group), the states
+// of the forward kernel's thread (16, or N below 16) in the forward table's pair order.
+template <typename Tin, int N>
+__global__ void __launch_bounds__(128) nadj_kernel(const AdjParams p) {
+  constexpr int NS = N >= 16 ? 16 : N;
+  constexpr int NG = N / NS;
+  constexpr int NPAIR = NS / 2;
+  const int gl = blockIdx.x * 128 + threadIdx.x;
+  const int d = gl / NG, g = gl % NG;
+  const int c = blockIdx.y + 1;
+  const int b = blockIdx.z;
+  if (d >= p.D) return;
+  const int64_t L = p.L, D = p.D;
+  const int tc = c * p.TC, te = min(p.L, tc + p.TC);
+  const Tin* DT = static_cast<const Tin*>(p.dt);
+  float2 a2[NPAIR], cr[NPAIR], ci[NPAIR];
+#pragma unroll
+  for (int q = 0; q < NPAIR; ++q) {
+    const int n = g * NS + 2 * q;
+    a2[q] = f2(p.A[int64_t(d) * N + n] * LOG2E_F, p.A[int64_t(d) * N + n + 1] * LOG2E_F);
+    cr[q] = ci[q] = f2(0.f, 0.f);
+  }
+  float sdt = 0.f;
+  const int f_first = tc / T_SUB, f_last = (te - 1) / T_SUB;
+  for (int f = f_last; f >= f_first; --f) {
+    if (f < f_last) {   // into sub-chunk f from f + 1: e^{-i Phi_last(f)}
+      const float2* rr = p.rot + ((int64_t(b) * p.S32 + f) * 4 + 3) * N + g * NS;
+#pragma unroll
+      for (int q = 0; q < NPAIR; ++q) {
+        const float2 r0 = rr[2 * q], r1 = rr[2 * q + 1];
+        const float2 cc = f2(r0.x, r1.x), ss = f2(r0.y, r1.y);
+        const float2 nr = fma2(cc, cr[q], mul2(ss, ci[q]));
+        const float2 ni = fma2(cc, ci[q], mul2(f2(-ss.x, -ss.y), cr[q]));
+        cr[q] = nr;
+        ci[q] = ni;
+      }
+    }
+    const int t1 = min(te, (f + 1) * T_SUB) - 1, t0 = f * T_SUB;
+#pragma unroll 2
+    for (int t = t1; t >= t0; --t) {
+      const int64_t bt = int64_t(b) * L + t;
+      const float dy = __ldg(p.dy + bt * D + d);
+      const float dt = load_in<Tin>(DT, bt * D + d);
+      sdt += dt;
+      const float4* ct = p.tab + (bt * 2 + 1) * (N / 2);
+      const float2 dy2 = f2(dy, dy), dt2 = f2(dt, dt);
+#pragma unroll
+      for (int q = 0; q < NPAIR; ++q) {
+        const float4 cv = __ldg(ct + q * p.tab_ng + g);   // (Re, Re', -Im, -Im') of Ct
+        const float2 r2 = ex2_pair(mul2(dt2, a2[q]));
+        const float2 gr = fma2(dy2, f2(cv.x, cv.y), cr[q]);
+        const float2 gi = fma2(dy2, f2(cv.z, cv.w), ci[q]);
+        cr[q] = mul2(r2, gr);
+        ci[q] = mul2(r2, gi);
+      }
+    }
+  }
+  float4* v4 = reinterpret_cast<float4*>(p.V + ((int64_t(b) * p.C + c) * D + d) * N + g * NS);
+#pragma unroll
+  for (int q = 0; q < NPAIR; ++q) v4[q] = make_float4(cr[q].x, ci[q].x, cr[q].y, ci[q].y);
+  if (g == 0) p.Sdt[(int64_t(b) * p.C + c) * D + d] = sdt;
+}
+
+// P_c = e^{-i sum theta over chunk c} as the product of its sub-chunks' e^{-i Phi_last}.
+static __global__ void __launch_bounds__(256) nphase_kernel(const AdjParams p, int N) {
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= int64_t(p.B) * p.C * N) return;
+  const int n = int(gid % N);
+  const int64_t bc = gid / N;
+  const int c = int(bc % p.C);
+  const int b = int(bc / p.C);
+  const int tc = c * p.TC, te = min(p.L, tc + p.TC);
+  float pr = 1.f, pi = 0.f;
+  for (int f = tc / T_SUB; f <= (te - 1) / T_SUB; ++f) {
+    const float2 r = p.rot[((int64_t(b) * p.S32 + f) * 4 + 3) * N + n];
+    const float nr = pr * r.x + pi * r.y, ni = pi * r.x - pr * r.y;   // times conj(r)
+    pr = nr;
+    pi = ni;
+  }
+  p.P[gid] = make_float2(pr, pi);
+}
+
+// kappa_c for every chunk, walking from the last: a thread per (b, d, n).
+static __global__ void __launch_bounds__(256) ncombine_kernel(const AdjParams p, int N) {
+  const int64_t gid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (gid >= int64_t(p.B) * p.D * N) return;
+  const int n = int(gid % N);
+  const int64_t bd = gid / N;
+  const int d = int(bd % p.D);
+  const int b = int(bd / p.D);
+  const float a2 = p.A[int64_t(d) * N + n] * LOG2E_F;
+  float kr = 0.f, ki = 0.f;
+  for (int c = p.C - 1; c >= 1; --c) {
+    const int64_t bcd = (int64_t(b) * p.C + c) * p.D + d;
+    p.kap[bcd * N + n] = make_float2(kr, ki);
+    const float e = ex2_approx(a2 * p.Sdt[bcd]);
+    const float2 P = p.P[(int64_t(b) * p.C + c) * N + n];
+    const float gr = e * P.x, gi = e * P.y;
+    const float2 V = p.V[bcd * N + n];
+    const float nr = V.x + gr * kr - gi * ki, ni = V.y + gr * ki + gi * kr;
+    kr = nr;
+    ki = ni;
+  }
+  p.kap[(int64_t(b) * p.C * p.D + d) * N + n] = make_float2(kr, ki);
 }
 
 // dBc, dCc from the rotated-frame sums: thread per (b, sub-chunk, n), the sub-chunk's running phase
