@@ -56,10 +56,14 @@ TOL = {"f32": 1e-4, "bf16": 2e-3}
 #   (plus an ex2 and a reciprocal).
 ALU_OPS_PER_ELEM = {0: 6, 1: 6, 2: 22}
 ZOH_ALU_OPS_PER_ELEM = ALU_OPS_PER_ELEM[2]
-# FP32 lane-operations per element of the backward pass (csscan_backward), counted from its
-# kernels: the checkpoint pass (~10 exp-Euler / ~17 trapezoid), the segment recompute (the same
-# again) and the reverse step (~28 / ~45).
-BWD_ALU_OPS_PER_ELEM = {0: 48, 1: 79}
+# FP32 lane-operations per element of the backward pass (csscan_backward) on inputs that meet the
+# tile-copy rules, counted from the formulation its kernels follow (rotating frame, look-ahead form,
+# so both modes do the same per-element work): the checkpoint scan 6 (as the forward); the
+# gradient kernel's recompute of the states, 1.5 passes of decay exponent 1, w Bt 2 and the update 2;
+# its reverse step: adjoint 2, Re(conj(Bt) gamma) 2, rho = r gamma 2, G(z) = rho conj(g) 4,
+# A Re G(z) 1, dA 1, dtheta 1, dBc 2, dCc 2 and the pair sum 0.5. (Time chunks add ~5 per element
+# for the chunk carries; not counted.)
+BWD_ALU_OPS_PER_ELEM = {0: 31, 1: 31}
 FP32_LANES_PER_SM = 128
 # nominal HBM3e bandwidth of the part (the measured copy peak is the roofline's denominator;
 # this one is reported beside it)
@@ -334,33 +338,37 @@ def alu_roofline(ops_per_elem: float, elements: int, seconds: float, clk: dict) 
 
 # ------------------------------------------------------------------------------ CPU oracle
 def cpu_oracle_sample(inp: wl.Inputs, target_s: float, nthreads: int = 0):
-    """Times the float64 oracle on a prefix of batch 0's channels (all L steps, all N states),
-    sized to about target_s seconds. Returns (Gelem/s, threads, description, seconds, y_ref)
-    with y_ref the oracle's output for those rows, (1, L, nd)."""
+    """Times the float64 oracle on a prefix of batch 0's channels (all L steps, all N states), or,
+    when all of batch 0 takes well under target_s, on the first nb whole batch rows; sized to about
+    target_s seconds. Returns (Gelem/s, threads, description, seconds, y_ref) with y_ref the
+    oracle's output for those rows, (nb, L, nd)."""
     import oracle
     w = inp.workload
     lib = oracle.load()
     threads = oracle.last_thread_count(nthreads)
 
-    def run(nd):
-        f = wl.widen(inp, b=slice(0, 1), d=np.arange(nd))
+    def run(nb, nd):
+        f = wl.widen(inp, b=slice(0, nb), d=np.arange(nd))
         t0 = time.perf_counter()
         y = oracle.forward(f["x"], f["delta"], f["A"], f["Bc"], f["Cc"], f["theta"], f["lam"], f["Dskip"], w.mode,
                            nthreads=nthreads, lib=lib)
         return time.perf_counter() - t0, y
 
-    nd = min(w.D, threads)
-    dt, y = run(nd)
+    nb, nd = 1, min(w.D, threads)
+    dt, y = run(nb, nd)
     while dt < 0.5 and nd < w.D:
         nd = min(w.D, nd * 4)
-        dt, y = run(nd)
+        dt, y = run(nb, nd)
     nd_final = max(1, min(w.D, int(nd * target_s / max(dt, 1e-6))))
-    if nd_final != nd:
+    if nd_final == w.D and nd == w.D:
+        nb = max(1, min(w.B, int(target_s / max(dt, 1e-6))))
+    if nd_final != nd or nb != 1:
         nd = nd_final
-        dt, y = run(nd)
-    elems = w.L * nd * w.N
-    desc = f"batch 0, channels 0..{nd - 1} of {w.D}, all {w.L} steps and {w.N} states ({elems:.3e} elements)"
-    return elems / dt / 1e9, oracle.last_thread_count(nthreads, rows=nd), desc, dt, y
+        dt, y = run(nb, nd)
+    elems = nb * w.L * nd * w.N
+    rows = "batch 0" if nb == 1 else f"batch rows 0..{nb - 1} of {w.B}"
+    desc = f"{rows}, channels 0..{nd - 1} of {w.D}, all {w.L} steps and {w.N} states ({elems:.3e} elements)"
+    return elems / dt / 1e9, oracle.last_thread_count(nthreads, rows=nb * nd), desc, dt, y
 
 
 def parity_errors(y: np.ndarray, y_ref: np.ndarray, x64: np.ndarray, dskip: np.ndarray):
@@ -596,7 +604,7 @@ def run_ours(args):
     elapsed_ms = t["elapsed_ms"]
     max_s = reduce_max(elapsed_ms / 1e3)
     value = aggregate_value(w.elements, K, world, max_s)
-    y_timed = y[0].clone() if rank == 0 else None   # batch row 0 of the timed output, for the parity check
+    y_timed = y.clone() if rank == 0 else None   # the timed output, for the parity check
 
     # end to end through the public API: pinned host inputs -> device, scan, y -> host, every
     # byte of every step inside the timed region. The batch is cut into pieces of whole rows on
@@ -669,9 +677,9 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         v, cores, desc, secs, y_ref = cpu_oracle_sample(inp, args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "seconds": secs}
-        nd = y_ref.shape[2]
-        f = wl.widen(inp, b=slice(0, 1), d=np.arange(nd))
-        e, e_ssm = parity_errors(y_timed[None, :, :nd].cpu().numpy().astype(np.float64), y_ref, f["x"], f["Dskip"])
+        nb, nd = y_ref.shape[0], y_ref.shape[2]
+        f = wl.widen(inp, b=slice(0, nb), d=np.arange(nd))
+        e, e_ssm = parity_errors(y_timed[:nb, :, :nd].cpu().numpy().astype(np.float64), y_ref, f["x"], f["Dskip"])
         parity = {"e": e, "e_ssm": e_ssm, "tol": TOL[w.dtype], "pass": bool(e <= TOL[w.dtype]),
                   "rows": "the timed output against the oracle rows of cpu_baseline: " + desc}
 

@@ -74,8 +74,11 @@ enum {
                                       predecessor's carry (reported by csscan_get_device_status;
                                       the outputs of that call are not valid) */
   CSSCAN_ERR_PIPELINE_TIMEOUT = 6, /* device: a tile copy did not arrive within its limit */
-  CSSCAN_ERR_SCRATCH_LIMIT = 7     /* csscan_forward_noalloc: the problem needs more scratch than
+  CSSCAN_ERR_SCRATCH_LIMIT = 7,    /* csscan_forward_noalloc: the problem needs more scratch than
                                       its fixed CSSCAN_NOALLOC_SCRATCH_BYTES array holds */
+  CSSCAN_ERR_BOUNDS = 8            /* device, bounds-checked builds only (CSSCAN_BOUNDS_CHECK): a
+                                      kernel index fell outside its array; the access was redirected
+                                      to the array's first element and the outputs are not valid */
 };
 
 /* Discretisation of the injection ("Mamba-3 paper story", discretisation table):

@@ -21,6 +21,9 @@ HEADERS = [os.path.join(CSRC, f) for f in ("scan_kernels.cuh", "nscan_kernels.cu
           [os.path.join(ROOT, "include", "csscan.h")]
 OUTPUT = os.path.join(HERE, "libcsscan.so")
 BUILD_DIR = os.path.join(HERE, "_build")
+# the bounds-checked variant (compiled with CSSCAN_BOUNDS_CHECK): see build_checked
+CHECKED_OUTPUT = os.path.join(HERE, "libcsscan_checked.so")
+CHECKED_BUILD_DIR = os.path.join(HERE, "_build_checked")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + os.path.join(ROOT, "include")]
@@ -52,6 +55,16 @@ def build(force: bool = False, verbose: bool = False, output: str = OUTPUT, defi
         objs = list(pool.map(compile_one, SOURCES))
     subprocess.run([NVCC, *ARCH, "-shared", "-cudart", "static", "-o", output, *objs], check=True)
     return output
+
+
+def build_checked(force: bool = False) -> str:
+    """The bounds-checked library: the same sources compiled with CSSCAN_BOUNDS_CHECK, under which
+    the kernels range-check their shared-memory and global indices, record CSSCAN_ERR_BOUNDS for
+    csscan_get_device_status and redirect the access instead of leaving its array (a debugging
+    build; slower than libcsscan.so)."""
+    if not force and up_to_date(CHECKED_OUTPUT):
+        return CHECKED_OUTPUT
+    return build(force=True, output=CHECKED_OUTPUT, defines=("CSSCAN_BOUNDS_CHECK",), build_dir=CHECKED_BUILD_DIR)
 
 
 if __name__ == "__main__":

@@ -425,6 +425,7 @@ int csscan_get_device_status(cudaStream_t stream) {
   CSSCAN_CUDA(cudaMemcpy(hdr, base, sizeof(hdr), cudaMemcpyDeviceToHost));
   if (hdr[H_ERROR] == 0) return CSSCAN_OK;
   CSSCAN_CUDA(cudaMemset(static_cast<uint32_t*>(base) + H_ERROR, 0, 3 * sizeof(uint32_t)));
+  if (hdr[H_ERROR] & ERR_BOUNDS) return CSSCAN_ERR_BOUNDS;
   if (hdr[H_ERROR] & ERR_PIPELINE) return CSSCAN_ERR_PIPELINE_TIMEOUT;
   return CSSCAN_ERR_LOOKBACK_TIMEOUT;
 }
@@ -443,6 +444,8 @@ const char* csscan_status_string(int status) {
     case CSSCAN_ERR_SCRATCH_LIMIT:
       return "problem needs more scratch than csscan_forward_noalloc's fixed array (CSSCAN_NOALLOC_SCRATCH_BYTES) holds; "
              "use csscan_forward";
+    case CSSCAN_ERR_BOUNDS:
+      return "a kernel index fell outside its array on the device (bounds-checked build); the outputs are not valid";
     default: return "unknown status";
   }
 }

@@ -214,6 +214,7 @@ inline TableParams table_params(const Args& a, const Plan& pl, char* rest, int N
   tp.ng = 1;
   tp.planes = 2;
   tp.plane_w = 2 * N;
+  tp.hdr = nullptr;
   return tp;
 }
 
@@ -240,6 +241,7 @@ struct NScan {
     tp.ng = TL::NG;
     tp.planes = TL::PLANES;
     tp.plane_w = TL::W;
+    tp.hdr = hdr;
     ScanParams sp;
     std::memset(&sp, 0, sizeof(sp));
     const CUtensorMapDataType tin = sizeof(Tin) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;

@@ -80,6 +80,7 @@ struct MScan {
     tp.S = int(S16);
     tp.ng = TL::NG;
     tp.auxw = TL::AUXW;
+    tp.hdr = reinterpret_cast<uint32_t*>(base);
 
     MScanParams mp;
     std::memset(&mp, 0, sizeof(mp));

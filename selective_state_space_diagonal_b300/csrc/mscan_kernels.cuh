@@ -87,6 +87,7 @@ struct MTableParams {
                        // 1 - lam_{t+1} (0 at t = L-1) (trapezoid)
   float* rot;          // (B, S, N, 2): e^{i Phi} after the sub-chunk's last step
   int B, L, N, P, S, ng, auxw;
+  uint32_t* hdr;       // workspace header (error word of bounds-checked builds)
 };
 
 // One thread per (b, sub-chunk, n): the running phase, the rotated Bm and Cm of every channel,
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(256) mtable_kernel(MTableParams p) {
     const int64_t tn = (int64_t(b) * p.L + t) * p.N + n;
     phi += load_in<Tin>(th, tn);
     sincosf(phi, &sn, &cs);
-    float* row = p.tab + (int64_t(b) * p.L + t) * (2 * P * W);
+    float* row = p.tab + CSSCAN_BCK(p.hdr, int64_t(b) * p.L + t, int64_t(p.B) * p.L, 21) * (2 * P * W);
     float br[P], bi[P], cr[P], ci[P];
 #pragma unroll
     for (int q = 0; q < P; ++q) {
@@ -262,7 +263,7 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
     if (c == 0) {
       pass1 = true;
     } else {
-      if (tid == 0) s_ctl[2] = flag_ready(ld_acquire_gpu(&p.ws.flags[(c - 1) * p.n_tiles + j]), epoch, ST_INCL);
+      if (tid == 0) s_ctl[2] = flag_ready(ld_acquire_gpu(&p.ws.flags[CSSCAN_BCK(hdr, (c - 1) * p.n_tiles + j, p.n_units, 18)]), epoch, ST_INCL);
       __syncthreads();
       pass1 = !s_ctl[2];
     }
@@ -334,16 +335,17 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
       float* yrow = p.y + ((b * L + t_sub0) * H + h) * P;   // used only by the lanes of valid heads
 
       auto prep = [&](int tt, const Scal& pv, Scal& sc, float2 (&e)[NPAIR]) {
-        smem_row<Tin, P>(sx + tt * (DH * P), sc.x);
+        smem_row<Tin, P>(sx + CSSCAN_BCKO(hdr, tt * (DH * P), hl * P, SG::X_ROWS * DH * P, 11), sc.x);
         float cw;
         if constexpr (MODE == 1) {
           sc.dt = pv.dtn;
-          sc.dtn = smem_in<Tin>(sdt, (tt + 1) * DH);
-          const float2 lm = *reinterpret_cast<const float2*>(saux + tt * TL::AUXW + TL::LAMW);
+          sc.dtn = smem_in<Tin>(sdt, CSSCAN_BCKO(hdr, (tt + 1) * DH, hl, SG::DT_ROWS * DH, 12));
+          const float2 lm =
+              *reinterpret_cast<const float2*>(saux + CSSCAN_BCK(hdr, tt, SG::AUX_ROWS, 13) * TL::AUXW + TL::LAMW);
           sc.m = lm.y * sc.dtn;
           cw = fmaf(lm.x, sc.dt, sc.m);
         } else {
-          sc.dt = smem_in<Tin>(sdt, tt * DH);
+          sc.dt = smem_in<Tin>(sdt, CSSCAN_BCKO(hdr, tt * DH, hl, SG::DT_ROWS * DH, 12));
           sc.dtn = 0.f;
           sc.m = 0.f;
           cw = sc.dt;
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
       // and the update of every state pair, and (WITH_Y) this lane's P partial outputs into
       // part[u * P ..].
       auto step = [&](int tt, int u, float (&part)[1][LEN]) {
-        const float4* row = stab + tt * (2 * P * W4);
+        const float4* row = stab + CSSCAN_BCK(hdr, tt, SG::TAB_ROWS, 14) * (2 * P * W4);
         Scal nxt;
         float2 en[NPAIR];
         prep(tt + 1, cur, nxt, en);
@@ -417,7 +419,7 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
           const int t = tt + s_hold;
           if (hvalid && t < nt) {
             float xa[P];   // the step's inputs: the held channels' Dskip term and the correction
-            smem_row<Tin, P>(sx + t * (DH * P), xa);
+            smem_row<Tin, P>(sx + CSSCAN_BCKO(hdr, t * (DH * P), hl * P, SG::X_ROWS * DH * P, 11), xa);
             float out[HOLDN];
             float m = 0.f;
             if constexpr (MODE == 1) m = saux[t * TL::AUXW + TL::LAMW + 1] * smem_in<Tin>(sdt, (t + 1) * DH);
@@ -438,7 +440,9 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
               }
               out[v] = fmaf(Dsk[v], xv, fmaf(-m, corr, part[0][v]));
             }
-            store_row<HOLDN>(yrow + int64_t(t) * H * P + p0, out);
+            store_row<HOLDN>(yrow + CSSCAN_BCKO(hdr, int64_t(t) * H * P + p0, ((b * L + t_sub0) * H + h) * P,
+                                                int64_t(p.B) * L * H * P, 16),
+                             out);
           }
         }
       }
@@ -475,7 +479,9 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
     aborted = __syncthreads_or(aborted) != 0;
   };
 
-  auto rec_of = [&](float2* base, int u) { return base + (int64_t(u) * DH + hl) * N + n0; };
+  auto rec_of = [&](float2* base, int u) {
+    return base + (int64_t(CSSCAN_BCK(hdr, u, p.n_units, 17)) * DH + hl) * N + n0;
+  };
   auto load_states = [&](const float2* rec, float2* re, float2* im) {
     const float4* r4 = reinterpret_cast<const float4*>(rec);
 #pragma unroll
@@ -494,7 +500,7 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
   auto publish = [&](uint32_t status) {
     __threadfence();
     __syncthreads();
-    if (tid == 0 && !silent) st_release_gpu(&p.ws.flags[unit], (epoch << 2) | status);
+    if (tid == 0 && !silent) st_release_gpu(&p.ws.flags[CSSCAN_BCK(hdr, unit, p.n_units, 18)], (epoch << 2) | status);
   };
 
   float2 hr[NPAIR], hi[NPAIR];
@@ -550,7 +556,7 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
           while (true) {
             uint32_t st = ST_INCL;   // before the sequence: the zero initial state acts as a final state
             if (cp >= 0) {
-              const uint32_t f = ld_acquire_gpu(&p.ws.flags[unit_of(cp)]);
+              const uint32_t f = ld_acquire_gpu(&p.ws.flags[CSSCAN_BCK(hdr, unit_of(cp), p.n_units, 18)]);
               st = ((f >> 2) == epoch) ? (f & 3u) : ST_NONE;
             }
             const unsigned incl = __ballot_sync(0xffffffffu, st == ST_INCL);
@@ -613,7 +619,7 @@ __global__ void __launch_bounds__(THREADS, 2) mscan_kernel(const __grid_constant
     }
   } else if (CARRY != CARRY_NONE && c > 0) {
     if (tid == 0) {
-      const uint32_t* fp = &p.ws.flags[unit_of(c - 1)];
+      const uint32_t* fp = &p.ws.flags[CSSCAN_BCK(hdr, unit_of(c - 1), p.n_units, 18)];
       long long polls = 0;
       int tout = 0;
       while (!flag_ready(ld_acquire_gpu(fp), epoch, ST_INCL)) {

@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
 
       auto ckpt_of = [&](int k) {
         const int d = d0 + (k * WARPS + w) * M + c;
-        return (s > 0 && d < p.D) ? __ldcg(p.ckpt + ((int64_t(b) * p.S8 + s) * D + d) * (N / 2) + g)
+        return (s > 0 && d < p.D) ? __ldcg(p.ckpt + ((int64_t(b) * p.S8 + CSSCAN_BCK(p.hdr, s, p.S8, 31)) * D + d) * (N / 2) + g)
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
       };
       float4 ck_next = ckpt_of(0);
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
             const float x = smem_in<Tin>(sX, i * BC + cbA);
             const float dt = pre[i * BC + cbA].x;
             const float dy = sDY[i * BC + cbA];
-            const int64_t row = (int64_t(b) * L + ts + i) * D + dA_;
+            const int64_t row = CSSCAN_BCK(p.hdr, (int64_t(b) * L + ts + i) * D + dA_, int64_t(p.B) * L * D, 32);
             dD_acc = fmaf(dy, x, dD_acc);
             if constexpr (MODE == 0) {
               p.dx[row] = fmaf(dt, gq.x, DsA * dy);
@@ -401,12 +401,13 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
                 const float gwe = fmaf(-dy, ax.z, gq.x);
                 const float crs = x * ax.y * gwe;
                 lam_next = -x * dtn * gwe;
+                const int64_t nxt = CSSCAN_BCK(p.hdr, row + D, int64_t(p.B) * L * D, 32);
                 if (half == 0) {
-                  p.ddt[row + D] = s_hpend[cbA] + crs;
+                  p.ddt[nxt] = s_hpend[cbA] + crs;
                 } else if (s < s_last) {
-                  p.ddt[row + D] = s_pend[(s + 1) & 1][cbA] + crs;
+                  p.ddt[nxt] = s_pend[(s + 1) & 1][cbA] + crs;
                 } else {
-                  p.xb[(int64_t(b) * p.C + chunk + 1) * D + dA_] = crs;
+                  p.xb[CSSCAN_BCK(p.hdr, (int64_t(b) * p.C + chunk + 1) * D + dA_, int64_t(p.B) * p.C * D, 33)] = crs;
                 }
               }
             }
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
         const int nh = min(H, nt - i0);
         for (int o = tid; o < nh * 3 * NG; o += THREADS) {
           const int ii = o / (3 * NG), rem = o % (3 * NG), kind = rem / NG, gg = rem % NG;
-          const int64_t tn = (int64_t(b) * L + ts + i0 + ii) * N + 2 * gg;
+          const int64_t tn = CSSCAN_BCK(p.hdr, (int64_t(b) * L + ts + i0 + ii) * N + 2 * gg, int64_t(p.B) * L * N, 34);
           if (kind == 0) {
             atomicAdd(reinterpret_cast<float2*>(p.dtheta + tn), rsum(ii, 0, gg));
           } else {

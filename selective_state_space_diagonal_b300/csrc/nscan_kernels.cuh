@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(256) ntable_kernel(TableParams p) {
     const float cr = load_in<Tin>(Cc, 2 * tn), ci = load_in<Tin>(Cc, 2 * tn + 1);
     const float btr = cs * br + sn * bi;   // Re(e^{-i Phi} Bc)
     const float bti = cs * bi - sn * br;   // Im(e^{-i Phi} Bc)
-    float* row = p.tab + (int64_t(b) * p.L + t) * (p.planes * W);
+    float* row = p.tab + CSSCAN_BCK(p.hdr, int64_t(b) * p.L + t, int64_t(p.B) * p.L, 20) * (p.planes * W);
     row[idx] = btr;
     row[idx + 2] = bti;
     row[W + idx] = cs * cr - sn * ci;        // Re(e^{+i Phi} Cc)
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
     if (c == 0) {
       pass1 = true;
     } else {
-      if (tid == 0) s_ctl[2] = flag_ready(ld_acquire_gpu(&p.ws.flags[(c - 1) * p.n_tiles + j]), epoch, ST_INCL);
+      if (tid == 0) s_ctl[2] = flag_ready(ld_acquire_gpu(&p.ws.flags[CSSCAN_BCK(hdr, (c - 1) * p.n_tiles + j, p.n_units, 8)]), epoch, ST_INCL);
       __syncthreads();
       pass1 = !s_ctl[2];
     }
@@ -344,19 +344,19 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
       // scalars and decays of local step tt (rows tt of x and aux, tt and tt + 1 of dt), given the
       // previous step's scalars
       auto prep = [&](int tt, const Scal& pv, Scal& sc, float2 (&e)[NPAIR]) {
-        const float x = smem_in<Tin>(sx, tt * DT);
+        const float x = smem_in<Tin>(sx, CSSCAN_BCKO(hdr, tt * DT, cl, SG::X_ROWS * DT, 1));
         float w, dt;
         if constexpr (MODE == 1) {
           dt = pv.dtn;   // dt_t was the previous step's look-ahead
-          const float dtn = smem_in<Tin>(sdt, (tt + 1) * DT);
-          const float4 a = saux[tt];   // (lam_t, 1 - lam_{t+1}, E_t, 0)
+          const float dtn = smem_in<Tin>(sdt, CSSCAN_BCKO(hdr, (tt + 1) * DT, cl, SG::DT_ROWS * DT, 2));
+          const float4 a = saux[CSSCAN_BCK(hdr, tt, SG::AUX_ROWS, 3)];   // (lam_t, 1 - lam_{t+1}, E_t, 0)
           const float m = a.y * dtn;
           w = x * fmaf(a.x, dt, m);
           sc.pc = m * x;
           sc.E = a.z;
           sc.dtn = dtn;
         } else {
-          dt = smem_in<Tin>(sdt, tt * DT);
+          dt = smem_in<Tin>(sdt, CSSCAN_BCKO(hdr, tt * DT, cl, SG::DT_ROWS * DT, 2));
           w = x * dt;
           sc.pc = 0.f;
           sc.E = 0.f;
@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
       }
 
       auto step = [&](int tt) {
-        const float4* row = stab + tt * (PL * W4);
+        const float4* row = stab + CSSCAN_BCK(hdr, tt, SG::TAB_ROWS, 4) * (PL * W4);
         Scal nxt;
         float2 en[NPAIR];
         prep(tt + 1, cur, nxt, en);
@@ -402,7 +402,8 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
 #pragma unroll
           for (int o = 1; o < NG; o <<= 1) ys += __shfl_xor_sync(0xffffffffu, ys, o);
           const float yv = fmaf(cur.sig, ys, fmaf(-cur.pc, cur.E, Dsk * cur.x));
-          if (g == 0 && dvalid) __stcs(yrow + tt * D, yv);
+          if (g == 0 && dvalid)
+            __stcs(yrow + CSSCAN_BCKO(hdr, tt * D, (b * L + t_sub0) * D + d, int64_t(p.B) * L * D, 6), yv);
         } else if (!WITH_Y) {
           sdt_acc += cur.dt;
         }
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
       // the true state (sigma of the last step times s) before segment s8, as (re, im) per state
       auto store_ckpt = [&](int s8) {
         if (!dvalid) return;
-        float4* r4 = p.ckpt + ((int64_t(b) * p.S8 + s8) * D + d) * (N / 2) + n0 / 2;
+        float4* r4 = p.ckpt + ((int64_t(b) * p.S8 + CSSCAN_BCK(hdr, s8, p.S8, 9)) * D + d) * (N / 2) + n0 / 2;
 #pragma unroll
         for (int q = 0; q < NPAIR; ++q)
           __stcg(r4 + q, make_float4(aw_last * sr[q].x, aw_last * si[q].x, aw_last * sr[q].y, aw_last * si[q].y));
@@ -466,7 +467,9 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
   };
 
   // ---- per-state helpers on the workspace records (float2 per state, states contiguous)
-  auto rec_of = [&](float2* base, int u) { return base + (int64_t(u) * DT + cl) * p.N + n0; };
+  auto rec_of = [&](float2* base, int u) {
+    return base + (int64_t(CSSCAN_BCK(hdr, u, p.n_units, 7)) * DT + cl) * p.N + n0;
+  };
   auto load_states = [&](const float2* rec, float2* re, float2* im) {
     const float4* r4 = reinterpret_cast<const float4*>(rec);
 #pragma unroll
@@ -487,7 +490,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
   auto publish = [&](uint32_t status) {
     __threadfence();
     __syncthreads();
-    if (tid == 0 && !silent) st_release_gpu(&p.ws.flags[unit], (epoch << 2) | status);
+    if (tid == 0 && !silent) st_release_gpu(&p.ws.flags[CSSCAN_BCK(hdr, unit, p.n_units, 8)], (epoch << 2) | status);
   };
 
   float2 hr[NPAIR], hi[NPAIR];   // carry-in h_{tc-1}
@@ -547,7 +550,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
           while (true) {
             uint32_t st = ST_INCL;   // before the sequence: the initial state acts as a final state
             if (cp >= 0) {
-              const uint32_t f = ld_acquire_gpu(&p.ws.flags[unit_of(cp)]);
+              const uint32_t f = ld_acquire_gpu(&p.ws.flags[CSSCAN_BCK(hdr, unit_of(cp), p.n_units, 8)]);
               st = ((f >> 2) == epoch) ? (f & 3u) : ST_NONE;
             }
             const unsigned incl = __ballot_sync(0xffffffffu, st == ST_INCL);
@@ -618,7 +621,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
     // ---- serial carry, or a decoupled chunk whose predecessor had already published its
     // final state when this block started: wait for (or take) that final state
     if (tid == 0) {
-      const uint32_t* fp = &p.ws.flags[unit_of(c - 1)];
+      const uint32_t* fp = &p.ws.flags[CSSCAN_BCK(hdr, unit_of(c - 1), p.n_units, 8)];
       long long polls = 0;
       int tout = 0;
       while (!flag_ready(ld_acquire_gpu(fp), epoch, ST_INCL)) {

@@ -102,7 +102,7 @@ struct Stage {
 
 enum : uint32_t { ST_NONE = 0, ST_AGG = 1, ST_INCL = 2 };
 enum : int { CARRY_NONE = 0, CARRY_SERIAL = 1, CARRY_DECOUPLED = 2 };
-enum : uint32_t { ERR_LOOKBACK = 1u, ERR_PIPELINE = 2u };
+enum : uint32_t { ERR_LOOKBACK = 1u, ERR_PIPELINE = 2u, ERR_BOUNDS = 4u };
 enum { H_EPOCH = 0, H_TICKET = 1, H_DONE = 2, H_ERROR = 3, H_ERR_UNIT = 4, H_ERR_PRED = 5 };
 
 constexpr long long MBAR_WAIT_LIMIT = 1ll << 22;   // about 0.5 s of polling
@@ -135,6 +135,7 @@ struct TableParams {
                // by group (pair q of group g at position q * ng + g)
   int planes;  // nscan table only: planes per row (Bt, Ct, and -Bt when 3)
   int plane_w; // nscan table only: floats per plane (2N plus padding)
+  uint32_t* hdr;   // workspace header (error word of bounds-checked builds)
 };
 
 template <typename Tin, int MODE>
@@ -266,6 +267,33 @@ __device__ __forceinline__ void record_error(uint32_t* hdr, uint32_t code, int u
     hdr[H_ERR_PRED] = uint32_t(pred);
   }
 }
+
+// ------------------------------------------------------------------------- bounds checks
+// Builds with CSSCAN_BOUNDS_CHECK defined range-check the kernels' shared-memory and global
+// indices: CSSCAN_BCKO(hdr, i, off, n, site) checks off + i against [0, n); outside it, the first
+// failure records ERR_BOUNDS with the site number and the offending index in the workspace header,
+// and the index is replaced by -off so that the access lands on the array's first element. The
+// kernel then runs on to its end (no trap, and no early exit that would leave a barrier or a
+// successor waiting); the host reads the error as CSSCAN_ERR_BOUNDS. Other builds compile the
+// index unchanged.
+#ifdef CSSCAN_BOUNDS_CHECK
+static __device__ __noinline__ void bounds_fail(uint32_t* hdr, int site, long long j) {
+  record_error(hdr, ERR_BOUNDS, site, int(j < -2147483647LL ? -2147483647LL : (j > 2147483647LL ? 2147483647LL : j)));
+}
+template <typename I>
+__device__ __forceinline__ I bck_off(uint32_t* hdr, I i, long long off, long long n, int site) {
+  const long long j = (long long)i + off;
+  if (j < 0 || j >= n) {
+    bounds_fail(hdr, site, j);
+    return I(-off);
+  }
+  return i;
+}
+#define CSSCAN_BCKO(hdr, i, off, n, site) ::csscan::bck_off((hdr), (i), (long long)(off), (long long)(n), (site))
+#else
+#define CSSCAN_BCKO(hdr, i, off, n, site) (i)
+#endif
+#define CSSCAN_BCK(hdr, i, n, site) CSSCAN_BCKO(hdr, i, 0, n, site)
 
 __device__ __forceinline__ bool wait_bar_bounded(uint64_t* bar, uint32_t parity) {
   for (long long i = 0; i < MBAR_WAIT_LIMIT; ++i) {

@@ -24,6 +24,7 @@ CSSCAN_ERR_CUDA = 4
 CSSCAN_ERR_LOOKBACK_TIMEOUT = 5
 CSSCAN_ERR_PIPELINE_TIMEOUT = 6
 CSSCAN_ERR_SCRATCH_LIMIT = 7
+CSSCAN_ERR_BOUNDS = 8
 
 CSSCAN_MODE_EXP_EULER = 0
 CSSCAN_MODE_EXP_TRAPEZOID = 1
