@@ -192,8 +192,11 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
-  const int g = lane % NG;                        // state group of this thread
-  const int cl = (tid >> 5) * CPW + lane / NG;    // channel of this thread within the block's tile
+  // The lanes of one state group are contiguous (a warp holds CPW channels for each of the NG
+  // groups): a table load then has one address per quarter-warp (two shared-memory wavefronts per
+  // 128-bit load; with the groups interleaved lane by lane it takes four).
+  const int g = lane / CPW;                       // state group of this thread
+  const int cl = (tid >> 5) * CPW + lane % CPW;   // channel of this thread within the block's tile
   const int n0 = g * NS;                          // first state of this thread
   uint32_t* hdr = p.ws.hdr;
 
@@ -400,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, NSCAN_MIN_BLOCKS) nscan_kernel(const 
         if (OUT) {
           float ys = (acc0.x + acc0.y) + (acc1.x + acc1.y);
 #pragma unroll
-          for (int o = 1; o < NG; o <<= 1) ys += __shfl_xor_sync(0xffffffffu, ys, o);
+          for (int o = 1; o < NG; o <<= 1) ys += __shfl_xor_sync(0xffffffffu, ys, o * CPW);
           const float yv = fmaf(cur.sig, ys, fmaf(-cur.pc, cur.E, Dsk * cur.x));
           if (g == 0 && dvalid)
             __stcs(yrow + CSSCAN_BCKO(hdr, tt * D, (b * L + t_sub0) * D + d, int64_t(p.B) * L * D, 6), yv);
