@@ -204,6 +204,20 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
   float dD_acc = 0.f;
   __syncthreads();
 
+  // checkpoint of (segment s, channel k of this thread): the rotated state before the segment;
+  // and A of the channel's state pair
+  auto ckpt_of = [&](int s, int k) {
+    const int d = d0 + (k * WARPS + w) * M + c;
+    return (s > 0 && d < p.D) ? __ldcg(p.ckpt + ((int64_t(b) * p.S8 + CSSCAN_BCK(p.hdr, s, p.S8, 31)) * D + d) * (N / 2) + g)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto a_of = [&](int k) {
+    const int d = d0 + (k * WARPS + w) * M + c;
+    return d < p.D ? __ldg(reinterpret_cast<const float2*>(p.A + int64_t(d) * N) + g) : f2(0.f, 0.f);
+  };
+  float4 ck_next = ckpt_of(s_last, 0);
+  float2 A_next = a_of(0);
+
   bool aborted = false;
   int q = 0;
 #pragma unroll 1
@@ -243,29 +257,27 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
     // while its four steps are worked, and its per-(t, d) partials share one scratch region with
     // them. Each half regenerates g from the segment's checkpoint (the later half through all
     // eight steps, keeping the last five states; the earlier half through its four).
-#pragma unroll
-    for (int half = 1; half >= 0; --half) {
+    auto run_half = [&](auto half_tag) {
+      constexpr int half = decltype(half_tag)::value;
       constexpr int H = SEG / 2;
-      const int i0 = half * H;
-      float2 aT[H], aBr[H], aBi[H], aCr[H], aCi[H];   // per-(t, n) sums over this thread's channels
+      constexpr int i0 = half * H;
+      // per-(t, n) sums over this thread's channels: Im G(z) as sum rho_i g_r - sum rho_r g_i (two
+      // accumulators, subtracted once per half), dBc (re, im), dCc as (dy g_r, dy g_i) (negated once)
+      float2 aT[H], aT2[H], aBr[H], aBi[H], aCr[H], aCi[H];
 #pragma unroll
-      for (int ii = 0; ii < H; ++ii) aT[ii] = aBr[ii] = aBi[ii] = aCr[ii] = aCi[ii] = f2(0.f, 0.f);
+      for (int ii = 0; ii < H; ++ii) aT[ii] = aT2[ii] = aBr[ii] = aBi[ii] = aCr[ii] = aCi[ii] = f2(0.f, 0.f);
 
-      auto ckpt_of = [&](int k) {
-        const int d = d0 + (k * WARPS + w) * M + c;
-        return (s > 0 && d < p.D) ? __ldcg(p.ckpt + ((int64_t(b) * p.S8 + CSSCAN_BCK(p.hdr, s, p.S8, 31)) * D + d) * (N / 2) + g)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-      };
-      float4 ck_next = ckpt_of(0);
 #pragma unroll 1
       for (int k = 0; k < K; ++k) {
+        // this channel's checkpoint was loaded one channel earlier; load the next one now (the
+        // first channel of the next half or segment after the last channel)
         const float4 ck = ck_next;
-        if (k + 1 < K) ck_next = ckpt_of(k + 1);   // in flight while this channel is worked
+        const float2 A2 = A_next;
+        if (k + 1 < K) ck_next = ckpt_of(s, k + 1);
+        else if (half == 1) ck_next = ckpt_of(s, 0);
+        else if (s > s_first) ck_next = ckpt_of(s - 1, 0);
+        A_next = a_of(k + 1 < K ? k + 1 : 0);
         const int cb = (k * WARPS + w) * M + c;
-        const int d = d0 + cb;
-        const bool valid = d < p.D;
-        const int64_t dd = valid ? d : 0;
-        const float2 A2 = valid ? f2(p.A[dd * N + 2 * g], p.A[dd * N + 2 * g + 1]) : f2(0.f, 0.f);
         const float2 a2 = mul2(A2, f2(LOG2E_F, LOG2E_F));
         float4 cv = s_carry[k][tid];
         float2 cr = f2(cv.x, cv.y), ci = f2(cv.z, cv.w);
@@ -320,15 +332,15 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
           const float2 P2 = fma2(f2(bt.x, bt.y), gr, mul2(f2(bt.z, bt.w), gi));   // Re(conj(Bt) gamma)
           const float2 rr = mul2(r2, gr), ri = mul2(r2, gi);                      // rho = r gamma
           const float2 zr = fma2(rr, hr[ii], mul2(ri, hi[ii]));                   // Re G(z) = Re(rho conj(g_{t-1}))
-          const float2 zi = fma2(ri, hr[ii], mul2(f2(-rr.x, -rr.y), hi[ii]));      // Im G(z)
           const float2 Q2 = mul2(A2, zr);
           dA2 = fma2(f2(pv.x, pv.x), zr, dA2);
-          aT[ii] = add2(aT[ii], zi);
+          aT[ii] = fma2(ri, hr[ii], aT[ii]);                                      // Im G(z), in two parts
+          aT2[ii] = fma2(rr, hi[ii], aT2[ii]);
           const float2 w2 = f2(pv.y, pv.y);
           aBr[ii] = fma2(w2, gr, aBr[ii]);
           aBi[ii] = fma2(w2, gi, aBi[ii]);
           aCr[ii] = fma2(dy2, hr[ii + 1], aCr[ii]);
-          aCi[ii] = fma2(f2(-dy, -dy), hi[ii + 1], aCi[ii]);
+          aCi[ii] = fma2(dy2, hi[ii + 1], aCi[ii]);
           float2 pq = f2(P2.x + P2.y, Q2.x + Q2.y);   // (Gw, sum A Re G(z)) partials of this pair
           cr = rr;
           ci = ri;
@@ -366,7 +378,10 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
         for (int j0 = 0; j0 < H; j0 += ROWS) {
           const int ii = j0 + rA;
           const int i = i0 + ii;
-          float lam_i = 0.f, ge_i = 0.f, lam_next = 0.f;
+          float lam_i = 0.f, ge_i = 0.f, lam_next = 0.f;   // trapezoid only
+          (void)lam_i;
+          (void)ge_i;
+          (void)lam_next;
           if (i < nt && validA) {
             const float2 gq = sums(ii);
             const float x = smem_in<Tin>(sX, i * BC + cbA);
@@ -437,11 +452,11 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
 #pragma unroll
         for (int ii = 0; ii < H; ++ii) {
           float2* row = reinterpret_cast<float2*>(scr + ((ii * 5) * NG + g) * SROW) + slot2;
-          row[0] = aT[ii];
+          row[0] = f2(aT[ii].x - aT2[ii].x, aT[ii].y - aT2[ii].y);
           row[(NG * SROW) / 2] = aBr[ii];
           row[2 * ((NG * SROW) / 2)] = aBi[ii];
           row[3 * ((NG * SROW) / 2)] = aCr[ii];
-          row[4 * ((NG * SROW) / 2)] = aCi[ii];
+          row[4 * ((NG * SROW) / 2)] = f2(-aCi[ii].x, -aCi[ii].y);
         }
       }
       __syncthreads();
@@ -473,7 +488,9 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
         }
       }
       __syncthreads();
-    }
+    };
+    run_half(std::integral_constant<int, 1>{});
+    run_half(std::integral_constant<int, 0>{});
 
     if constexpr (MODE == 1) {
       if (tid <= SEG) {
