@@ -206,8 +206,25 @@ int launch_backward_rot(const BwdArgs& a, cudaStream_t st) {
 
   // ---- chunk carries: kappa_c entering every chunk's last step
   if (C > 1) {
+    using AS = ngrad::AdjStage<N, Tin>;
     ngrad::AdjParams ap;
-    ap.tab = reinterpret_cast<const float4*>(rest + fpl.o_tab);
+    std::memset(&ap, 0, sizeof(ap));
+    {
+      const CUtensorMapDataType tin =
+          sizeof(Tin) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      const uint64_t B = uint64_t(a.B), L = uint64_t(a.L), D = uint64_t(a.D), s_in = sizeof(Tin);
+      const uint64_t cdims[4] = {2 * N, 2, L, B};
+      const uint64_t cstrides[3] = {2 * N * 4, 4 * N * 4, L * 4 * N * 4};
+      const uint32_t cbox[4] = {2 * N, 1, T_SUB, 1};
+      const bool ok = map3(&ap.tm_dy, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.dy, D, L, B, D * 4, L * D * 4, AS::CH, T_SUB, 1) &&
+                      map3(&ap.tm_dt, tin, a.delta, D, L, B, D * s_in, L * D * s_in, AS::CH, T_SUB, 1) &&
+                      make_map(&ap.tm_ct, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rest + fpl.o_tab, 4, cdims, cstrides, cbox);
+      if (!ok) {
+        set_last_error("cuTensorMapEncodeTiled failed or unavailable");
+        return CSSCAN_ERR_CUDA;
+      }
+    }
+    ap.hdr = hdr;
     ap.rot = reinterpret_cast<const float2*>(rest + fpl.o_rot);
     ap.dy = a.dy;
     ap.dt = a.delta;
@@ -223,9 +240,11 @@ int launch_backward_rot(const BwdArgs& a, cudaStream_t st) {
     ap.TC = int(TC);
     ap.C = int(C);
     ap.tab_ng = NTile<N, NSF>::NG;
-    constexpr int NGA = N >= 16 ? N / 16 : 1;
-    const dim3 agrid{unsigned((a.D * NGA + 127) / 128), unsigned(C - 1), unsigned(a.B)};
-    ngrad::nadj_kernel<Tin, N><<<agrid, 128, 0, st>>>(ap);
+    int aocc = 0;
+    rc = occupancy_of(ngrad::nadj_kernel<Tin, N>, dev, AS::SMEM, &aocc);   // raises the shared-memory limit
+    if (rc != CSSCAN_OK) return rc;
+    const dim3 agrid{unsigned((a.D + AS::CH - 1) / AS::CH), unsigned(C - 1), unsigned(a.B)};
+    ngrad::nadj_kernel<Tin, N><<<agrid, 128, AS::SMEM, st>>>(ap);
     CSSCAN_CUDA(cudaGetLastError());
     const long long n_ph = (long long)a.B * C * N, n_cb = (long long)a.B * a.D * N;
     if (!grid_fits(n_ph) || !grid_fits(n_cb)) return CSSCAN_ERR_UNSUPPORTED;

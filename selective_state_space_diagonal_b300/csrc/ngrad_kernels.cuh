@@ -533,7 +533,10 @@ __global__ void __launch_bounds__(THREADS, GTile<N>::MIN_BLOCKS) ngrad_kernel(co
 // V_c being the carry out of chunk c's first step from a zero carry (the sub-chunk frames make the
 // decays real; crossing into an earlier sub-chunk multiplies by e^{-i Phi_last} of that sub-chunk).
 struct AdjParams {
-  const float4* tab;   // (B, L, 2, N/2) float4: the forward table (Bt and Ct planes)
+  CUtensorMap tm_dy;   // (D, L, B) f32, box (CH, T_SUB, 1)
+  CUtensorMap tm_dt;   // (D, L, B) input dtype, box (CH, T_SUB, 1)
+  CUtensorMap tm_ct;   // the forward table (2N, 2, L, B) f32, box (2N, 1, T_SUB, 1): the Ct plane
+  uint32_t* hdr;       // error word of the workspace header
   const float2* rot;   // (B, S32, 4, N) e^{i Phi} rows; row 3: after the sub-chunk's last step
   const float* dy;     // (B, L, D)
   const void* dt;      // (B, L, D) input dtype
@@ -546,30 +549,74 @@ struct AdjParams {
 };
 
 // V_c and the chunk's sum of dt, for c >= 1: a thread per (b, c, channel, state group), the states
-// of the forward kernel's thread (16, or N below 16) in the forward table's pair order.
+// of the forward kernel's thread (16, or N below 16) in the forward table's pair order; a block
+// of 128 threads owns 128 / NG channels of one (b, c). Each 32-step sub-chunk's dy and dt rows of
+// the block's channels and its Ct rows arrive by tile copies into a 2-slot ring (the next
+// sub-chunk's while the current one is worked); rows past the sequence's end arrive as zeros and
+// leave the carry unchanged.
+template <int N, typename Tin>
+struct AdjStage {
+  static constexpr int NS = N >= 16 ? 16 : N;
+  static constexpr int NG = N / NS;
+  static constexpr int CH = 128 / NG;   // channels per block
+  static constexpr int DY_BYTES = T_SUB * CH * 4;
+  static constexpr int DT_BYTES = T_SUB * CH * int(sizeof(Tin));
+  static constexpr int CT_BYTES = T_SUB * 2 * N * 4;
+  static constexpr int OFF_DY = 0;
+  static constexpr int OFF_DT = align128(OFF_DY + DY_BYTES);
+  static constexpr int OFF_CT = align128(OFF_DT + DT_BYTES);
+  static constexpr int BYTES = align128(OFF_CT + CT_BYTES);
+  static constexpr int TX_BYTES = DY_BYTES + DT_BYTES + CT_BYTES;
+  static constexpr int SMEM = 2 * BYTES + 128;
+};
+
 template <typename Tin, int N>
-__global__ void __launch_bounds__(128) nadj_kernel(const AdjParams p) {
-  constexpr int NS = N >= 16 ? 16 : N;
-  constexpr int NG = N / NS;
-  constexpr int NPAIR = NS / 2;
-  const int gl = blockIdx.x * 128 + threadIdx.x;
-  const int d = gl / NG, g = gl % NG;
+__global__ void __launch_bounds__(128) nadj_kernel(const __grid_constant__ AdjParams p) {
+  using AS = AdjStage<N, Tin>;
+  constexpr int NS = AS::NS, NG = AS::NG, CH = AS::CH, NPAIR = NS / 2;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((128u - (smem_addr(smem_raw) & 127u)) & 127u);
+  __shared__ __align__(8) uint64_t bar[2];
+  const int tid = threadIdx.x;
+  const int cl = tid / NG, g = tid % NG;
+  const int d0 = blockIdx.x * CH;
+  const int d = d0 + cl;
   const int c = blockIdx.y + 1;
   const int b = blockIdx.z;
-  if (d >= p.D) return;
-  const int64_t L = p.L, D = p.D;
   const int tc = c * p.TC, te = min(p.L, tc + p.TC);
-  const Tin* DT = static_cast<const Tin*>(p.dt);
+  const int f_first = tc / T_SUB, f_last = (te - 1) / T_SUB;
+  auto issue = [&](int f, int slot) {
+    unsigned char* base = smem + slot * AS::BYTES;
+    mbar_arrive_expect_tx(&bar[slot], uint32_t(AS::TX_BYTES));
+    tma_load_3d(base + AS::OFF_DY, &p.tm_dy, d0, f * T_SUB, b, &bar[slot]);
+    tma_load_3d(base + AS::OFF_DT, &p.tm_dt, d0, f * T_SUB, b, &bar[slot]);
+    tma_load_4d(base + AS::OFF_CT, &p.tm_ct, 0, 1, f * T_SUB, b, &bar[slot]);
+  };
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    fence_mbar_init();
+    prefetch_tmap(&p.tm_dy);
+    prefetch_tmap(&p.tm_dt);
+    prefetch_tmap(&p.tm_ct);
+    issue(f_last, 0);
+  }
+  __syncthreads();
+  const bool valid = d < p.D;
   float2 a2[NPAIR], cr[NPAIR], ci[NPAIR];
 #pragma unroll
   for (int q = 0; q < NPAIR; ++q) {
     const int n = g * NS + 2 * q;
-    a2[q] = f2(p.A[int64_t(d) * N + n] * LOG2E_F, p.A[int64_t(d) * N + n + 1] * LOG2E_F);
+    a2[q] = valid ? f2(p.A[int64_t(d) * N + n] * LOG2E_F, p.A[int64_t(d) * N + n + 1] * LOG2E_F) : f2(0.f, 0.f);
     cr[q] = ci[q] = f2(0.f, 0.f);
   }
   float sdt = 0.f;
-  const int f_first = tc / T_SUB, f_last = (te - 1) / T_SUB;
-  for (int f = f_last; f >= f_first; --f) {
+  bool aborted = false;
+  int k = 0;
+  for (int f = f_last; f >= f_first; --f, ++k) {
+    const int slot = k & 1;
+    // the other slot held sub-chunk f + 1, consumed before the barrier that closed it
+    if (tid == 0 && f > f_first) issue(f - 1, slot ^ 1);
     if (f < f_last) {   // into sub-chunk f from f + 1: e^{-i Phi_last(f)}
       const float2* rr = p.rot + ((int64_t(b) * p.S32 + f) * 4 + 3) * N + g * NS;
 #pragma unroll
@@ -582,18 +629,24 @@ __global__ void __launch_bounds__(128) nadj_kernel(const AdjParams p) {
         ci[q] = ni;
       }
     }
-    const int t1 = min(te, (f + 1) * T_SUB) - 1, t0 = f * T_SUB;
-#pragma unroll 2
-    for (int t = t1; t >= t0; --t) {
-      const int64_t bt = int64_t(b) * L + t;
-      const float dy = __ldg(p.dy + bt * D + d);
-      const float dt = load_in<Tin>(DT, bt * D + d);
+    const bool ok = wait_bar_bounded(&bar[slot], uint32_t(k >> 1) & 1u);
+    if (__syncthreads_or(!ok)) {
+      aborted = true;
+      break;
+    }
+    const unsigned char* base = smem + slot * AS::BYTES;
+    const float* sdy = reinterpret_cast<const float*>(base + AS::OFF_DY) + cl;
+    const Tin* sdtp = reinterpret_cast<const Tin*>(base + AS::OFF_DT) + cl;
+    const float4* sct = reinterpret_cast<const float4*>(base + AS::OFF_CT) + g;
+#pragma unroll 4
+    for (int r = T_SUB - 1; r >= 0; --r) {
+      const float dy = sdy[r * CH];
+      const float dt = smem_in<Tin>(sdtp, r * CH);
       sdt += dt;
-      const float4* ct = p.tab + (bt * 2 + 1) * (N / 2);
       const float2 dy2 = f2(dy, dy), dt2 = f2(dt, dt);
 #pragma unroll
       for (int q = 0; q < NPAIR; ++q) {
-        const float4 cv = __ldg(ct + q * p.tab_ng + g);   // (Re, Re', -Im, -Im') of Ct
+        const float4 cv = sct[r * (N / 2) + q * p.tab_ng];   // Ct: (Re, Re', -Im, -Im')
         const float2 r2 = ex2_pair(mul2(dt2, a2[q]));
         const float2 gr = fma2(dy2, f2(cv.x, cv.y), cr[q]);
         const float2 gi = fma2(dy2, f2(cv.z, cv.w), ci[q]);
@@ -601,11 +654,20 @@ __global__ void __launch_bounds__(128) nadj_kernel(const AdjParams p) {
         ci[q] = mul2(r2, gi);
       }
     }
+    __syncthreads();
   }
-  float4* v4 = reinterpret_cast<float4*>(p.V + ((int64_t(b) * p.C + c) * D + d) * N + g * NS);
+  if (aborted) {
+    if (tid == 0) {
+      record_error(p.hdr, ERR_PIPELINE, int(blockIdx.x), -4);
+      for (int u = k; u <= k + 1 && u <= f_last - f_first; ++u) wait_bar_bounded(&bar[u & 1], uint32_t(u >> 1) & 1u);
+    }
+    return;
+  }
+  if (!valid) return;
+  float4* v4 = reinterpret_cast<float4*>(p.V + ((int64_t(b) * p.C + c) * p.D + d) * N + g * NS);
 #pragma unroll
   for (int q = 0; q < NPAIR; ++q) v4[q] = make_float4(cr[q].x, ci[q].x, cr[q].y, ci[q].y);
-  if (g == 0) p.Sdt[(int64_t(b) * p.C + c) * D + d] = sdt;
+  if (g == 0) p.Sdt[(int64_t(b) * p.C + c) * p.D + d] = sdt;
 }
 
 // P_c = e^{-i sum theta over chunk c} as the product of its sub-chunks' e^{-i Phi_last}.
