@@ -86,7 +86,7 @@ enum {
  *   EXP_TRAPEZOID beta_t = (1 - lam_t) dt_t a_t on Bc_{t-1} x_{t-1}, gamma_t = lam_t dt_t
  *   ZOH           gamma_t = dt_t (e^{z_t} - 1) / z_t with z_t = dt_t A + i theta_t (the table's
  *                 A^{-1}(exp(dt A) - I) with the complex exponent of a_t in place of dt A);
- *                 the scans (csscan_forward, _ex, _state, _noalloc; N <= 32) and
+ *                 the scans (csscan_forward, _ex, _state, _noalloc; every N) and
  *                 csscan_decode_step; csscan_backward returns CSSCAN_ERR_UNSUPPORTED for it */
 typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1, CSSCAN_MODE_ZOH = 2 } csscan_mode_t;
 typedef enum { CSSCAN_F32 = 0, CSSCAN_BF16 = 1 } csscan_dtype_t;

@@ -108,7 +108,7 @@ namespace {
 
 // ----------------------------------------------------------------------------- forward checks
 // One set of rules for every forward entry point and every mode: pointers, sizes, the tile
-// copies' 16-byte rule on x and delta, and N (the zero-order hold takes N <= 32).
+// copies' 16-byte rule on x and delta, and N.
 int validate(const Args& a, const csscan_options_t& o) {
   if (a.mode != CSSCAN_MODE_EXP_EULER && a.mode != CSSCAN_MODE_EXP_TRAPEZOID && a.mode != CSSCAN_MODE_ZOH)
     return CSSCAN_ERR_INVALID_ARG;
@@ -121,7 +121,6 @@ int validate(const Args& a, const csscan_options_t& o) {
       o.poll_limit < 0)
     return CSSCAN_ERR_INVALID_ARG;
   if (a.N != 2 && a.N != 4 && a.N != 8 && a.N != 16 && a.N != 32 && a.N != 64) return CSSCAN_ERR_UNSUPPORTED;
-  if (a.mode == CSSCAN_MODE_ZOH && a.N > 32) return CSSCAN_ERR_UNSUPPORTED;
   if (a.B > (int64_t(1) << 31) - 1 || a.L > (int64_t(1) << 30) || a.D > (int64_t(1) << 30)) return CSSCAN_ERR_UNSUPPORTED;
   const size_t s = a.dtype == CSSCAN_F32 ? 4 : 2;
   if (!aligned(a.x, 16) || !aligned(a.delta, 16) || ((a.D * int64_t(s)) % 16) != 0) return CSSCAN_ERR_MISALIGNED;
@@ -436,8 +435,8 @@ const char* csscan_status_string(int status) {
     case CSSCAN_ERR_INVALID_ARG: return "invalid argument";
     case CSSCAN_ERR_MISALIGNED: return "misaligned pointer or row stride (x/delta need 16-byte alignment and D*sizeof(dtype) % 16 == 0)";
     case CSSCAN_ERR_UNSUPPORTED:
-      return "unsupported size or mode for this entry point (N in {2, 4, 8, 16, 32, 64}; N <= 32 for the backward and "
-             "for the zero-order-hold scan, which the backward does not take)";
+      return "unsupported size or mode for this entry point (N in {2, 4, 8, 16, 32, 64}; N <= 32 for the backward, "
+             "which does not take the zero-order hold, and for the MIMO scan)";
     case CSSCAN_ERR_CUDA: return g_last_cuda_error[0] ? g_last_cuda_error : "CUDA error";
     case CSSCAN_ERR_LOOKBACK_TIMEOUT: return "a chunk's carry wait timed out on the device";
     case CSSCAN_ERR_PIPELINE_TIMEOUT: return "a tile copy did not arrive within its limit on the device";

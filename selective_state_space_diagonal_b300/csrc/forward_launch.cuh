@@ -285,6 +285,20 @@ struct NScan {
 template <int N, typename Tin, int MODE, bool CKPT = false>
 struct RScan {
   using SG = Stage<N, Tin, MODE>;
+  // the table's tile-copy descriptor: rows of TABW N floats, boxed whole, or as (256, rows / 256)
+  // when a row is wider than one box (256 elements)
+  static bool table_map(CUtensorMap* m, const float* tab, uint64_t L, uint64_t B) {
+    constexpr uint64_t W = uint64_t(SG::TABW) * N;
+    if constexpr (W > 256) {
+      static_assert(W % 256 == 0, "table row not a whole number of boxes");
+      const uint64_t dims[4] = {256, W / 256, L, B};
+      const uint64_t strides[3] = {256 * 4, W * 4, L * W * 4};
+      const uint32_t box[4] = {256, uint32_t(W / 256), uint32_t(SG::TAB_ROWS), 1};
+      return make_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tab, 4, dims, strides, box);
+    } else {
+      return map3(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tab, W, L, B, W * 4, L * W * 4, uint32_t(W), SG::TAB_ROWS, 1);
+    }
+  }
   static_assert(SG::SMEM <= MAX_DYN_SMEM, "stage ring too large");
   static constexpr KernelShape shape() { return KernelShape{Tile<N>::DT, SG::SMEM, SG::TABW * N, MODE == 1 ? SG::AUX_W : 0}; }
   static int occ(int carry, int dev, int* out) {
@@ -304,8 +318,7 @@ struct RScan {
     const uint64_t B = uint64_t(a.B), L = uint64_t(a.L), D = uint64_t(a.D), S = uint64_t(pl.S);
     bool ok = map3(&sp.tm_x, tin, a.x, D, L, B, D * s_in, L * D * s_in, pl.DT, SG::X_ROWS, 1) &&
               map3(&sp.tm_dt, tin, a.delta, D, L, B, D * s_in, L * D * s_in, pl.DT, SG::DT_ROWS, 1) &&
-              map3(&sp.tm_tab, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.tab, SG::TABW * N, L, B, SG::TABW * N * 4,
-                   L * SG::TABW * N * 4, SG::TABW * N, SG::TAB_ROWS, 1) &&
+              table_map(&sp.tm_tab, tp.tab, L, B) &&
               map3(&sp.tm_rot, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.rot, 2 * N, 4 * S, B, 8 * N, 4 * S * 8 * N, 2 * N, 4, 1);
     if (ok && MODE == 1)
       ok = map3(&sp.tm_aux, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, tp.aux, SG::AUX_W, L, B, SG::AUX_W * 4, L * SG::AUX_W * 4,
@@ -367,7 +380,8 @@ int forward_dispatch(const Args& a, const csscan_options_t& o, cudaStream_t st, 
       case 8: return launch_forward<RScan<8, Tin, 2>>(a, o, st, fx);
       case 16: return launch_forward<RScan<16, Tin, 2>>(a, o, st, fx);
       case 32: return launch_forward<RScan<32, Tin, 2>>(a, o, st, fx);
-      default: return CSSCAN_ERR_UNSUPPORTED;   // the zero-order-hold table row exceeds one box at N = 64
+      case 64: return launch_forward<RScan<64, Tin, 2>>(a, o, st, fx);
+      default: return CSSCAN_ERR_UNSUPPORTED;
     }
   }
   int dev = 0, nsm = 0;

@@ -232,7 +232,8 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
 struct ScanParams {
   CUtensorMap tm_x;    // (D, L, B) input dtype, box (DT, T_SUB + 1, 1)
   CUtensorMap tm_dt;   // (D, L, B) input dtype, box (DT, T_SUB + 2, 1)
-  CUtensorMap tm_tab;  // (4N, L, B) f32, box (4N, T_SUB + 1, 1)
+  CUtensorMap tm_tab;  // (4N, L, B) f32, box (4N, T_SUB + 1, 1); rows over 256 floats (zero-order
+                       // hold at N = 64): (256, rows / 256, L, B), box (256, rows / 256, T_SUB + 1, 1)
   CUtensorMap tm_aux;  // (8, L, B) f32, box (8, T_SUB + 1, 1)
   CUtensorMap tm_rot;  // (2N, 4S, B) f32, box (2N, 4, 1)
   const float* A;
@@ -454,7 +455,10 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
     mbar_arrive_expect_tx(&full_bar[slot], uint32_t(SG::TX_BYTES));
     tma_load_3d(base + SG::OFF_X, &p.tm_x, d0, sub * T_SUB, b, &full_bar[slot]);
     tma_load_3d(base + SG::OFF_DT, &p.tm_dt, d0, sub * T_SUB, b, &full_bar[slot]);
-    tma_load_3d(base + SG::OFF_TAB, &p.tm_tab, 0, sub * T_SUB, b, &full_bar[slot]);
+    if constexpr (SG::TABW * N > 256)   // the row as (256, TABW N / 256): a box is at most 256 wide
+      tma_load_4d(base + SG::OFF_TAB, &p.tm_tab, 0, 0, sub * T_SUB, b, &full_bar[slot]);
+    else
+      tma_load_3d(base + SG::OFF_TAB, &p.tm_tab, 0, sub * T_SUB, b, &full_bar[slot]);
     if (MODE == 1) tma_load_3d(base + SG::OFF_AUX, &p.tm_aux, 0, sub * T_SUB, b, &full_bar[slot]);
     tma_load_3d(base + SG::OFF_ROT, &p.tm_rot, 0, 4 * sub, b, &full_bar[slot]);
   };

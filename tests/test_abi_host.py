@@ -52,7 +52,6 @@ def call(lib, B=1, L=64, D=16, N=8, mode=0, dtype=0, x=A16, lam=A16, y=A16, opts
 
 def test_rejects_bad_arguments_on_host(lib):
     assert call(lib, mode=3) == csscan.CSSCAN_ERR_INVALID_ARG
-    assert call(lib, mode=2, N=64) == csscan.CSSCAN_ERR_UNSUPPORTED   # zero-order hold: N <= 32
     assert call(lib, dtype=7) == csscan.CSSCAN_ERR_INVALID_ARG
     assert call(lib, B=-1) == csscan.CSSCAN_ERR_INVALID_ARG
     assert call(lib, N=0) == csscan.CSSCAN_ERR_INVALID_ARG

@@ -169,11 +169,11 @@ def test_lookback_timeout_is_reported(carry):
 
 
 # ---------------------------------------------------------------------------- zero-order hold
-@pytest.mark.parametrize("N", [2, 4, 8, 16, 32])
+@pytest.mark.parametrize("N", [2, 4, 8, 16, 32, 64])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_zoh_shapes(N, dtype):
     """Mode 2 (the scan kernel's zero-order-hold step; the small rows run as decoupled time
-    chunks) on ragged shapes."""
+    chunks) on ragged shapes. At N = 64 a table row (8 N floats) is copied as two 256-wide boxes."""
     base = wl.WORKLOADS["zoh_bf16_batch"]
     for (B, L, D) in [(1, 1, 8), (2, 13, 8), (1, 95, 24), (2, 300, 72)]:
         w = base.with_shape(B=B, L=L, D=D, N=N, dtype=dtype, seed=base.seed + 13 * N + L)
@@ -206,11 +206,15 @@ def test_zoh_rejected_where_unsupported():
     with pytest.raises(csscan.CsscanError) as e:
         csscan.csscan_backward(*args, torch.zeros_like(y), 2)
     assert e.value.status == csscan.CSSCAN_ERR_UNSUPPORTED
-    w64 = w.with_shape(N=64)
-    dev64 = gu.to_device(wl.generate(w64))
-    rc = csscan.csscan_forward_ex(dev64["x"], dev64["delta"], dev64["A"], dev64["Bc"], dev64["Cc"], dev64["theta"],
-                                  None, dev64["Dskip"], y, 2)
-    assert rc == csscan.CSSCAN_ERR_UNSUPPORTED
+
+
+def test_zoh_n64_rows_rich():
+    """N = 64 zero-order hold with enough rows for serial chunks (the two-box table rows on every
+    stage of the ring), sampled rows against the oracle."""
+    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=4, L=200, D=1536, N=64)
+    inp = wl.generate(w)
+    check(inp, gu.run_gpu(gu.to_device(inp), w.mode), "zoh:N64:rows", b_rows=[0, 3],
+          d_rows=np.array([0, 7, 777, 1535]))
 
 
 FULL = ["euler_f32_mamba1", "trap_bf16_mamba3", "euler_bf16_long", "trap_bf16_batch", "zoh_bf16_batch"]

@@ -72,6 +72,7 @@ CASES = [
     ("rich-zoh-bf16", "zoh_bf16_batch", dict(B=16, L=160, D=2560)),
     ("mid-zoh-f32", "zoh_bf16_batch", dict(B=2, L=333, D=48, dtype="f32")),
     ("long-zoh-bf16", "zoh_bf16_batch", dict(B=1, L=3000, D=24)),
+    ("mid-zoh-n64-f32", "zoh_bf16_batch", dict(B=2, L=333, D=48, N=64, dtype="f32")),
 ]
 
 
