@@ -87,6 +87,7 @@ def parse_args(argv=None):
     p.add_argument("--config-steps", type=int, default=20, help="timed steps of each per-config entry")
     p.add_argument("--batch", type=int, default=0, help="override the workload's B (smaller profiling cases)")
     p.add_argument("--length", type=int, default=0, help="override the workload's L (smaller profiling cases)")
+    p.add_argument("--states", type=int, default=0, help="override the workload's N (other state sizes)")
     return p.parse_args(argv)
 
 
@@ -94,7 +95,7 @@ def selected_workload(args):
     """The workload named by --workload, with --batch / --length applied."""
     table = wl.MIMO_WORKLOADS if args.workload in wl.MIMO_WORKLOADS else wl.WORKLOADS
     w = table[args.workload]
-    kw = {k: v for k, v in (("B", args.batch), ("L", args.length)) if v}
+    kw = {k: v for k, v in (("B", args.batch), ("L", args.length), ("N", args.states)) if v}
     return w.with_shape(**kw) if kw else w
 
 
@@ -664,7 +665,7 @@ def run_ours(args):
     hbm_achieved = w.min_bytes() / scan_s / 1e9
     roofline = {"bound": "hbm", "achieved": hbm_achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": hbm_achieved / hbm_peak,
-                "traffic": None if (args.batch or args.length) else traffic_from_profiles(w.name, kernel),
+                "traffic": None if (args.batch or args.length or args.states) else traffic_from_profiles(w.name, kernel),
                 "kernel": kernel, "ms_per_launch": 1e3 * scan_s, "peak_kind": peak_kind,
                 "frac_of_nominal": hbm_achieved / HBM_NOMINAL_GBS, "nominal_peak": HBM_NOMINAL_GBS,
                 "algorithmic_bytes_per_launch": w.min_bytes(),

@@ -53,6 +53,9 @@ struct Args {
   const void *x_prev, *Bc_prev;
   int64_t B, L, D, N;
   int mode, dtype;
+  // the zero-order-hold scan of a part of the states (forward_launch.cuh splits N > 16 into
+  // 16-state parts): N of the whole problem (0: N) and the part's first state
+  int64_t n_full = 0, n_off = 0;
 };
 
 struct MimoArgs {

@@ -136,6 +136,8 @@ struct TableParams {
   int planes;  // nscan table only: planes per row (Bt, Ct, and -Bt when 3)
   int plane_w; // nscan table only: floats per plane (2N plus padding)
   uint32_t* hdr;   // workspace header (error word of bounds-checked builds)
+  int n_full;  // scan table only: states per (b, t) row of Bc, Cc and theta (N of the whole problem)
+  int n_off;   // scan table only: first state of this part (the tables hold states n_off .. n_off + N - 1)
 };
 
 template <typename Tin, int MODE>
@@ -160,7 +162,7 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
   const unsigned gmask = p.N >= 32 ? 0xffffffffu : (((1u << p.N) - 1u) << ((threadIdx.x & 31) & ~(p.N - 1)));
   const Tin* lam = static_cast<const Tin*>(p.lam);
   for (int t = t0; t < t1; ++t) {
-    const int64_t tn = (int64_t(b) * p.L + t) * p.N + n;
+    const int64_t tn = (int64_t(b) * p.L + t) * p.n_full + p.n_off + n;   // this state in the inputs
     phi += load_in<Tin>(th, tn);
     sincosf(phi, &sn, &cs);
     if (((t - t0) & 7) == 7) {
@@ -232,8 +234,7 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
 struct ScanParams {
   CUtensorMap tm_x;    // (D, L, B) input dtype, box (DT, T_SUB + 1, 1)
   CUtensorMap tm_dt;   // (D, L, B) input dtype, box (DT, T_SUB + 2, 1)
-  CUtensorMap tm_tab;  // (4N, L, B) f32, box (4N, T_SUB + 1, 1); rows over 256 floats (zero-order
-                       // hold at N = 64): (256, rows / 256, L, B), box (256, rows / 256, T_SUB + 1, 1)
+  CUtensorMap tm_tab;  // (TABW N, L, B) f32, box (TABW N, T_SUB + 1, 1)
   CUtensorMap tm_aux;  // (8, L, B) f32, box (8, T_SUB + 1, 1)
   CUtensorMap tm_rot;  // (2N, 4S, B) f32, box (2N, 4, 1)
   const float* A;
@@ -256,6 +257,9 @@ struct ScanParams {
   long long poll_limit;
   float4* ckpt;         // checkpoint variant: (B, S8, D, N/2) state pairs before every 8-step segment
   int S8;               // ceil(L / 8)
+  // scan_kernel, a part of the states of a larger problem: N states n_off .. n_off + N - 1 of
+  // n_full (the row length of A, h0 and h_last)
+  int n_full, n_off;
 };
 
 __device__ __forceinline__ bool flag_ready(uint32_t f, uint32_t epoch, uint32_t need) {
@@ -366,7 +370,9 @@ __device__ __forceinline__ void zoh_update(float2& kr, float2& ki, float2 r, flo
   ki = fma2(r, ki, mul2(sw, mi));
 }
 
-template <int N, typename Tin, int MODE, int CARRY, bool CKPT = false>
+// ACC = true: a later part of a state split (see ScanParams::n_off): this part's Re(sum_n Cc h)
+// is added to y, which an earlier part wrote together with the Dskip term.
+template <int N, typename Tin, int MODE, int CARRY, bool CKPT = false, bool ACC = false>
 __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant__ ScanParams p) {
   using TL = Tile<N>;
   using SG = Stage<N, Tin, MODE>;
@@ -455,10 +461,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
     mbar_arrive_expect_tx(&full_bar[slot], uint32_t(SG::TX_BYTES));
     tma_load_3d(base + SG::OFF_X, &p.tm_x, d0, sub * T_SUB, b, &full_bar[slot]);
     tma_load_3d(base + SG::OFF_DT, &p.tm_dt, d0, sub * T_SUB, b, &full_bar[slot]);
-    if constexpr (SG::TABW * N > 256)   // the row as (256, TABW N / 256): a box is at most 256 wide
-      tma_load_4d(base + SG::OFF_TAB, &p.tm_tab, 0, 0, sub * T_SUB, b, &full_bar[slot]);
-    else
-      tma_load_3d(base + SG::OFF_TAB, &p.tm_tab, 0, sub * T_SUB, b, &full_bar[slot]);
+    tma_load_3d(base + SG::OFF_TAB, &p.tm_tab, 0, sub * T_SUB, b, &full_bar[slot]);
     if (MODE == 1) tma_load_3d(base + SG::OFF_AUX, &p.tm_aux, 0, sub * T_SUB, b, &full_bar[slot]);
     tma_load_3d(base + SG::OFF_ROT, &p.tm_rot, 0, 4 * sub, b, &full_bar[slot]);
   };
@@ -472,10 +475,10 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   for (int ch = 0; ch < CH; ++ch)
 #pragma unroll
     for (int q = 0; q < NPAIR; ++q)
-      Ap[ch][q] = dvalid ? f2(p.A[int64_t(chan(ch)) * p.N + n0 + 2 * q] * LOG2E_F,
-                              p.A[int64_t(chan(ch)) * p.N + n0 + 2 * q + 1] * LOG2E_F)
+      Ap[ch][q] = dvalid ? f2(p.A[int64_t(chan(ch)) * p.n_full + p.n_off + n0 + 2 * q] * LOG2E_F,
+                              p.A[int64_t(chan(ch)) * p.n_full + p.n_off + n0 + 2 * q + 1] * LOG2E_F)
                          : f2(0.f, 0.f);
-  const float2 Ds = dvalid ? f2(p.Dskip[chan(0)], p.Dskip[chan(1)]) : f2(0.f, 0.f);
+  const float2 Ds = (dvalid && !ACC) ? f2(p.Dskip[chan(0)], p.Dskip[chan(1)]) : f2(0.f, 0.f);
 
   // trapezoid halo: k at the chunk start is h_in + p_tc Bc_{tc-1}, p_tc = (1-lam_tc) dt_tc x_{tc-1}
   float2 halo_p = f2(0.f, 0.f);
@@ -531,9 +534,12 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   auto finish_y = [&](float2 yp, const StepIn& sc, float* yrow, bool ok) {
     if (CKPT) return;
     if (NG == 1) {
-      const float o0 = fmaf(Ds.x, sc.x.x, fmaf(-sc.pc.x, sc.E, yp.x));
-      const float o1 = fmaf(Ds.y, sc.x.y, fmaf(-sc.pc.y, sc.E, yp.y));
-      if (ok && dvalid) {
+      float o0 = fmaf(Ds.x, sc.x.x, fmaf(-sc.pc.x, sc.E, yp.x));
+      float o1 = fmaf(Ds.y, sc.x.y, fmaf(-sc.pc.y, sc.E, yp.y));
+      if (ACC && ok && dvalid) {   // reductions (nothing waits for them); parts run in stream order
+        atomicAdd(yrow, o0);
+        atomicAdd(yrow + 1, o1);
+      } else if (ok && dvalid) {
         if (p.y_vec2) {
           __stcs(reinterpret_cast<float2*>(yrow), f2(o0, o1));
         } else {
@@ -547,7 +553,10 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
 #pragma unroll
       for (int o = 2; o < NG; o <<= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
       const float o = fmaf(Ds.x, sc.x.x, fmaf(-sc.pc.x, sc.E, keep));
-      if (ok && store_one) __stcs(yrow + g, o);
+      if (ok && store_one) {
+        if (ACC) atomicAdd(yrow + g, o);   // a reduction: nothing waits for it
+        else __stcs(yrow + g, o);
+      }
     }
   };
 
@@ -766,7 +775,7 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
   bool incl_published = false;
   const bool has_h0 = (p.h0 != nullptr) && dvalid;
   auto h0rec = [&](int ch) {
-    return reinterpret_cast<const float2*>(p.h0) + (int64_t(b) * p.D + chan(ch)) * p.N + n0;
+    return reinterpret_cast<const float2*>(p.h0) + (int64_t(b) * p.D + chan(ch)) * p.n_full + p.n_off + n0;
   };
 
   if (CARRY == CARRY_DECOUPLED && pass1) {
@@ -950,7 +959,8 @@ __global__ void __launch_bounds__(THREADS, 2) scan_kernel(const __grid_constant_
     if (c == p.n_chunks - 1 && p.h_last != nullptr && dvalid) {
 #pragma unroll
       for (int ch = 0; ch < CH; ++ch)
-        store_states(reinterpret_cast<float2*>(p.h_last) + (int64_t(b) * p.D + chan(ch)) * p.N + n0, kr[ch], ki[ch]);
+        store_states(reinterpret_cast<float2*>(p.h_last) + (int64_t(b) * p.D + chan(ch)) * p.n_full + p.n_off + n0,
+                     kr[ch], ki[ch]);
     }
   } else {
     // a tile copy never arrived: report, drain what is still in flight (bounded), leave
