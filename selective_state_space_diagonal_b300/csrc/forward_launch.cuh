@@ -411,12 +411,14 @@ int forward_dispatch(const Args& a, const csscan_options_t& o, cudaStream_t st, 
   int dev = 0, nsm = 0;
   CSSCAN_CUDA(cudaGetDevice(&dev));
   CSSCAN_CUDA(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev));
-  // states per thread: 16 where the (b, d) rows give enough threads; 8 (two lanes per channel,
-  // twice the threads) for N = 32 rows that would leave the SMs under 8 warps each, and for N = 16
-  // rows under 2 warps per SM on short sequences, whose decoupled chunks would otherwise be too
-  // short to amortise their look-back
+  // states per thread: 16 where the (b, d) rows give enough threads or the sequence is long
+  // enough for decoupled chunks to supply them; 8 (two lanes per channel, twice the threads) for
+  // N = 32 rows that would leave the SMs under 8 warps each, and for N = 16 rows under 2 warps per
+  // SM, on sequences whose decoupled chunks would otherwise be too short to amortise their
+  // look-back (measured on B, L, D = 1, 131072, 1024: N = 32 at 16 states per thread 2.5 ms, at 8
+  // states 3.4 ms)
   const int64_t rows = a.B * a.D;
-  const bool wide32 = 2 * rows >= int64_t(nsm) * 32 * RESIDENT_WARPS_PER_SM;
+  const bool wide32 = 2 * rows >= int64_t(nsm) * 32 * RESIDENT_WARPS_PER_SM || a.L > 16384;
   const bool wide16 = rows >= int64_t(nsm) * 64 || a.L > 16384;
   if (a.mode == CSSCAN_MODE_EXP_EULER) {
     switch (a.N) {
