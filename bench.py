@@ -63,6 +63,8 @@ ZOH_ALU_OPS_PER_ELEM = ALU_OPS_PER_ELEM[2]
 # its reverse step: adjoint 2, Re(conj(Bt) gamma) 2, rho = r gamma 2, G(z) = rho conj(g) 4,
 # A Re G(z) 1, dA 1, dtheta 1, dBc 2, dCc 2 and the pair sum 0.5. (Time chunks add ~5 per element
 # for the chunk carries; not counted.)
+# (The zero-order hold's backward runs the absolute-frame path with its complex per-element
+# weight and derivative; no count is given for it.)
 BWD_ALU_OPS_PER_ELEM = {0: 31, 1: 31}
 FP32_LANES_PER_SM = 128
 # nominal HBM3e bandwidth of the part (the measured copy peak is the roofline's denominator;
@@ -650,7 +652,7 @@ def run_ours(args):
     e2e_s = reduce_max(time.perf_counter() - t0)
     e2e_value = aggregate_value(w.elements, e2e_steps, world, e2e_s)
 
-    bwd = None if (args.no_backward or w.mode == wl.MODE_ZOH) else measure_backward(w, dev, stream,
+    bwd = None if args.no_backward else measure_backward(w, dev, stream,
                                                                                    max(1, args.backward_steps))
 
     if rank != 0:
@@ -695,7 +697,8 @@ def run_ours(args):
         ms = bwd.pop("ms")
         gbs = bwd["min_bytes"] / (ms / 1e3) / 1e9
         bwd.update({"ms_per_step": ms, "value": w.elements / (ms / 1e3) / 1e9, "unit": UNIT,
-                    "alu": alu_roofline(BWD_ALU_OPS_PER_ELEM[w.mode], w.elements, ms / 1e3, clk),
+                    "alu": (alu_roofline(BWD_ALU_OPS_PER_ELEM[w.mode], w.elements, ms / 1e3, clk)
+                            if w.mode in BWD_ALU_OPS_PER_ELEM else None),
                     "hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak}})
         line["backward"] = bwd
     if world == 1 and not args.no_per_config:

@@ -86,8 +86,8 @@ enum {
  *   EXP_TRAPEZOID beta_t = (1 - lam_t) dt_t a_t on Bc_{t-1} x_{t-1}, gamma_t = lam_t dt_t
  *   ZOH           gamma_t = dt_t (e^{z_t} - 1) / z_t with z_t = dt_t A + i theta_t (the table's
  *                 A^{-1}(exp(dt A) - I) with the complex exponent of a_t in place of dt A);
- *                 the scans (csscan_forward, _ex, _state, _noalloc; every N) and
- *                 csscan_decode_step; csscan_backward returns CSSCAN_ERR_UNSUPPORTED for it */
+ *                 the scans (csscan_forward, _ex, _state, _noalloc; every N),
+ *                 csscan_decode_step and csscan_backward (N <= 32); not the MIMO scan */
 typedef enum { CSSCAN_MODE_EXP_EULER = 0, CSSCAN_MODE_EXP_TRAPEZOID = 1, CSSCAN_MODE_ZOH = 2 } csscan_mode_t;
 typedef enum { CSSCAN_F32 = 0, CSSCAN_BF16 = 1 } csscan_dtype_t;
 
@@ -221,7 +221,8 @@ int csscan_forward_mimo(const void* x, const void* delta, const float* A, const 
  *   dtheta     : (B, L, N)          dlambda : (B, L), trapezoid mode only (may be NULL in exp-Euler mode)
  * Inputs need their element alignment, Bc and Cc that of one complex entry (no 16-byte rule;
  * inputs that also meet csscan_forward's 16-byte rule let the library take the checkpoints from
- * the scan kernel, otherwise from a slower pass of its own). N must be 2, 4, 8, 16 or 32
+ * the scan kernel, otherwise from a slower pass of its own; the zero-order hold, whose
+ * injection weight is complex per element, always takes the slower path). N must be 2, 4, 8, 16 or 32
  * (CSSCAN_ERR_UNSUPPORTED otherwise) and B <= 65535. The library grows its per-stream
  * workspace to B*L*N*8 + B*ceil(L/8)*D*N*8 bytes (rotation table and checkpoints). Sums over
  * rows use float32 atomic adds, so the summed gradients (dA, dBc, dCc, dtheta, dlambda,

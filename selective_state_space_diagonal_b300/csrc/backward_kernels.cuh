@@ -13,6 +13,11 @@
 //   injection      exp-Euler:  u_t = dt_t x_t Bc_t
 //                  trapezoid:  u_t = lam_t dt_t x_t Bc_t + (1-lam_t) dt_t x_{t-1} a_t Bc_{t-1}
 //                  with P_t = Re(conj(Bc_t) ghat_t) and R_t = Re(conj(a_t Bc_{t-1}) ghat_t)
+//                  zero-order hold: u_t = x_t gam_t Bc_t, gam_t = dt_t E(z_t), E(z) = (e^z - 1) / z
+//                  ("Mamba-3 paper story", discretisation table, row ZOH, with the complex
+//                  exponent): G(gam) = x conj(Bc) ghat, dBc += x conj(gam) ghat,
+//                  dx += Re(conj(gam Bc) ghat), ddt += Re(conj(E) G(gam)) and
+//                  G(z) += conj(E'(z)) dt G(gam)
 //   output         dCc_t += dy_t conj(h_t),  dx_t += Dskip dy_t,  dDskip += dy_t x_t
 //
 // The sequence is cut into C chunks of TC steps so that all chunks run at once. Both sweeps are
@@ -32,7 +37,8 @@
 //                     inputs do not meet the tile-copy rules of the scan kernel, whose
 //                     checkpoint variant otherwise writes every segment's entry state and makes
 //                     chunk_fwd_kernel and this pass unnecessary);
-//   grad_kernel   a thread owns one state n of K = 4 channels of one batch row. For each segment,
+//   grad_kernel   a thread owns one state n of K = 4 channels of one batch row.
+//                 (This path also serves every zero-order-hold backward, whatever the alignment.) For each segment,
 //                 last to first, and each of its channels it recomputes the segment's SEG states
 //                 from the checkpoint into registers, then walks the segment backwards. Sums over
 //                 n (dx, ddt, dlam) use a butterfly over the N lanes of a channel; sums over d
@@ -68,6 +74,7 @@ struct Params {
   float* dlam;         // (B, L)         accumulated (trapezoid only)
   float* dD;           // (D)            accumulated
   const float2* rot;   // (B, L, N)      e^{i theta}
+  const void* theta;   // (B, L, N)      theta (zero-order hold: z = dt A + i theta)
   float2* ckpt;        // (B, S, D, N)   state before segment s (s >= 1)
   float2* chunk;       // (B, C, D, N, 5) per chunk: U | h_in, P, W | ghat_first, Q, conj(a_tc)
   int B, L, D, N, S;
@@ -92,20 +99,58 @@ __global__ void __launch_bounds__(256) rot_kernel(const void* theta, float2* rot
   rot[i] = make_float2(c, s);
 }
 
+// Zero-order hold: E(z) = (e^z - 1) / z (gam = dt E) and, with DERIV, E'(z) = (e^z - E(z)) / z,
+// for z = v + i th with (c, s) = (cos th, sin th). Where |z| < 0.05 both come from their power
+// series, sum z^k / (k+1)! and sum (k+1) z^k / (k+2)!, to z^4 (the first omitted terms are below
+// 5e-10 relative); elsewhere from the closed forms, with e^z - 1 = (e^v - 1) c + (c - 1) + i e^v s
+// formed without cancellation (c - 1 = -s^2 / (1 + c) where c > 0).
+template <bool DERIV>
+__device__ __forceinline__ void zoh_factor(float v, float th, float c, float s, float2& E, float2& dE) {
+  const float z2 = fmaf(v, v, th * th);
+  if (z2 < 0.0025f) {
+    const float k1[5] = {1.f, 1.f / 2.f, 1.f / 6.f, 1.f / 24.f, 1.f / 120.f};
+    const float k2[5] = {1.f / 2.f, 1.f / 3.f, 1.f / 8.f, 1.f / 30.f, 1.f / 144.f};
+    float er = k1[4], ei = 0.f, dr = k2[4], di = 0.f;
+#pragma unroll
+    for (int k = 3; k >= 0; --k) {   // Horner: p <- p z + coefficient
+      const float nr = fmaf(er, v, fmaf(-ei, th, k1[k])), ni = fmaf(er, th, ei * v);
+      er = nr;
+      ei = ni;
+      if (DERIV) {
+        const float mr = fmaf(dr, v, fmaf(-di, th, k2[k])), mi = fmaf(dr, th, di * v);
+        dr = mr;
+        di = mi;
+      }
+    }
+    E = make_float2(er, ei);
+    dE = make_float2(dr, di);
+  } else {
+    const float em1 = expm1f(v), ev = em1 + 1.f;
+    const float cm1 = c > 0.f ? -s * s / (1.f + c) : c - 1.f;
+    const float nr = fmaf(em1, c, cm1), ni = ev * s;   // e^z - 1
+    const float inv = 1.f / z2;                        // 1 / z = (v - i th) / |z|^2
+    E = make_float2(fmaf(nr, v, ni * th) * inv, fmaf(ni, v, -nr * th) * inv);
+    if (DERIV) {
+      const float dr = fmaf(ev, c, -E.x), di = fmaf(ev, s, -E.y);   // e^z - E
+      dE = make_float2(fmaf(dr, v, di * th) * inv, fmaf(di, v, -dr * th) * inv);
+    }
+  }
+}
+
 // The forward recurrence of one (b, d, n) over groups of SEG steps: every load of a group is
 // issued before its arithmetic, so that the group's memory latencies overlap.
 template <typename Tin, int MODE>
 struct FwdStep {
-  const Tin *X, *DT, *BC, *LAM;
+  const Tin *X, *DT, *BC, *LAM, *TH;
   const float2* rot;
   long long b;
   int L, D, N, d, n;
-  float a2;
+  float a2, A;
   // steps t0 .. min(t0 + SEG, te) - 1: h <- a_t h + u_t; xp, bpr, bpi hold x_{t-1}, Bc_{t-1}
   // (trapezoid) and advance; P (if given) is multiplied by every a_t
   __device__ __forceinline__ void group(int t0, int te, float& hr, float& hi, float& xp, float& bpr, float& bpi,
                                         float* Pr = nullptr, float* Pi = nullptr) const {
-    float xs[SEG], ds[SEG], brs[SEG], bis[SEG], ls[SEG];
+    float xs[SEG], ds[SEG], brs[SEG], bis[SEG], ls[SEG], ths[SEG];
     float2 ros[SEG];
     // one 64-bit base per array for the group; steps past te - 1 repeat the last one
     const long long bt = b * L + t0;
@@ -124,6 +169,7 @@ struct FwdStep {
       brs[i] = bb.x;
       bis[i] = bb.y;
       ls[i] = MODE == 1 ? load_in<Tin>(LAM, bt + ii) : 0.f;
+      ths[i] = MODE == 2 ? load_in<Tin>(TH, (bt + ii) * N + n) : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < SEG; ++i) {
@@ -135,6 +181,13 @@ struct FwdStep {
           const float w = ds[i] * xs[i];
           ur = w * brs[i];
           ui = w * bis[i];
+        } else if (MODE == 2) {
+          float2 E, dE;
+          zoh_factor<false>(ds[i] * A, ths[i], ros[i].x, ros[i].y, E, dE);
+          const float w = ds[i] * xs[i];
+          const float gr = w * E.x, gi = w * E.y;   // x gam
+          ur = fmaf(gr, brs[i], -gi * bis[i]);
+          ui = fmaf(gr, bis[i], gi * brs[i]);
         } else {
           const float w = ls[i] * ds[i] * xs[i], c2 = (1.f - ls[i]) * ds[i] * xp;
           ur = w * brs[i] + c2 * (ar * bpr - ai * bpi);
@@ -174,6 +227,7 @@ __device__ __forceinline__ FwdStep<Tin, MODE> fwd_step(const Params& p, long lon
   f.DT = static_cast<const Tin*>(p.dt);
   f.BC = static_cast<const Tin*>(p.Bc);
   f.LAM = static_cast<const Tin*>(p.lam);
+  f.TH = static_cast<const Tin*>(p.theta);
   f.rot = p.rot;
   f.b = b;
   f.L = p.L;
@@ -181,7 +235,8 @@ __device__ __forceinline__ FwdStep<Tin, MODE> fwd_step(const Params& p, long lon
   f.N = p.N;
   f.d = d;
   f.n = n;
-  f.a2 = p.A[(long long)d * p.N + n] * LOG2E;
+  f.A = p.A[(long long)d * p.N + n];
+  f.a2 = f.A * LOG2E;
   return f;
 }
 
@@ -357,14 +412,15 @@ template <int N> struct GradStage {
   static constexpr int OFF_TR = OFF_TQ + (SEG + 2) * CB * 16;             // float4 [SEG+2][CB]
   static constexpr int OFF_TN = OFF_TR + (SEG + 2) * CB * 16;             // float4 [SEG+1][N]: rot c, s, Bc re, im
   static constexpr int OFF_CC = OFF_TN + (SEG + 1) * N * 16;              // float2 [SEG+1][N]: Cc re, im
-  static constexpr int BYTES = OFF_CC + (SEG + 1) * N * 8;
+  static constexpr int OFF_TH = OFF_CC + (SEG + 1) * N * 8;               // float [SEG+1][N]: theta (zero-order hold)
+  static constexpr int BYTES = OFF_TH + (SEG + 1) * N * 4;
 };
 
 // Resident blocks per SM that grad_kernel is compiled for. Five (96 registers) hides more
 // latency than four for every shape but the N = 32 trapezoid, where the 96-register cap
 // spills inside the butterfly and four (128 registers) is faster.
 template <int MODE, int N> struct GradOcc {
-  static constexpr int MIN_BLOCKS = MODE == 1 && N == 32 ? 4 : 5;
+  static constexpr int MIN_BLOCKS = (MODE == 1 && N == 32) || MODE == 2 ? 4 : 5;
 };
 
 template <typename Tin, int MODE, int N>
@@ -389,6 +445,7 @@ __global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_ke
   float4 (*s_tr)[CB] = reinterpret_cast<float4 (*)[CB]>(g_stage + GS::OFF_TR);
   float4 (*s_tn)[N] = reinterpret_cast<float4 (*)[N]>(g_stage + GS::OFF_TN);
   float2 (*s_cc)[N] = reinterpret_cast<float2 (*)[N]>(g_stage + GS::OFF_CC);
+  float (*s_th)[N] = reinterpret_cast<float (*)[N]>(g_stage + GS::OFF_TH);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = lane % N, cl = lane / N;
@@ -403,6 +460,7 @@ __global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_ke
   const Tin* BC = static_cast<const Tin*>(p.Bc);
   const Tin* CC = static_cast<const Tin*>(p.Cc);
   const Tin* LAM = static_cast<const Tin*>(p.lam);
+  const Tin* TH = static_cast<const Tin*>(p.theta);
   const long long L = p.L, D = p.D;
 
   // the adjoint entering from the next chunk: carry = conj(a_te) ghat_te and R_te
@@ -463,14 +521,17 @@ __global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_ke
       const long long t = ts - 1 + r;
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
       float2 c = make_float2(0.f, 0.f);
+      float th = 0.f;
       if (t >= 0 && t < L) {
         const long long tn = (b * L + t) * N + nn;
         const float2 ro = p.rot[tn];
         v = make_float4(ro.x, ro.y, load_in<Tin>(BC, 2 * tn), load_in<Tin>(BC, 2 * tn + 1));
         c = make_float2(load_in<Tin>(CC, 2 * tn), load_in<Tin>(CC, 2 * tn + 1));
+        if (MODE == 2) th = load_in<Tin>(TH, tn);
       }
       s_tn[r][nn] = v;
       s_cc[r][nn] = c;
+      s_th[r][nn] = th;
     }
     __syncthreads();
 
@@ -530,6 +591,13 @@ __global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_ke
               const float w = dtt * xt;
               ur = w * q.z;
               ui = w * q.w;
+            } else if (MODE == 2) {
+              float2 E, dE;
+              zoh_factor<false>(dtt * Ad, s_th[i + 1][n], q.x, q.y, E, dE);
+              const float w = dtt * xt;
+              const float gr = w * E.x, gi = w * E.y;   // x gam
+              ur = fmaf(gr, q.z, -gi * q.w);
+              ui = fmaf(gr, q.w, gi * q.z);
             } else {
               const float4 qp = s_tn[i][n];
               const float4 q2 = s_tq[i + 1][cb];
@@ -578,12 +646,25 @@ __global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_ke
           float Gai = gi * hpr - gr * hpi;
           const float P = br * gr + bi * gi;
           float R = 0.f, gx, gdt, glam = 0.f;
+          float zr = 0.f, zi = 0.f;   // zero-order hold: G(z) through gam's factor E(z)
           if (MODE == 0) {
             const float coef = dtt * xt;
             acc[i][0] = fmaf(coef, gr, acc[i][0]);
             acc[i][1] = fmaf(coef, gi, acc[i][1]);
             gx = dtt * P;
             gdt = xt * P;
+          } else if (MODE == 2) {
+            float2 E, dE;
+            zoh_factor<true>(dtt * Ad, s_th[i + 1][n], q.x, q.y, E, dE);
+            const float Pi = br * gi - bi * gr;        // conj(Bc) ghat = P + i Pi
+            const float mr = dtt * E.x, mi = dtt * E.y;  // gam
+            acc[i][0] = fmaf(xt, fmaf(mr, gr, mi * gi), acc[i][0]);   // dBc += x conj(gam) ghat
+            acc[i][1] = fmaf(xt, fmaf(mr, gi, -mi * gr), acc[i][1]);
+            gx = fmaf(mr, P, mi * Pi);                   // Re(conj(gam Bc) ghat)
+            gdt = xt * fmaf(E.x, P, E.y * Pi);            // Re(conj(E) G(gam)), G(gam) = x (P + i Pi)
+            const float k = dtt * xt;                     // conj(E') dt G(gam)
+            zr = k * fmaf(dE.x, P, dE.y * Pi);
+            zi = k * fmaf(dE.x, Pi, -dE.y * P);
           } else {
             const float4 q2 = s_tq[i + 1][cb];   // lam dt x, (1 - lam) dt, (1 - lam) dt x_{t-1}, lam dt
             const float4 q3 = s_tr[i + 1][cb];   // lam x, (1 - lam) x_{t-1}, dt x, dt x_{t-1}
@@ -604,8 +685,8 @@ __global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_ke
             mnext = q2.y;
           }
           // exponential: G(z) = conj(a) G(a)
-          const float Gzr = ar * Gar + ai * Gai;
-          const float Gzi = ar * Gai - ai * Gar;
+          const float Gzr = ar * Gar + ai * Gai + zr;
+          const float Gzi = ar * Gai - ai * Gar + zi;
           dA_acc = fmaf(dtt, Gzr, dA_acc);
           gdt = fmaf(Ad, Gzr, gdt);
           acc[i][4] += Gzi;

@@ -4,8 +4,9 @@
 //     with 16-byte (b, t) rows, 16-byte aligned dBc and dCc, 8-byte aligned dA and dtheta): the
 //     forward scan kernel's checkpoint variant, the chunk adjoints where the sequence is split,
 //     and ngrad_kernel (ngrad_kernels.cuh) in the rotating frame;
-//   launch_backward: every other input: checkpoints from ckpt_kernel and the absolute-frame
-//     grad_kernel (backward_kernels.cuh).
+//   launch_backward: every other input, and the zero-order hold (whose injection weight is
+//     complex per element): checkpoints from ckpt_kernel and the absolute-frame grad_kernel
+//     (backward_kernels.cuh).
 #pragma once
 
 #include "backward_kernels.cuh"
@@ -38,12 +39,30 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
   const size_t rot_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float2), 256);
   const size_t ckpt_bytes = align_up(size_t(a.B * S * a.D * N) * sizeof(float2), 256);
   const size_t chunk_bytes = C > 1 ? size_t(a.B * C * a.D * N) * 5 * sizeof(float2) : 0;
-  // checkpoints from ckpt_kernel (the inputs this path takes do not meet the tile-copy rules)
-  const bool fwd_ckpt = false;
+  // checkpoints: the zero-order hold on inputs that meet the forward scan's tile-copy rules takes
+  // them (every segment's entry state, chunk starts included) from the scan kernel's checkpoint
+  // variant, one pass at forward speed; every other input from ckpt_kernel
+  const int64_t s_in = a.dtype == CSSCAN_F32 ? 4 : 2;
+  const bool fwd_ckpt = MODE == 2 && aligned(a.x, 16) && aligned(a.delta, 16) && (a.D * s_in) % 16 == 0;
+  Args fa{a.x, a.delta, a.Bc, a.Cc, a.theta, a.lam, a.A, a.Dskip, nullptr, nullptr, nullptr, nullptr, nullptr,
+          a.B, a.L, a.D, N, a.mode, a.dtype};
+  const csscan_options_t fo = default_options();
+  Plan fpl;
+  size_t f_rest = 0, f_units = 1;
+  if constexpr (MODE == 2) {
+    if (fwd_ckpt) {
+      const int prc = make_plan(fa, fo, dev, RScan<N, Tin, 2, true>::shape(), &RScan<N, Tin, 2, true>::occ, &fpl);
+      if (prc != CSSCAN_OK) return prc;
+      f_rest = align_up(fpl.rest_bytes, 256);
+      f_units = size_t(fpl.n_units);
+    }
+  }
   WsEntry ws;
-  int rc = get_workspace(dev, st, 1, rot_bytes + ckpt_bytes + chunk_bytes, &ws);
+  int rc = get_workspace(dev, st, f_units, f_rest + rot_bytes + ckpt_bytes + chunk_bytes, &ws);
   if (rc != CSSCAN_OK) return rc;
-  char* rest = ws_rest(ws);
+  char* const ws_base = static_cast<char*>(ws.base);
+  char* const f_area = ws_rest(ws);   // the checkpoint scan's tables and carries (zero-order hold)
+  char* rest = f_area + f_rest;
 
   // gradients that are sums over several rows are accumulated and start at zero
   CSSCAN_CUDA(cudaMemsetAsync(a.dA, 0, size_t(a.D * N) * 4, st));
@@ -71,6 +90,7 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
   p.dlam = MODE == 1 ? a.dlam : nullptr;
   p.dD = a.dDskip;
   p.rot = reinterpret_cast<const float2*>(rest);
+  p.theta = a.theta;
   p.ckpt = reinterpret_cast<float2*>(rest + rot_bytes);
   p.chunk = C > 1 ? reinterpret_cast<float2*>(rest + rot_bytes + ckpt_bytes) : nullptr;
   p.B = int(a.B);
@@ -83,6 +103,14 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
   p.fwd_ckpt = fwd_ckpt ? 1 : 0;
 
   if (!grid_fits((long long)a.B * a.L * N) || !grid_fits((long long)a.B * C * a.D * N)) return CSSCAN_ERR_UNSUPPORTED;
+  if constexpr (MODE == 2) {
+    if (fwd_ckpt) {
+      rc = RScan<N, Tin, 2, true>::enqueue(fa, fo, fpl, reinterpret_cast<uint32_t*>(ws_base),
+                                           reinterpret_cast<uint32_t*>(ws_base + HDR_BYTES), f_area, st,
+                                           reinterpret_cast<float2*>(rest + rot_bytes), S);
+      if (rc != CSSCAN_OK) return rc;
+    }
+  }
   const long long n_rot = (long long)a.B * a.L * N;
   bwd::rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest), n_rot);
   CSSCAN_CUDA(cudaGetLastError());
@@ -324,14 +352,16 @@ inline bool backward_rot_takes(const BwdArgs& a) {
 
 template <typename Tin, int MODE>
 int dispatch_backward_n(const BwdArgs& a, cudaStream_t st) {
-  if (backward_rot_takes(a)) {
-    switch (a.N) {
-      case 2: return launch_backward_rot<Tin, MODE, 2>(a, st);
-      case 4: return launch_backward_rot<Tin, MODE, 4>(a, st);
-      case 8: return launch_backward_rot<Tin, MODE, 8>(a, st);
-      case 16: return launch_backward_rot<Tin, MODE, 16>(a, st);
-      case 32: return launch_backward_rot<Tin, MODE, 32>(a, st);
-      default: return CSSCAN_ERR_UNSUPPORTED;
+  if constexpr (MODE != 2) {   // the zero-order hold takes the absolute-frame path only
+    if (backward_rot_takes(a)) {
+      switch (a.N) {
+        case 2: return launch_backward_rot<Tin, MODE, 2>(a, st);
+        case 4: return launch_backward_rot<Tin, MODE, 4>(a, st);
+        case 8: return launch_backward_rot<Tin, MODE, 8>(a, st);
+        case 16: return launch_backward_rot<Tin, MODE, 16>(a, st);
+        case 32: return launch_backward_rot<Tin, MODE, 32>(a, st);
+        default: return CSSCAN_ERR_UNSUPPORTED;
+      }
     }
   }
   switch (a.N) {
@@ -346,6 +376,7 @@ int dispatch_backward_n(const BwdArgs& a, cudaStream_t st) {
 
 template <typename Tin>
 int backward_dispatch(const BwdArgs& a, cudaStream_t st) {
+  if (a.mode == 2) return dispatch_backward_n<Tin, 2>(a, st);
   return a.mode == 0 ? dispatch_backward_n<Tin, 0>(a, st) : dispatch_backward_n<Tin, 1>(a, st);
 }
 

@@ -233,8 +233,8 @@ int mimo_impl(const MimoArgs& a, cudaStream_t st) {
 }
 
 int backward_impl(const BwdArgs& a, cudaStream_t st) {
-  if (a.mode == CSSCAN_MODE_ZOH) return CSSCAN_ERR_UNSUPPORTED;
-  if (a.mode != CSSCAN_MODE_EXP_EULER && a.mode != CSSCAN_MODE_EXP_TRAPEZOID) return CSSCAN_ERR_INVALID_ARG;
+  if (a.mode != CSSCAN_MODE_EXP_EULER && a.mode != CSSCAN_MODE_EXP_TRAPEZOID && a.mode != CSSCAN_MODE_ZOH)
+    return CSSCAN_ERR_INVALID_ARG;
   if (a.dtype != CSSCAN_F32 && a.dtype != CSSCAN_BF16) return CSSCAN_ERR_INVALID_ARG;
   if (a.B < 0 || a.L < 0 || a.D < 0 || a.N <= 0) return CSSCAN_ERR_INVALID_ARG;
   // arrays with no elements may be NULL (an empty tensor has no storage)
@@ -435,8 +435,8 @@ const char* csscan_status_string(int status) {
     case CSSCAN_ERR_INVALID_ARG: return "invalid argument";
     case CSSCAN_ERR_MISALIGNED: return "misaligned pointer or row stride (x/delta need 16-byte alignment and D*sizeof(dtype) % 16 == 0)";
     case CSSCAN_ERR_UNSUPPORTED:
-      return "unsupported size or mode for this entry point (N in {2, 4, 8, 16, 32, 64}; N <= 32 for the backward, "
-             "which does not take the zero-order hold, and for the MIMO scan)";
+      return "unsupported size or mode for this entry point (N in {2, 4, 8, 16, 32, 64}; N <= 32 for the backward "
+             "and for the MIMO scan, which does not take the zero-order hold)";
     case CSSCAN_ERR_CUDA: return g_last_cuda_error[0] ? g_last_cuda_error : "CUDA error";
     case CSSCAN_ERR_LOOKBACK_TIMEOUT: return "a chunk's carry wait timed out on the device";
     case CSSCAN_ERR_PIPELINE_TIMEOUT: return "a tile copy did not arrive within its limit on the device";

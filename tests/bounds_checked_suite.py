@@ -30,8 +30,6 @@ def forward_cases() -> int:
     for mode in (0, 1, 2):
         for dtype in ("f32", "bf16"):
             for N in (2, 16, 32, 64):
-                if mode == 2 and N == 64:
-                    continue
                 w = base.with_shape(B=2, L=77, D=24, N=N, mode=mode, dtype=dtype,
                                     seed=0x5EED3000 + 7 * N + 3 * mode + (dtype == "bf16"))
                 inp = wl.generate(w)
@@ -64,7 +62,8 @@ def mimo_cases() -> int:
 def backward_cases() -> int:
     import test_backward_gpu as tb
     n = 0
-    for (D, N, mode, dtype) in ((24, 16, 1, "f32"), (40, 8, 0, "bf16"), (6, 8, 1, "f32")):   # D = 6: unaligned rows
+    for (D, N, mode, dtype) in ((24, 16, 1, "f32"), (40, 8, 0, "bf16"), (6, 8, 1, "f32"),   # D = 6: unaligned rows
+                                (24, 16, 2, "f32")):
         w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=2, L=77, D=D, N=N, mode=mode, dtype=dtype,
                                                        seed=0x5EED3200 + D + N)
         inp = wl.generate(w)

@@ -99,7 +99,7 @@ def compare(g: dict, r: dict, name: str, keys=GRADS):
 
 
 # ---------------------------------------------------------------------------- small cases
-SMALL = [(mode, dtype, N) for mode in (0, 1) for dtype in ("f32", "bf16") for N in (2, 4, 8, 16, 32)]
+SMALL = [(mode, dtype, N) for mode in (0, 1, 2) for dtype in ("f32", "bf16") for N in (2, 4, 8, 16, 32)]
 
 
 @pytest.mark.parametrize("mode,dtype,N", SMALL, ids=[f"m{m}-{d}-N{n}" for m, d, n in SMALL])
@@ -113,7 +113,7 @@ def test_backward_matches_oracle(mode, dtype, N):
     compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"m{mode}-{dtype}-N{N}")
 
 
-@pytest.mark.parametrize("name", [k for k, v in wl.WORKLOADS.items() if v.mode != wl.MODE_ZOH])
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
 def test_backward_workload_shapes(name):
     """Each benchmark workload's distributions, modes and N at a reduced size."""
     w0 = wl.WORKLOADS[name]
@@ -130,6 +130,21 @@ def test_backward_long_sequence():
     inp = wl.generate(w)
     dy = make_dy(w, seed=13)
     compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), "long")
+
+
+def test_backward_zoh_small_exponents_and_chunks():
+    """Zero-order hold with |z| = |dt A + i theta| around 1e-3 and below, where the weight E(z)
+    and its derivative come from their power series, and a longer sequence cut into time
+    chunks (the chunk passes run the held-input injection too)."""
+    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=2, L=90, D=40, N=8, dtype="f32", dt_lo=1e-5, dt_hi=1e-3,
+                                                  theta_max=1e-3)
+    inp = wl.generate(w)
+    dy = make_dy(w, seed=41)
+    compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), "zoh small z")
+    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=1, L=3000, D=8, N=16)
+    inp = wl.generate(w)
+    dy = make_dy(w, seed=43)
+    compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), "zoh long")
 
 
 def test_backward_single_step_and_short():
@@ -204,14 +219,14 @@ def test_backward_full_size_batch_workload():
 
 def test_backward_unchunked_row_rich():
     """Enough (b, d) rows to fill the GPU without time chunks: the single-chunk path."""
-    for mode in (0, 1):
+    for mode in (0, 1, 2):
         w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=16, L=21, D=5000, N=16, mode=mode, dtype="f32")
         inp = wl.generate(w)
         dy = make_dy(w, seed=19 + mode)
         compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"unchunked m{mode}")
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_backward_rows_the_tile_copies_cannot_take(mode):
     """Rows of D * sizeof(dtype) bytes that are not a multiple of 16 (float32 D = 6, bf16 D = 12):
     the checkpoints then come from the backward's own sequential pass instead of the scan

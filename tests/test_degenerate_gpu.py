@@ -77,7 +77,7 @@ def test_degenerate_forward(kind, mode):
 
 
 @pytest.mark.parametrize("kind", [k for k in KINDS if k != "zero_x"])
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_degenerate_backward(kind, mode):
     if kind.startswith("lam") and mode != 1:
         pytest.skip("lam only enters the trapezoid rule")

@@ -199,7 +199,8 @@ def test_zoh_one_chunk_and_small_exponents():
 
 
 def test_zoh_rejected_where_unsupported():
-    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=1, L=16, D=16, N=16, dtype="f32")
+    """The backward covers N <= 32 in every mode, the zero-order hold included."""
+    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=1, L=16, D=16, N=64, dtype="f32")
     dev = gu.to_device(wl.generate(w))
     y = torch.empty((1, 16, 16), device="cuda")
     args = (dev["x"], dev["delta"], dev["A"], dev["Bc"], dev["Cc"], dev["theta"], None, dev["Dskip"])
