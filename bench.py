@@ -929,6 +929,30 @@ def measure_mimo_config(label, name, args, stream, local, scratch, hbm_peak) -> 
     return rec
 
 
+def measure_mimo_backward(w, dev, stream, steps: int) -> dict:
+    """Time csscan_backward_mimo on the same inputs (seeded dy ~ N(0, 1) on the device), CUDA
+    events on the launching stream around each call, after one warm-up call."""
+    import torch
+    from selective_state_space_diagonal_b300 import csscan
+    g = torch.Generator(device="cuda")
+    g.manual_seed(0x5EED0000 + 98)
+    dy = torch.randn((w.B, w.L, w.H, w.P), dtype=torch.float32, device="cuda", generator=g)
+    args = (dev["x"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], dev["theta"], dev["lam"], dev["Dskip"], dy, w.mode)
+    out = csscan.csscan_backward_mimo(*args, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        csscan.csscan_backward_mimo(*args, stream=stream, out=out)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    del out, dy
+    return {"ms": ms, "steps": steps,
+            "note": "csscan_backward_mimo (checkpointed recompute, a thread per (b, head, state)), inputs resident, "
+                    "median of CUDA-event times"}
+
+
 def run_mimo(args):
     """The bench contract for a MIMO workload (csscan_forward_mimo): one step = one call."""
     import torch
@@ -981,6 +1005,7 @@ def run_mimo(args):
         y_host.copy_(y, non_blocking=True)
         stream.synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0)
+    bwd = None if args.no_backward else measure_mimo_backward(w, dev, stream, max(1, args.backward_steps))
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -1006,6 +1031,10 @@ def run_mimo(args):
             "e2e": {"value": aggregate_value(w.elements, e2e_steps, world, e2e_s), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": y.numel() * 4, "steps": e2e_steps},
             "gpu_launches": mimo_launches(w, nsm) * K, "clocks": t["clocks"]}
+    if bwd is not None:
+        ms = bwd.pop("ms")
+        bwd.update({"ms_per_step": ms, "value": w.elements / (ms / 1e3) / 1e9, "unit": UNIT})
+        line["backward"] = bwd
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

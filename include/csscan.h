@@ -234,6 +234,30 @@ int csscan_backward(const void* x, const void* delta, const float* A, const void
                     int64_t B, int64_t L, int64_t D, int64_t N, int mode, int dtype, cudaStream_t stream);
 
 /*
+ * Backward pass of csscan_forward_mimo (from the zero state): the gradients of
+ * l = sum_{b,t,h,p} dy[b,t,h,p] y[b,t,h,p] with respect to every input, by reverse-mode
+ * differentiation of the MIMO recurrence above, the states regenerated from checkpoints taken
+ * every 8 steps ("Complex parallel scan", sections 一个问题，两种命运 and 硬件落地的挑战).
+ *   x .. Dskip, B, L, H, P, N, mode, dtype : exactly as passed to csscan_forward_mimo
+ *   dy      : device float32 (B, L, H, P), the gradient of the loss with respect to y
+ * Outputs (device float32, caller-owned, fully written by the call, any alignment of 4 bytes):
+ *   dx : (B, L, H, P)   ddelta : (B, L, H)   dA : (H, N)   dDskip : (H, P)
+ *   dBm, dCm : (B, L, N, P, 2), (d/dRe, d/dIm) of each complex entry
+ *   dtheta : (B, L, N)   dlambda : (B, L), trapezoid mode only (may be NULL in exp-Euler mode)
+ * mode: CSSCAN_MODE_EXP_EULER or CSSCAN_MODE_EXP_TRAPEZOID (ZOH: CSSCAN_ERR_UNSUPPORTED). N must be
+ * 2, 4, 8, 16 or 32, P 1, 2, 4 or 8 and B <= 65535 (CSSCAN_ERR_UNSUPPORTED otherwise); pointers
+ * need their element alignment, Bm and Cm that of one complex entry. One thread walks the whole
+ * sequence of each (b, head, state), so the call is fastest with many heads. The library grows
+ * its per-stream workspace to B*L*N*8 + B*ceil(L/8)*H*N*8 bytes. Sums over rows use float32
+ * atomic adds (the summed gradients can differ in the last bits from run to run).
+ */
+int csscan_backward_mimo(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
+                         const void* theta, const void* lambda, const float* Dskip, const float* dy, float* dx,
+                         float* ddelta, float* dA, float* dBm, float* dCm, float* dtheta, float* dlambda,
+                         float* dDskip, int64_t B, int64_t L, int64_t H, int64_t P, int64_t N, int mode, int dtype,
+                         cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns the device-side status of the calls made on it since
  * the last query (CSSCAN_OK, CSSCAN_ERR_LOOKBACK_TIMEOUT or CSSCAN_ERR_PIPELINE_TIMEOUT), or
  * CSSCAN_ERR_CUDA if the stream reports an error. Clears the device status.

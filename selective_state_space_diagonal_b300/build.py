@@ -17,6 +17,7 @@ SOURCES = [os.path.join(CSRC, f) for f in ("csscan.cu", "forward_f32.cu", "forwa
                                            "backward_bf16.cu", "mimo_f32.cu", "mimo_bf16.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("scan_kernels.cuh", "nscan_kernels.cuh", "device_util.cuh",
                                            "decode_kernel.cuh", "backward_kernels.cuh", "ngrad_kernels.cuh", "mimo_kernels.cuh", "mscan_kernels.cuh",
+                                           "mgrad_kernels.cuh",
                                            "forward_launch.cuh", "backward_launch.cuh", "mimo_launch.cuh", "host_common.h")] + \
           [os.path.join(ROOT, "include", "csscan.h")]
 OUTPUT = os.path.join(HERE, "libcsscan.so")

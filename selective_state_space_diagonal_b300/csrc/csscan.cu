@@ -232,6 +232,46 @@ int mimo_impl(const MimoArgs& a, cudaStream_t st) {
   return a.dtype == CSSCAN_F32 ? mimo_f32(a, st) : mimo_bf16(a, st);
 }
 
+int mimo_backward_impl(const MimoBwdArgs& a, cudaStream_t st) {
+  if (a.mode != CSSCAN_MODE_EXP_EULER && a.mode != CSSCAN_MODE_EXP_TRAPEZOID) {
+    return a.mode == CSSCAN_MODE_ZOH ? CSSCAN_ERR_UNSUPPORTED : CSSCAN_ERR_INVALID_ARG;
+  }
+  if (a.dtype != CSSCAN_F32 && a.dtype != CSSCAN_BF16) return CSSCAN_ERR_INVALID_ARG;
+  if (a.B < 0 || a.L < 0 || a.H < 0 || a.P <= 0 || a.N <= 0) return CSSCAN_ERR_INVALID_ARG;
+  // arrays with no elements may be NULL (an empty tensor has no storage)
+  const bool rows = a.B > 0 && a.L > 0, heads = a.H > 0;
+  if (heads && (!a.A || !a.Dskip || !a.dA || !a.dDskip)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && (!a.Bm || !a.Cm || !a.theta || !a.dBm || !a.dCm || !a.dtheta)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && heads && (!a.x || !a.delta || !a.dy || !a.dx || !a.ddelta)) return CSSCAN_ERR_INVALID_ARG;
+  if (rows && a.mode == CSSCAN_MODE_EXP_TRAPEZOID && (!a.lam || !a.dlam)) return CSSCAN_ERR_INVALID_ARG;
+  if (a.N != 2 && a.N != 4 && a.N != 8 && a.N != 16 && a.N != 32) return CSSCAN_ERR_UNSUPPORTED;
+  if (a.P != 1 && a.P != 2 && a.P != 4 && a.P != 8) return CSSCAN_ERR_UNSUPPORTED;
+  if (a.B > 65535 || a.L > (int64_t(1) << 30) || a.H > (int64_t(1) << 30) ||
+      a.B * a.L * a.H * a.P > (int64_t(1) << 40) || a.B * a.L * a.N * a.P > (int64_t(1) << 40))
+    return CSSCAN_ERR_UNSUPPORTED;
+  const size_t s = a.dtype == CSSCAN_F32 ? 4 : 2;
+  if (!aligned(a.x, s) || !aligned(a.delta, s) || !aligned(a.Bm, 2 * s) || !aligned(a.Cm, 2 * s) ||
+      !aligned(a.theta, s) || (a.lam && !aligned(a.lam, s)) || !aligned(a.A, 4) || !aligned(a.Dskip, 4) ||
+      !aligned(a.dy, 4) || !aligned(a.dx, 4) || !aligned(a.ddelta, 4) || !aligned(a.dA, 4) || !aligned(a.dBm, 4) ||
+      !aligned(a.dCm, 4) || !aligned(a.dtheta, 4) || (a.dlam && !aligned(a.dlam, 4)) || !aligned(a.dDskip, 4))
+    return CSSCAN_ERR_MISALIGNED;
+  if (!rows || !heads) {
+    // no steps or no heads: every gradient is an empty sum
+    if (heads) {
+      CSSCAN_CUDA(cudaMemsetAsync(a.dA, 0, size_t(a.H * a.N) * 4, st));
+      CSSCAN_CUDA(cudaMemsetAsync(a.dDskip, 0, size_t(a.H * a.P) * 4, st));
+    }
+    if (rows) {
+      CSSCAN_CUDA(cudaMemsetAsync(a.dBm, 0, size_t(a.B * a.L * a.N * a.P) * 8, st));
+      CSSCAN_CUDA(cudaMemsetAsync(a.dCm, 0, size_t(a.B * a.L * a.N * a.P) * 8, st));
+      CSSCAN_CUDA(cudaMemsetAsync(a.dtheta, 0, size_t(a.B * a.L * a.N) * 4, st));
+      if (a.mode == CSSCAN_MODE_EXP_TRAPEZOID) CSSCAN_CUDA(cudaMemsetAsync(a.dlam, 0, size_t(a.B * a.L) * 4, st));
+    }
+    return CSSCAN_OK;
+  }
+  return a.dtype == CSSCAN_F32 ? mimo_backward_f32(a, st) : mimo_backward_bf16(a, st);
+}
+
 int backward_impl(const BwdArgs& a, cudaStream_t st) {
   if (a.mode != CSSCAN_MODE_EXP_EULER && a.mode != CSSCAN_MODE_EXP_TRAPEZOID && a.mode != CSSCAN_MODE_ZOH)
     return CSSCAN_ERR_INVALID_ARG;
@@ -406,6 +446,16 @@ int csscan_backward(const void* x, const void* delta, const float* A, const void
   BwdArgs a{x, delta, Bc, Cc, theta, lambda, A, Dskip, dy, dx, ddelta, dA, dBc, dCc, dtheta, dlambda, dDskip,
             B, L, D, N, mode, dtype};
   return backward_impl(a, stream);
+}
+
+int csscan_backward_mimo(const void* x, const void* delta, const float* A, const void* Bm, const void* Cm,
+                         const void* theta, const void* lambda, const float* Dskip, const float* dy, float* dx,
+                         float* ddelta, float* dA, float* dBm, float* dCm, float* dtheta, float* dlambda,
+                         float* dDskip, int64_t B, int64_t L, int64_t H, int64_t P, int64_t N, int mode, int dtype,
+                         cudaStream_t stream) {
+  MimoBwdArgs a{x, delta, Bm, Cm, theta, lambda, A, Dskip, dy, dx, ddelta, dA, dBm, dCm, dtheta, dlambda, dDskip,
+                B, L, H, P, N, mode, dtype};
+  return mimo_backward_impl(a, stream);
 }
 
 int csscan_get_device_status(cudaStream_t stream) {

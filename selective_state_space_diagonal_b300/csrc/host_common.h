@@ -66,6 +66,14 @@ struct MimoArgs {
   int mode, dtype;
 };
 
+struct MimoBwdArgs {
+  const void *x, *delta, *Bm, *Cm, *theta, *lam;
+  const float *A, *Dskip, *dy;
+  float *dx, *ddelta, *dA, *dBm, *dCm, *dtheta, *dlam, *dDskip;
+  int64_t B, L, H, P, N;
+  int mode, dtype;
+};
+
 struct BwdArgs {
   const void *x, *delta, *Bc, *Cc, *theta, *lam;
   const float *A, *Dskip, *dy;
@@ -107,5 +115,8 @@ int backward_bf16(const BwdArgs& a, cudaStream_t st);
 // MIMO scan of a validated, non-empty problem. Defined in mimo_f32.cu / mimo_bf16.cu.
 int mimo_f32(const MimoArgs& a, cudaStream_t st);
 int mimo_bf16(const MimoArgs& a, cudaStream_t st);
+// Backward of a validated, non-empty MIMO problem. Defined in mimo_f32.cu / mimo_bf16.cu.
+int mimo_backward_f32(const MimoBwdArgs& a, cudaStream_t st);
+int mimo_backward_bf16(const MimoBwdArgs& a, cudaStream_t st);
 
 }  // namespace csscan_host

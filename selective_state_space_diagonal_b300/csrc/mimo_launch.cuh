@@ -1,5 +1,5 @@
-// mimo_launch.cuh -- host side of csscan_forward_mimo, included by the per-dtype units
-// mimo_f32.cu / mimo_bf16.cu. Two kernel families:
+// mimo_launch.cuh -- host side of csscan_forward_mimo and csscan_backward_mimo, included by the
+// per-dtype units mimo_f32.cu / mimo_bf16.cu. The forward has two kernel families:
 //   mscan_kernel (mscan_kernels.cuh): staged tile copies, chunk carries as the forward scan;
 //     taken for N = 8, 16, 32 with P N <= 128 when the inputs meet the tile-copy rules (16-byte
 //     aligned x, dt and y, the (b, t) rows of x and dt whole multiples of 16 bytes);
@@ -10,6 +10,7 @@
 #include <cstring>
 
 #include "forward_launch.cuh"
+#include "mgrad_kernels.cuh"
 #include "mimo_kernels.cuh"
 #include "mscan_kernels.cuh"
 
@@ -246,6 +247,86 @@ template <typename Tin>
 int mimo_dispatch(const MimoArgs& a, cudaStream_t st) {
   const bool staged = mscan_takes(a);
   return a.mode == 0 ? dispatch_mimo_p<Tin, 0>(a, st, staged) : dispatch_mimo_p<Tin, 1>(a, st, staged);
+}
+
+// ----------------------------------------------------------------------------- backward
+// csscan_backward_mimo: e^{i theta} table, the checkpoint pass and the gradient pass of
+// mgrad_kernels.cuh (a thread per (b, head, state); the whole sequence per thread).
+template <typename Tin, int MODE, int P>
+int launch_mimo_backward(const MimoBwdArgs& a, cudaStream_t st) {
+  int dev = 0;
+  CSSCAN_CUDA(cudaGetDevice(&dev));
+  const int64_t N = a.N, S = (a.L + mgrad::SEG - 1) / mgrad::SEG;
+  const size_t rot_bytes = align_up(size_t(a.B * a.L * N) * sizeof(float2), 256);
+  const size_t ckpt_bytes = align_up(size_t(a.B * S * a.H * N) * sizeof(float2), 256);
+  WsEntry ws;
+  int rc = get_workspace(dev, st, 1, rot_bytes + ckpt_bytes, &ws);
+  if (rc != CSSCAN_OK) return rc;
+  char* rest = ws_rest(ws);
+  // gradients that are sums over several rows are accumulated and start at zero
+  CSSCAN_CUDA(cudaMemsetAsync(a.dA, 0, size_t(a.H * N) * 4, st));
+  CSSCAN_CUDA(cudaMemsetAsync(a.dBm, 0, size_t(a.B * a.L * N * a.P) * 8, st));
+  CSSCAN_CUDA(cudaMemsetAsync(a.dCm, 0, size_t(a.B * a.L * N * a.P) * 8, st));
+  CSSCAN_CUDA(cudaMemsetAsync(a.dtheta, 0, size_t(a.B * a.L * N) * 4, st));
+  if (MODE == 1) CSSCAN_CUDA(cudaMemsetAsync(a.dlam, 0, size_t(a.B * a.L) * 4, st));
+  CSSCAN_CUDA(cudaMemsetAsync(a.dDskip, 0, size_t(a.H * a.P) * 4, st));
+
+  mgrad::Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.x = a.x;
+  p.dt = a.delta;
+  p.Bm = a.Bm;
+  p.Cm = a.Cm;
+  p.lam = MODE == 1 ? a.lam : nullptr;
+  p.A = a.A;
+  p.Dskip = a.Dskip;
+  p.dy = a.dy;
+  p.rot = reinterpret_cast<const float2*>(rest);
+  p.ckpt = reinterpret_cast<float2*>(rest + rot_bytes);
+  p.dx = a.dx;
+  p.ddt = a.ddelta;
+  p.dA = a.dA;
+  p.dBm = a.dBm;
+  p.dCm = a.dCm;
+  p.dtheta = a.dtheta;
+  p.dlam = MODE == 1 ? a.dlam : nullptr;
+  p.dD = a.dDskip;
+  p.B = int(a.B);
+  p.L = int(a.L);
+  p.H = int(a.H);
+  p.N = int(N);
+  p.S = int(S);
+
+  const long long n_rot = (long long)a.B * a.L * N;
+  if (!grid_fits(n_rot)) return CSSCAN_ERR_UNSUPPORTED;
+  bwd::rot_kernel<Tin><<<unsigned((n_rot + 255) / 256), 256, 0, st>>>(a.theta, reinterpret_cast<float2*>(rest), n_rot);
+  CSSCAN_CUDA(cudaGetLastError());
+  const int64_t heads_per_block = mgrad::THREADS / N;
+  const dim3 grid{unsigned((a.H + heads_per_block - 1) / heads_per_block), unsigned(a.B)};
+  if (S > 1) {
+    mgrad::mckpt_kernel<Tin, MODE, P><<<grid, mgrad::THREADS, 0, st>>>(p);
+    CSSCAN_CUDA(cudaGetLastError());
+  }
+  const int smem = mgrad::MGradSmem<P>::bytes(int(N));
+  mgrad::mgrad_kernel<Tin, MODE, P><<<grid, mgrad::THREADS, unsigned(smem), st>>>(p);
+  CSSCAN_CUDA(cudaGetLastError());
+  return CSSCAN_OK;
+}
+
+template <typename Tin, int MODE>
+int mimo_backward_p(const MimoBwdArgs& a, cudaStream_t st) {
+  switch (a.P) {
+    case 1: return launch_mimo_backward<Tin, MODE, 1>(a, st);
+    case 2: return launch_mimo_backward<Tin, MODE, 2>(a, st);
+    case 4: return launch_mimo_backward<Tin, MODE, 4>(a, st);
+    case 8: return launch_mimo_backward<Tin, MODE, 8>(a, st);
+    default: return CSSCAN_ERR_UNSUPPORTED;
+  }
+}
+
+template <typename Tin>
+int mimo_backward_dispatch(const MimoBwdArgs& a, cudaStream_t st) {
+  return a.mode == 0 ? mimo_backward_p<Tin, 0>(a, st) : mimo_backward_p<Tin, 1>(a, st);
 }
 
 }  // namespace mimo_detail

@@ -75,6 +75,8 @@ def load_library(path: str = LIBRARY) -> ctypes.CDLL:
     lib.csscan_forward_mimo.argtypes = [vp] * 9 + [i64] * 5 + [i32, i32, vp]
     lib.csscan_forward_mimo.restype = i32
     lib.csscan_backward.argtypes = [vp] * 17 + [i64] * 4 + [i32, i32, vp]
+    lib.csscan_backward_mimo.argtypes = [vp] * 17 + [i64] * 5 + [i32, i32, vp]
+    lib.csscan_backward_mimo.restype = i32
     lib.csscan_backward.restype = i32
     _lib = lib
     return lib
@@ -190,6 +192,27 @@ def csscan_backward(x, delta, A, Bc, Cc, theta, lam, Dskip, dy, mode: int, strea
         _stream_handle(stream))
     if rc != CSSCAN_OK:
         raise CsscanError(rc, "csscan_backward")
+    return out
+
+
+def csscan_backward_mimo(x, delta, A, Bm, Cm, theta, lam, Dskip, dy, mode: int, stream=None, out=None) -> dict:
+    """Gradients of sum(dy * y) for csscan_forward_mimo from the zero state. Inputs as
+    csscan_forward_mimo plus dy (B, L, H, P) float32. Returns (or fills ``out``) dx (B,L,H,P),
+    ddelta (B,L,H), dA (H,N), dBm, dCm (B,L,N,P,2), dtheta (B,L,N), dlam (B,L) in the trapezoid
+    mode (None otherwise) and dDskip (H,P), float32 CUDA tensors."""
+    B, L, H, P = x.shape
+    N = A.shape[1]
+    if out is None:
+        f = lambda *shape: torch.empty(shape, dtype=torch.float32, device=x.device)
+        out = dict(dx=f(B, L, H, P), ddelta=f(B, L, H), dA=f(H, N), dBm=f(B, L, N, P, 2), dCm=f(B, L, N, P, 2),
+                   dtheta=f(B, L, N), dlam=f(B, L) if mode == CSSCAN_MODE_EXP_TRAPEZOID else None, dDskip=f(H, P))
+    rc = load_library().csscan_backward_mimo(
+        _ptr(x), _ptr(delta), _ptr(A), _ptr(Bm), _ptr(Cm), _ptr(theta), _ptr(lam), _ptr(Dskip), _ptr(dy),
+        _ptr(out["dx"]), _ptr(out["ddelta"]), _ptr(out["dA"]), _ptr(out["dBm"]), _ptr(out["dCm"]),
+        _ptr(out["dtheta"]), _ptr(out.get("dlam")), _ptr(out["dDskip"]), B, L, H, P, N, int(mode), _dtype_code(x),
+        _stream_handle(stream))
+    if rc != CSSCAN_OK:
+        raise CsscanError(rc, "csscan_backward_mimo")
     return out
 
 

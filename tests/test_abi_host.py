@@ -128,3 +128,19 @@ def test_mimo_rejects_bad_arguments_on_host(lib):
     assert mf(*args(mode=5)) == csscan.CSSCAN_ERR_INVALID_ARG
     assert mf(*args(mode=1, lam=None)) == csscan.CSSCAN_ERR_INVALID_ARG
     assert mf(*args(bm=A16 + 4)) == csscan.CSSCAN_ERR_MISALIGNED    # one float32 complex entry is 8 bytes
+
+
+def test_mimo_backward_rejects_bad_arguments_on_host(lib):
+    mb = lib.csscan_backward_mimo
+    def args(**k):
+        return [A16, A16, A16, k.get("bm", A16), A16, A16, k.get("lam", A16), A16, k.get("dy", A16),
+                A16, A16, A16, A16, A16, A16, k.get("dlam", A16), A16,
+                k.get("B", 2), 64, 4, k.get("P", 4), k.get("N", 16), k.get("mode", 0), k.get("dtype", 0), None]
+    assert mb(*args(P=3)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert mb(*args(N=64)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert mb(*args(mode=2)) == csscan.CSSCAN_ERR_UNSUPPORTED          # no zero-order hold in MIMO
+    assert mb(*args(B=70000)) == csscan.CSSCAN_ERR_UNSUPPORTED
+    assert mb(*args(mode=5)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert mb(*args(mode=1, dlam=None)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert mb(*args(dy=None)) == csscan.CSSCAN_ERR_INVALID_ARG
+    assert mb(*args(bm=A16 + 4)) == csscan.CSSCAN_ERR_MISALIGNED       # one float32 complex entry is 8 bytes

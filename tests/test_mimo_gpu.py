@@ -144,3 +144,67 @@ def test_mimo_staged_long_decoupled():
     w = BASE.with_shape(B=1, L=20000, H=32, P=4, N=16, mode=1, dtype="bf16", dt_lo=1e-4, dt_hi=1e-2)
     inp = wl.generate_mimo(w)
     check(inp, run(inp), "staged long", h=np.array([0, 17, 31]))
+
+
+# ---------------------------------------------------------------------------- backward
+MGRADS = ("dx", "ddelta", "dA", "dBm", "dCm", "dtheta", "dlam", "dDskip")
+MGRAD_TOL = 1e-3   # the single-input backward's bound (tests/test_backward_gpu.py), same reasoning
+
+
+def mimo_backward_case(w: wl.MimoWorkload, name: str, seed: int):
+    """csscan_backward_mimo against oracle.backward_mimo, every gradient tensor by
+    e_g = max|g - g_ref| / max|g_ref|."""
+    inp = wl.generate_mimo(w)
+    dev = to_device(inp)
+    dy = np.random.default_rng(seed).standard_normal((w.B, w.L, w.H, w.P), dtype=np.float32)
+    g = csscan.csscan_backward_mimo(dev["x"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], dev["theta"], dev["lam"],
+                                    dev["Dskip"], torch.from_numpy(dy).cuda(), w.mode)
+    assert csscan.csscan_get_device_status() == csscan.CSSCAN_OK
+    f = wl.widen_mimo(inp)
+    r = oracle.backward_mimo(f["x"], f["delta"], f["A"], f["Bm"], f["Cm"], f["theta"], f["lam"], f["Dskip"],
+                             dy.astype(np.float64), w.mode)
+    for k in MGRADS:
+        if r.get(k) is None:
+            assert g.get(k) is None, f"{name}: {k} should be absent"
+            continue
+        v = g[k].cpu().numpy().astype(np.float64)
+        if k in ("dBm", "dCm"):
+            v = v[..., 0] + 1j * v[..., 1]
+        assert np.isfinite(v).all(), f"{name}: {k} has non-finite or unwritten entries"
+        e = float(np.abs(v - r[k]).max()) / max(float(np.abs(r[k]).max()), 1e-30)
+        assert e <= MGRAD_TOL, f"{name}: {k} e={e:.3e} > {MGRAD_TOL}"
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8])
+@pytest.mark.parametrize("N", [2, 4, 8, 16, 32])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_mimo_backward_matches_oracle(P, N, mode):
+    """Ragged sequence (5 segments of 8 plus 5 steps), a partial block of heads, both dtypes."""
+    for (B, L, H, dtype) in [(2, 45, 5, "f32"), (1, 19, 3, "bf16")]:
+        w = BASE.with_shape(B=B, L=L, H=H, P=P, N=N, mode=mode, dtype=dtype, seed=BASE.seed + 13 * P + 5 * N + L)
+        mimo_backward_case(w, f"bwd P{P}:N{N}:m{mode}:{dtype}:{B}x{L}x{H}", seed=17 + P + N)
+
+
+def test_mimo_backward_longer_and_many_heads():
+    """A longer sequence (the adjoint carried over 600 steps) and more heads than one block."""
+    for mode in (0, 1):
+        w = BASE.with_shape(B=1, L=600, H=40, P=4, N=16, mode=mode, dtype="bf16", seed=BASE.seed + 601 + mode)
+        mimo_backward_case(w, f"bwd long m{mode}", seed=23 + mode)
+
+
+def test_mimo_backward_rejects_zoh_and_handles_empty():
+    w = BASE.with_shape(B=1, L=16, H=2, P=4, N=8, mode=1, dtype="f32")
+    dev = to_device(wl.generate_mimo(w))
+    dy = torch.zeros((1, 16, 2, 4), device="cuda")
+    with pytest.raises(csscan.CsscanError) as e:
+        csscan.csscan_backward_mimo(dev["x"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], dev["theta"], None,
+                                    dev["Dskip"], dy, 2)
+    assert e.value.status == csscan.CSSCAN_ERR_UNSUPPORTED
+    # no steps: the summed gradients are zero
+    z = lambda *s: torch.zeros(s, device="cuda")
+    out = dict(dx=z(1, 0, 2, 4), ddelta=z(1, 0, 2), dA=torch.full((2, 8), 5.0, device="cuda"), dBm=z(1, 0, 8, 4, 2),
+               dCm=z(1, 0, 8, 4, 2), dtheta=z(1, 0, 8), dlam=z(1, 0), dDskip=torch.full((2, 4), 5.0, device="cuda"))
+    csscan.csscan_backward_mimo(z(1, 0, 2, 4), z(1, 0, 2), dev["A"], z(1, 0, 8, 4, 2), z(1, 0, 8, 4, 2), z(1, 0, 8),
+                                z(1, 0), dev["Dskip"], z(1, 0, 2, 4), 1, out=out)
+    torch.cuda.synchronize()
+    assert float(out["dA"].abs().max()) == 0.0 and float(out["dDskip"].abs().max()) == 0.0
