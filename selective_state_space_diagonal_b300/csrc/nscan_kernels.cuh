@@ -111,34 +111,50 @@ __global__ void __launch_bounds__(256) ntable_kernel(TableParams p) {
   // E_t by a shuffle sum over the N lanes of (b, s), neighbours in a warp when N <= 32
   const bool lane_sum = MODE == 1 && p.N <= 32;
   const unsigned gmask = p.N >= 32 ? 0xffffffffu : (((1u << p.N) - 1u) << ((threadIdx.x & 31) & ~(p.N - 1)));
-  for (int t = t0; t < t1; ++t) {
-    const int64_t tn = (int64_t(b) * p.L + t) * p.N + n;
-    phi += load_in<Tin>(th, tn);
-    sincosf(phi, &sn, &cs);
-    if (((t - t0) & 7) == 7) {
-      rr[((t - t0) >> 3) * 2 * p.N] = cs;
-      rr[((t - t0) >> 3) * 2 * p.N + 1] = sn;
+  // groups of 8 steps: every load of a group is issued before its arithmetic, so that the
+  // group's memory latencies overlap (the phase itself is a running sum)
+  for (int tg = t0; tg < t1; tg += 8) {
+    float ths[8], brs[8], bis[8], crs[8], cis[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t tn = (int64_t(b) * p.L + min(tg + i, t1 - 1)) * p.N + n;
+      ths[i] = load_in<Tin>(th, tn);
+      brs[i] = load_in<Tin>(Bc, 2 * tn);
+      bis[i] = load_in<Tin>(Bc, 2 * tn + 1);
+      crs[i] = load_in<Tin>(Cc, 2 * tn);
+      cis[i] = load_in<Tin>(Cc, 2 * tn + 1);
     }
-    const float br = load_in<Tin>(Bc, 2 * tn), bi = load_in<Tin>(Bc, 2 * tn + 1);
-    const float cr = load_in<Tin>(Cc, 2 * tn), ci = load_in<Tin>(Cc, 2 * tn + 1);
-    const float btr = cs * br + sn * bi;   // Re(e^{-i Phi} Bc)
-    const float bti = cs * bi - sn * br;   // Im(e^{-i Phi} Bc)
-    float* row = p.tab + CSSCAN_BCK(p.hdr, int64_t(b) * p.L + t, int64_t(p.B) * p.L, 20) * (p.planes * W);
-    row[idx] = btr;
-    row[idx + 2] = bti;
-    row[W + idx] = cs * cr - sn * ci;        // Re(e^{+i Phi} Cc)
-    row[W + idx + 2] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
-    if (p.planes == 3) {
-      row[2 * W + idx] = -btr;
-      row[2 * W + idx + 2] = -bti;
-    }
-    if (lane_sum) {
-      float E = cr * br - ci * bi;
-      for (int o = p.N / 2; o >= 1; o >>= 1) E += __shfl_xor_sync(gmask, E, o);
-      if (n == 0) {
-        const int64_t tb = int64_t(b) * p.L + t;
-        const float mu = (t + 1 < p.L) ? 1.f - load_in<Tin>(lam, tb + 1) : 0.f;
-        reinterpret_cast<float4*>(p.aux)[tb] = make_float4(load_in<Tin>(lam, tb), mu, E, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = tg + i;
+      if (t >= t1) break;
+      phi += ths[i];
+      sincosf(phi, &sn, &cs);
+      if (((t - t0) & 7) == 7) {
+        rr[((t - t0) >> 3) * 2 * p.N] = cs;
+        rr[((t - t0) >> 3) * 2 * p.N + 1] = sn;
+      }
+      const float br = brs[i], bi = bis[i];
+      const float cr = crs[i], ci = cis[i];
+      const float btr = cs * br + sn * bi;   // Re(e^{-i Phi} Bc)
+      const float bti = cs * bi - sn * br;   // Im(e^{-i Phi} Bc)
+      float* row = p.tab + CSSCAN_BCK(p.hdr, int64_t(b) * p.L + t, int64_t(p.B) * p.L, 20) * (p.planes * W);
+      row[idx] = btr;
+      row[idx + 2] = bti;
+      row[W + idx] = cs * cr - sn * ci;        // Re(e^{+i Phi} Cc)
+      row[W + idx + 2] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
+      if (p.planes == 3) {
+        row[2 * W + idx] = -btr;
+        row[2 * W + idx + 2] = -bti;
+      }
+      if (lane_sum) {
+        float E = cr * br - ci * bi;
+        for (int o = p.N / 2; o >= 1; o >>= 1) E += __shfl_xor_sync(gmask, E, o);
+        if (n == 0) {
+          const int64_t tb = int64_t(b) * p.L + t;
+          const float mu = (t + 1 < p.L) ? 1.f - load_in<Tin>(lam, tb + 1) : 0.f;
+          reinterpret_cast<float4*>(p.aux)[tb] = make_float4(load_in<Tin>(lam, tb), mu, E, 0.f);
+        }
       }
     }
   }

@@ -161,49 +161,65 @@ __global__ void __launch_bounds__(256) table_kernel(TableParams p) {
   const bool lane_sum = MODE == 1 && p.N <= 32;
   const unsigned gmask = p.N >= 32 ? 0xffffffffu : (((1u << p.N) - 1u) << ((threadIdx.x & 31) & ~(p.N - 1)));
   const Tin* lam = static_cast<const Tin*>(p.lam);
-  for (int t = t0; t < t1; ++t) {
-    const int64_t tn = (int64_t(b) * p.L + t) * p.n_full + p.n_off + n;   // this state in the inputs
-    phi += load_in<Tin>(th, tn);
-    sincosf(phi, &sn, &cs);
-    if (((t - t0) & 7) == 7) {
-      rr[((t - t0) >> 3) * 2 * p.N] = cs;
-      rr[((t - t0) >> 3) * 2 * p.N + 1] = sn;
+  // groups of 8 steps: every load of a group is issued before its arithmetic, so that the
+  // group's memory latencies overlap (the phase itself is a running sum)
+  for (int tg = t0; tg < t1; tg += 8) {
+    float ths[8], brs[8], bis[8], crs[8], cis[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t tn = (int64_t(b) * p.L + min(tg + i, t1 - 1)) * p.n_full + p.n_off + n;   // this state in the inputs
+      ths[i] = load_in<Tin>(th, tn);
+      brs[i] = load_in<Tin>(Bc, 2 * tn);
+      bis[i] = load_in<Tin>(Bc, 2 * tn + 1);
+      crs[i] = load_in<Tin>(Cc, 2 * tn);
+      cis[i] = load_in<Tin>(Cc, 2 * tn + 1);
     }
-    const float br = load_in<Tin>(Bc, 2 * tn), bi = load_in<Tin>(Bc, 2 * tn + 1);
-    const float cr = load_in<Tin>(Cc, 2 * tn), ci = load_in<Tin>(Cc, 2 * tn + 1);
-    constexpr int TW = MODE == 2 ? 8 : 4;
-    float* row = p.tab + (int64_t(b) * p.L + t) * (TW * p.N) + q * 2 * TW;
-    const float btr = cs * br + sn * bi;   // Re(e^{-i Phi} Bc)
-    const float bti = cs * bi - sn * br;   // Im(e^{-i Phi} Bc)
-    if (MODE == 2) {
-      // e^{i theta} - 1 without cancellation: cos theta - 1 = -2 sin^2(theta / 2)
-      const float th_t = load_in<Tin>(th, tn);
-      float sh, chh;
-      sincosf(0.5f * th_t, &sh, &chh);
-      const float cm1 = -2.f * sh * sh, s1 = 2.f * sh * chh, c1 = 1.f + cm1;
-      row[odd] = LOG2E_F * (btr * c1 - bti * s1);        // beta = Bt e^{i theta}
-      row[2 + odd] = LOG2E_F * (btr * s1 + bti * c1);
-      row[8 + odd] = LOG2E_F * (btr * cm1 - bti * s1);   // delta = Bt (e^{i theta} - 1)
-      row[10 + odd] = LOG2E_F * (btr * s1 + bti * cm1);
-      const float tq = LOG2E_F * th_t;
-      row[12 + odd] = tq;
-      row[14 + odd] = fmaf(tq, tq, ZOH_TAU);
-    } else {
-      row[odd] = btr;
-      row[2 + odd] = bti;
-    }
-    row[4 + odd] = cs * cr - sn * ci;    // Re(e^{+i Phi} Cc)
-    row[6 + odd] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
-    if (lane_sum) {
-      float E = cr * br - ci * bi;
-      for (int o = p.N / 2; o >= 1; o >>= 1) E += __shfl_xor_sync(gmask, E, o);
-      if (n == 0) {
-        const int64_t tb = int64_t(b) * p.L + t;
-        const float lt = load_in<Tin>(lam, tb);
-        const float mu = (t + 1 < p.L) ? 1.f - load_in<Tin>(lam, tb + 1) : 0.f;
-        float4* a = reinterpret_cast<float4*>(p.aux) + 2 * tb;
-        a[0] = make_float4(lt, lt, mu, mu);
-        a[1] = make_float4(E, E, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = tg + i;
+      if (t >= t1) break;
+      const float th_t = ths[i];
+      phi += th_t;
+      sincosf(phi, &sn, &cs);
+      if (((t - t0) & 7) == 7) {
+        rr[((t - t0) >> 3) * 2 * p.N] = cs;
+        rr[((t - t0) >> 3) * 2 * p.N + 1] = sn;
+      }
+      const float br = brs[i], bi = bis[i];
+      const float cr = crs[i], ci = cis[i];
+      constexpr int TW = MODE == 2 ? 8 : 4;
+      float* row = p.tab + (int64_t(b) * p.L + t) * (TW * p.N) + q * 2 * TW;
+      const float btr = cs * br + sn * bi;   // Re(e^{-i Phi} Bc)
+      const float bti = cs * bi - sn * br;   // Im(e^{-i Phi} Bc)
+      if (MODE == 2) {
+        // e^{i theta} - 1 without cancellation: cos theta - 1 = -2 sin^2(theta / 2)
+        float sh, chh;
+        sincosf(0.5f * th_t, &sh, &chh);
+        const float cm1 = -2.f * sh * sh, s1 = 2.f * sh * chh, c1 = 1.f + cm1;
+        row[odd] = LOG2E_F * (btr * c1 - bti * s1);        // beta = Bt e^{i theta}
+        row[2 + odd] = LOG2E_F * (btr * s1 + bti * c1);
+        row[8 + odd] = LOG2E_F * (btr * cm1 - bti * s1);   // delta = Bt (e^{i theta} - 1)
+        row[10 + odd] = LOG2E_F * (btr * s1 + bti * cm1);
+        const float tq = LOG2E_F * th_t;
+        row[12 + odd] = tq;
+        row[14 + odd] = fmaf(tq, tq, ZOH_TAU);
+      } else {
+        row[odd] = btr;
+        row[2 + odd] = bti;
+      }
+      row[4 + odd] = cs * cr - sn * ci;    // Re(e^{+i Phi} Cc)
+      row[6 + odd] = -(cs * ci + sn * cr); // -Im(e^{+i Phi} Cc)
+      if (lane_sum) {
+        float E = cr * br - ci * bi;
+        for (int o = p.N / 2; o >= 1; o >>= 1) E += __shfl_xor_sync(gmask, E, o);
+        if (n == 0) {
+          const int64_t tb = int64_t(b) * p.L + t;
+          const float lt = load_in<Tin>(lam, tb);
+          const float mu = (t + 1 < p.L) ? 1.f - load_in<Tin>(lam, tb + 1) : 0.f;
+          float4* a = reinterpret_cast<float4*>(p.aux) + 2 * tb;
+          a[0] = make_float4(lt, lt, mu, mu);
+          a[1] = make_float4(E, E, 0.f, 0.f);
+        }
       }
     }
   }
