@@ -19,8 +19,9 @@
 //   mckpt_kernel  the forward recurrence, storing the state before every 8-step segment;
 //   mgrad_kernel  per segment, last to first: regenerate the segment's states from its
 //                 checkpoint, walk it backwards; sums over n of a (t, h) by shuffles across the
-//                 head's lanes, sums over h of a (t, n) through shared memory once per segment and
-//                 then one atomic add per value and block.
+//                 head's lanes; sums over h of a (t, n) by shuffles across the warp's heads, then
+//                 over the block's warps through shared memory once per segment, then one atomic
+//                 add per value and block.
 // e^{i theta} comes from bwd::rot_kernel's table (B, L, N), shared by every head.
 #pragma once
 
@@ -137,6 +138,13 @@ __global__ void __launch_bounds__(THREADS) mgrad_kernel(const Params p) {
   // the N lanes of this head within the warp (N <= 32 divides 32)
   const unsigned gmask = N >= 32 ? 0xffffffffu : (((1u << N) - 1u) << (lane & ~unsigned(N - 1)));
   const float Ad = valid ? p.A[(long long)hh * N + n] : 0.f;
+  // sum over the 32 / N heads of this warp (lanes n of every head), at every lane
+  auto head_sum = [&](float v) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1)
+      if (o >= N) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+  };
   const float a2 = Ad * LOG2E;
   for (int k = tid; k < SEG * N * P * 4 + SEG * N + SEG; k += THREADS) s_mem[k] = 0.f;
 
@@ -235,19 +243,24 @@ __global__ void __launch_bounds__(THREADS) mgrad_kernel(const Params p) {
       for (int q = 0; q < P; ++q) {
         const float br = load_in<Tin>(BM, 2 * q), bi = load_in<Tin>(BM, 2 * q + 1);
         dxs[q] = br * Gvr + bi * Gvi;   // Re(conj(Bm) G(v))
-        float* sb = s_bc + ((i * N + n) * P + q) * 4;
-        if (valid) {
-          atomicAdd(sb + 0, xs[q] * Gvr);
-          atomicAdd(sb + 1, xs[q] * Gvi);
-          atomicAdd(sb + 2, dys[q] * hr);    // dy conj(h)
-          atomicAdd(sb + 3, -dys[q] * hi);
+        // dBm (x G(v)) and dCm (dy conj(h)) summed over the warp's heads first (an absent
+        // head contributes zeros), then one shared-memory add per warp
+        const float bmr = head_sum(xs[q] * Gvr), bmi = head_sum(xs[q] * Gvi);
+        const float cmr = head_sum(dys[q] * hr), cmi = head_sum(-dys[q] * hi);
+        if (lane < unsigned(N)) {
+          float* sb = s_bc + ((i * N + n) * P + q) * 4;
+          atomicAdd(sb + 0, bmr);
+          atomicAdd(sb + 1, bmi);
+          atomicAdd(sb + 2, cmr);
+          atomicAdd(sb + 3, cmi);
         }
       }
       const float Gzr = a.x * Gar + a.y * Gai;   // conj(a) G(a)
       const float Gzi = a.x * Gai - a.y * Gar;
       dA_acc = fmaf(dtt, Gzr, dA_acc);
       float dz = Ad * Gzr;
-      if (valid) atomicAdd(&s_th[i * N + n], Gzi);
+      const float gth = head_sum(Gzi);
+      if (lane < unsigned(N)) atomicAdd(&s_th[i * N + n], gth);
       // sums over the head's N lanes: dc1, dc2, dz and dx[p]
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
