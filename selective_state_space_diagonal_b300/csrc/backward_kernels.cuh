@@ -100,12 +100,14 @@ __global__ void __launch_bounds__(256) rot_kernel(const void* theta, float2* rot
 }
 
 // Zero-order hold: E(z) = (e^z - 1) / z (gam = dt E) and, with DERIV, E'(z) = (e^z - E(z)) / z,
-// for z = v + i th with (c, s) = (cos th, sin th). Where |z| < 0.05 both come from their power
-// series, sum z^k / (k+1)! and sum (k+1) z^k / (k+2)!, to z^4 (the first omitted terms are below
-// 5e-10 relative); elsewhere from the closed forms, with e^z - 1 = (e^v - 1) c + (c - 1) + i e^v s
-// formed without cancellation (c - 1 = -s^2 / (1 + c) where c > 0).
+// for z = v + i th with (c, s) = (cos th, sin th) and r = e^v (the decay's magnitude, from the
+// hardware 2^x). Where |z| < 0.05 both come from their power series, sum z^k / (k+1)! and
+// sum (k+1) z^k / (k+2)!, to z^4 (the first omitted terms are below 5e-10 relative); elsewhere
+// from the closed forms, with e^z - 1 = (r - 1) c + (c - 1) + i r s and c - 1 = -s^2 / (1 + c)
+// where c > 0: there |e^z - 1| is at least about |z| / 2 >= 0.025, so the absolute error of r - 1
+// (a few 1e-7) stays below 2e-5 of it.
 template <bool DERIV>
-__device__ __forceinline__ void zoh_factor(float v, float th, float c, float s, float2& E, float2& dE) {
+__device__ __forceinline__ void zoh_factor(float v, float th, float c, float s, float r, float2& E, float2& dE) {
   const float z2 = fmaf(v, v, th * th);
   if (z2 < 0.0025f) {
     const float k1[5] = {1.f, 1.f / 2.f, 1.f / 6.f, 1.f / 24.f, 1.f / 120.f};
@@ -125,10 +127,10 @@ __device__ __forceinline__ void zoh_factor(float v, float th, float c, float s, 
     E = make_float2(er, ei);
     dE = make_float2(dr, di);
   } else {
-    const float em1 = expm1f(v), ev = em1 + 1.f;
+    const float em1 = r - 1.f, ev = r;
     const float cm1 = c > 0.f ? -s * s / (1.f + c) : c - 1.f;
     const float nr = fmaf(em1, c, cm1), ni = ev * s;   // e^z - 1
-    const float inv = 1.f / z2;                        // 1 / z = (v - i th) / |z|^2
+    const float inv = __frcp_rn(z2);                   // 1 / z = (v - i th) / |z|^2
     E = make_float2(fmaf(nr, v, ni * th) * inv, fmaf(ni, v, -nr * th) * inv);
     if (DERIV) {
       const float dr = fmaf(ev, c, -E.x), di = fmaf(ev, s, -E.y);   // e^z - E
@@ -183,7 +185,7 @@ struct FwdStep {
           ui = w * bis[i];
         } else if (MODE == 2) {
           float2 E, dE;
-          zoh_factor<false>(ds[i] * A, ths[i], ros[i].x, ros[i].y, E, dE);
+          zoh_factor<false>(ds[i] * A, ths[i], ros[i].x, ros[i].y, r, E, dE);
           const float w = ds[i] * xs[i];
           const float gr = w * E.x, gi = w * E.y;   // x gam
           ur = fmaf(gr, brs[i], -gi * bis[i]);
@@ -593,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_ke
               ui = w * q.w;
             } else if (MODE == 2) {
               float2 E, dE;
-              zoh_factor<false>(dtt * Ad, s_th[i + 1][n], q.x, q.y, E, dE);
+              zoh_factor<false>(dtt * Ad, s_th[i + 1][n], q.x, q.y, r, E, dE);
               const float w = dtt * xt;
               const float gr = w * E.x, gi = w * E.y;   // x gam
               ur = fmaf(gr, q.z, -gi * q.w);
@@ -655,7 +657,7 @@ __global__ void __launch_bounds__(THREADS, GradOcc<MODE, N>::MIN_BLOCKS) grad_ke
             gdt = xt * P;
           } else if (MODE == 2) {
             float2 E, dE;
-            zoh_factor<true>(dtt * Ad, s_th[i + 1][n], q.x, q.y, E, dE);
+            zoh_factor<true>(dtt * Ad, s_th[i + 1][n], q.x, q.y, r, E, dE);
             const float Pi = br * gi - bi * gr;        // conj(Bc) ghat = P + i Pi
             const float mr = dtt * E.x, mi = dtt * E.y;  // gam
             acc[i][0] = fmaf(xt, fmaf(mr, gr, mi * gi), acc[i][0]);   // dBc += x conj(gam) ghat
