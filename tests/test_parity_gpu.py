@@ -209,6 +209,22 @@ def test_zoh_rejected_where_unsupported():
     assert e.value.status == csscan.CSSCAN_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("carry", [1, 2])
+def test_zoh_parts_take_the_options(carry):
+    """N = 64 runs as four 16-state parts: forced serial and decoupled chunks of 64 steps reach
+    every part, and the scan events bracket the parts (recorded, positive interval)."""
+    w = wl.WORKLOADS["zoh_bf16_batch"].with_shape(B=2, L=300, D=16, N=64, dtype="f32", seed=0x5EED4000 + carry)
+    inp = wl.generate(w)
+    dev = gu.to_device(inp)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    ev1.record()   # creates the CUDA events; the library records them again by handle
+    y = gu.run_gpu(dev, w.mode, carry=carry, chunk_len=64, scan_begin=ev0, scan_end=ev1)
+    torch.cuda.synchronize()
+    assert ev0.elapsed_time(ev1) > 0.0
+    check(inp, y, f"zoh:parts:carry{carry}")
+
+
 def test_zoh_n64_rows_rich():
     """N = 64 zero-order hold with enough rows for serial chunks (the two-box table rows on every
     stage of the ring), sampled rows against the oracle."""

@@ -41,6 +41,7 @@ def rel_diff(a: torch.Tensor, b: torch.Tensor) -> float:
     ("trap_bf16_batch", dict(B=2, L=2048, D=256)),
     ("euler_f32_mamba1", dict(B=1, L=1000, D=64)),
     ("zoh_bf16_batch", dict(B=2, L=2048, D=256)),
+    ("zoh_bf16_batch", dict(B=1, L=700, D=64, N=64)),   # four 16-state parts through the fixed scratch
 ])
 def test_noalloc_matches_forward_twice(name, shape):
     w = wl.WORKLOADS[name].with_shape(**shape)
