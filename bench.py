@@ -558,7 +558,8 @@ def config_entry(label, w, t, steps, hbm_peak) -> dict:
             "scan_ms": 1e3 * scan_s, "step_ms": 1e3 * step_s, "value": w.elements / step_s / 1e9, "unit": UNIT,
             "scan_gelem_s": w.elements / scan_s / 1e9,
             "hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-                    "frac_of_nominal": gbs / HBM_NOMINAL_GBS},
+                    "frac_of_nominal": gbs / HBM_NOMINAL_GBS,
+                    "traffic": traffic_from_profiles(w.name, scan_kernel_name(w))},
             "alu": alu_roofline(ALU_OPS_PER_ELEM[w.mode], w.elements, scan_s, t["clocks"]),
             "kernel": scan_kernel_name(w), "clocks": t["clocks"], "gpu_launches": launches_per_step(w) * steps}
 
@@ -920,7 +921,8 @@ def measure_mimo_config(label, name, args, stream, local, scratch, hbm_peak) -> 
     rec = {"config": label, **mimo_config(w), "l2": l2_note(w, t["flush"]), "steps": steps,
            "call_ms": 1e3 * mean_s, "value": w.elements / mean_s / 1e9, "unit": UNIT,
            "hbm": {"achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
-                   "frac_of_nominal": gbs / HBM_NOMINAL_GBS},
+                   "frac_of_nominal": gbs / HBM_NOMINAL_GBS,
+                   "traffic": traffic_from_profiles(w.name, "mscan_kernel")},
            "alu": alu_roofline(mimo_alu_ops_per_elem(w.P, w.mode), w.elements, mean_s, t["clocks"]),
            "kernel": "mscan_kernel (+ table pass)", "clocks": t["clocks"],
            "gpu_launches": mimo_launches(w, nsm) * steps, "parity": mimo_parity(inp, y)}
