@@ -95,3 +95,12 @@ def test_parity_errors():
     e, e_ssm = bench.parity_errors(y, y_ref, x, d)
     assert e == pytest.approx(0.01 / 4.0)
     assert e_ssm == pytest.approx(0.01 / 2.0)   # the state-space part y - Dskip x peaks at 2
+
+
+def test_shape_overrides():
+    """--batch, --length and --states change only the named dimensions of the workload."""
+    a = bench.parse_args(["--workload", "zoh_bf16_batch", "--states", "64", "--length", "512"])
+    w = bench.selected_workload(a)
+    base = wl.WORKLOADS["zoh_bf16_batch"]
+    assert (w.B, w.L, w.D, w.N, w.mode, w.dtype) == (base.B, 512, base.D, 64, base.mode, base.dtype)
+    assert bench.selected_workload(bench.parse_args([])) == wl.WORKLOADS[bench.DEFAULT_WORKLOAD]
