@@ -147,12 +147,13 @@ def test_backward_zoh_small_exponents_and_chunks():
     compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), "zoh long")
 
 
-def test_backward_single_step_and_short():
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_backward_single_step_and_short(mode):
     for L in (1, 7, 8, 9):
-        w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=1, L=L, D=16, N=16, dtype="f32")
+        w = wl.WORKLOADS["trap_bf16_batch"].with_shape(B=1, L=L, D=16, N=16, mode=mode, dtype="f32")
         inp = wl.generate(w)
         dy = make_dy(w, seed=L)
-        compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"L{L}")
+        compare(widen_grads(gpu_backward(inp, dy)), oracle_backward(inp, dy), f"L{L}:m{mode}")
 
 
 def test_backward_empty_sequence_zeroes_sums():
